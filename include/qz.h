@@ -1,0 +1,235 @@
+/*
+ * qz.h - C ABI of libqz: weight-only quantized dequant-GEMV/GEMM for one GB300.
+ *
+ * The operations follow three web pages about serving a decoder LLM from
+ * compressed weights:
+ *   [ELG]  "Open Origin - ELG Stream Layer" (INT8 layer paging),
+ *   [OTF]  "On-The-Fly Weight Synthesizer (OTF-LLM Engine)" (outlier-aware INT4),
+ *   [NTR]  "NTransformer" summary (tiered layer streaming with custom GEMV).
+ * Each entry point below names the section of the page that defines it.
+ *
+ * Conventions for every call
+ *   - Pointers are DEVICE pointers unless the comment says host.
+ *   - The caller allocates and owns every buffer.  The library never allocates
+ *     or frees device memory and keeps no pointer to caller memory between
+ *     calls (the pager keeps the pointers it is given until it is destroyed).
+ *   - fp16 data is passed as qz_half: the bit pattern of an IEEE-754 binary16.
+ *   - Matrices are row-major.  ld* is the distance between rows in ELEMENTS
+ *     of the array's own type (bytes for int8/uint8 arrays).
+ *   - Every call that launches GPU work is asynchronous on the given stream
+ *     (NULL = the legacy default stream).  Outputs are valid once the stream
+ *     has reached the call.  Calls that overlap on the GPU and write the same
+ *     output race.
+ *   - Arguments are validated on the host before anything is enqueued: a call
+ *     that returns an error has enqueued nothing (QZ_ERR_CUDA excepted: the
+ *     launch itself failed, and cudaGetLastError's code is kept in
+ *     qz_last_cuda_error(), per host thread).
+ *   - Alignment: every device pointer of a matrix or vector must be 16-byte
+ *     aligned, and every ld* must make rows 16-byte multiples (ld % 8 == 0 for
+ *     fp16, ld % 16 == 0 for int8/uint8).  Violations return QZ_ERR_ALIGNMENT.
+ *   - Inputs must be finite.  Non-finite weights or profiles give unspecified
+ *     (but memory-safe) results.
+ *   - No exception, abort or device trap is ever raised by the library.
+ */
+#ifndef QZ_H
+#define QZ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *qz_stream; /* the same type as cudaStream_t */
+typedef uint16_t qz_half;              /* IEEE-754 binary16 bit pattern */
+
+typedef enum {
+  QZ_OK = 0,
+  QZ_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size */
+  QZ_ERR_ALIGNMENT = 2,   /* pointer or leading dimension breaks the 16-B rule */
+  QZ_ERR_UNSUPPORTED = 3, /* valid but outside what the kernels handle (see call) */
+  QZ_ERR_CUDA = 4,        /* a CUDA launch/enqueue failed; see qz_last_cuda_error */
+  QZ_ERR_IO = 5,          /* pager host-side failure (copy enqueue, event) */
+  QZ_ERR_DATA = 6         /* data check failed (qz_check_perm) */
+} qz_status;
+
+/* Human-readable name of a status; never NULL. */
+const char *qz_status_string(qz_status st);
+/* Library version as major*10000 + minor*100 + patch. */
+int qz_version(void);
+/* The cudaError_t of the last QZ_ERR_CUDA returned on this host thread. */
+int qz_last_cuda_error(void);
+
+/* Largest batch the GEMM entry points accept. */
+#define QZ_MAX_BATCH 64
+/* Largest number of matrices in one grouped launch. */
+#define QZ_MAX_GROUP 4
+
+/* ======================================================================
+ * INT8, one scale per tensor  [ELG "Technical Architecture > INT8
+ * Quantization & Direct Mapping": scale = max|W| / 127, q = round(W/scale);
+ * "FP16 On-The-Fly GPU Reconstruction": w = q * scale]
+ * ====================================================================== */
+
+/* Quantize an fp16 matrix W [N][ldw] to q [N][ldq] int8 and one fp32 scale.
+ *   scale = fp32(max |W|) / 127 (IEEE fp32 divide, round to nearest even);
+ *   q     = clamp(rint(fp32(W) / scale), -127, 127), rint = half-to-even;
+ *   an all-zero W gives scale = 0 and q = 0.
+ * Columns K..ldq-1 of q are written as 0.  *scale is used as the running
+ * maximum while the call runs, so no other work may read it until the
+ * stream has passed this call.  N, K >= 1; ldw >= K; ldq >= K. */
+qz_status qz_quantize_int8(const qz_half *W, int64_t N, int64_t K, int64_t ldw,
+                           int8_t *q, int64_t ldq, float *scale, qz_stream s);
+
+/* A quantized INT8 matrix as the GEMV calls read it (a host struct holding
+ * device pointers).  Bytes q[i][K..ldq) are never used in a product. */
+typedef struct {
+  const int8_t *q;     /* [N][ldq] codes */
+  const float *scale;  /* [1] per-tensor scale */
+  int64_t N, K, ldq;
+} qz_int8_weight;
+
+/* y[i] = fp16( scale * sum_j q[i][j] * x[j] ), fp32 accumulation, products of
+ * the exact integer code with the fp16 input; no fp16 weight is formed.
+ * x [K], y [N].  K <= 57344 (the permuted input is staged in shared memory). */
+qz_status qz_gemv_int8(const qz_int8_weight *w, const qz_half *x, qz_half *y,
+                       qz_stream s);
+
+/* Y[b][i] = fp16( scale * sum_j q[i][j] * X[b][j] ) for b < B.
+ * X [B][ldx], Y [B][ldy]; 1 <= B <= QZ_MAX_BATCH.  B <= 4 runs on CUDA
+ * cores; larger batches on the tensor cores.  QZ_ERR_UNSUPPORTED if the
+ * batch's inputs do not fit in shared memory (4*B*K bytes > 200 KiB for
+ * B <= 4). */
+qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X,
+                       int64_t ldx, qz_half *Y, int64_t ldy, qz_stream s);
+
+/* n matrices (1 <= n <= QZ_MAX_GROUP) that read the same input x, in one
+ * launch (q/k/v, gate/up).  Each keeps its own scale.  ws: host array of n
+ * structs with equal K; ys: host array of n device pointers. */
+qz_status qz_gemv_int8_grouped(const qz_int8_weight *ws, int n,
+                               const qz_half *x, qz_half *const *ys,
+                               qz_stream s);
+
+/* ======================================================================
+ * Outlier-aware INT4  [OTF "Architecture & Key Innovations": diagram and
+ * key innovation 3 (global_perm_idx; top-1% channels by |W| x |X_profile|
+ * kept in FP16; background INT4 in [-7,7], zero-point 0, 2:1 uint8 packing;
+ * output = outlier product + background product); key innovation 1 (packed
+ * weights dequantized in registers, no fp16 weight tensor)]
+ *
+ * Format of one [N][K] matrix with n_out outlier channels, kb = K - n_out:
+ *   perm  int32 [K]          : permuted input t reads x[perm[t]]; t < n_out
+ *                              are the outliers (global_perm_idx);
+ *   w_out fp16  [N][ld_out]  : w_out[i][t] = W[i][perm[t]], t < n_out;
+ *   q4    uint8 [N][ld_q4]   : background code of permuted input n_out + t'
+ *                              in byte t'/2, low nibble if t' even, as the
+ *                              two's-complement nibble (values -7..7);
+ *   scale fp32  [N]          : s_i = fp32(max_t' |W[i][perm[n_out+t']]|) / 7.
+ * ld_out = roundup(n_out, 8), ld_q4 = roundup(ceil(kb/2), 16); padding is 0.
+ * ====================================================================== */
+
+/* Row strides of the format (host only, no GPU work).  ld_out/ld_q4: host. */
+qz_status qz_int4o_layout(int64_t N, int64_t K, int64_t n_out, int64_t *ld_out,
+                          int64_t *ld_q4);
+
+/* colsum[j] += sum_i |W[i][j]| * 2^24, exactly, as int64 (every fp16 value
+ * is an integer multiple of 2^-24, so the sum is order-independent).  Call it
+ * once per matrix that shares the permutation; the caller zeroes colsum. */
+qz_status qz_saliency_accumulate(const qz_half *W, int64_t N, int64_t K,
+                                 int64_t ldw, int64_t *colsum, qz_stream s);
+
+/* Build global_perm_idx from colsum [K] and the activation profile
+ * x_profile [K] (fp32): score_j = fp64(colsum[j]) * fp64(|x_profile[j]|); the
+ * n_out channels of highest score (ties: lower j first) come first, in
+ * ascending j, then the rest in ascending j.  0 <= n_out <= K <= 2^20.
+ * perm [K] int32 is also used as working storage during the call. */
+qz_status qz_select_outliers(const int64_t *colsum, const float *x_profile,
+                             int64_t K, int64_t n_out, int32_t *perm,
+                             qz_stream s);
+
+/* *flag = 0 if perm [K] is a permutation of 0..K-1, 1 if an entry is out of
+ * range, 2 if an entry repeats.  K <= 2^20.  The host reads flag after the
+ * stream reaches the call; QZ_ERR_DATA is the host's verdict for flag != 0. */
+qz_status qz_check_perm(const int32_t *perm, int64_t K, int32_t *flag,
+                        qz_stream s);
+
+/* Quantize W [N][ldw] fp16 with the given perm into the format above.
+ * w_out may be NULL when n_out == 0.  ld_out/ld_q4 must be at least the
+ * values of qz_int4o_layout and keep the 16-B rule; all padding is written
+ * as 0.  K <= 2^17. */
+qz_status qz_quantize_int4_outlier(const qz_half *W, int64_t ldw,
+                                   const int32_t *perm, int64_t N, int64_t K,
+                                   int64_t n_out, qz_half *w_out,
+                                   int64_t ld_out, uint8_t *q4, int64_t ld_q4,
+                                   float *scale, qz_stream s);
+
+/* One quantized INT4-outlier matrix (host struct holding device pointers). */
+typedef struct {
+  int64_t N, K, n_out, ld_out, ld_q4;
+  const int32_t *perm;
+  const qz_half *w_out; /* may be NULL when n_out == 0 */
+  const uint8_t *q4;
+  const float *scale;
+} qz_int4o_weight;
+
+/* y[i] = fp16( sum_{t<n_out} w_out[i][t] * x[perm[t]]
+ *            + s_i * sum_{t'} q[i][t'] * x[perm[n_out+t']] )
+ * fp32 accumulation of exact products; x is gathered through perm into
+ * shared memory inside the kernel.  x [K] in ORIGINAL channel order, y [N].
+ * K <= 57344. */
+qz_status qz_gemv_int4_outlier(const qz_int4o_weight *w, const qz_half *x,
+                               qz_half *y, qz_stream s);
+
+/* The same for a batch: X [B][ldx], Y [B][ldy], 1 <= B <= QZ_MAX_BATCH; same
+ * CUDA-core / tensor-core split and shared-memory limit as qz_gemm_int8. */
+qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B,
+                               const qz_half *X, int64_t ldx, qz_half *Y,
+                               int64_t ldy, qz_stream s);
+
+/* n matrices sharing one input and one permutation (same perm pointer, K and
+ * n_out), one launch.  ws: host array; ys: host array of device pointers. */
+qz_status qz_gemv_int4_outlier_grouped(const qz_int4o_weight *ws, int n,
+                                       const qz_half *x, qz_half *const *ys,
+                                       qz_stream s);
+
+/* ======================================================================
+ * Layer pager  [ELG "Key Features" 2 (prefetch, transfer, reconstruct,
+ * purge) and 3 (a second CUDA stream copies layer N+1 while layer N
+ * computes); NTR "3-Tier Adaptive Caching", Tier B (pinned RAM, H2D DMA)]
+ *
+ * Double-buffers packed layers from pinned host memory into two device
+ * slots owned by the caller.  acquire(L) makes the compute stream wait until
+ * layer L is in its slot and starts the copy of layer L+1 into the other
+ * slot (after the compute that last used that slot, recorded by release);
+ * release(L) marks the end of the compute work that reads layer L.  Layers
+ * must be acquired in order 0, 1, ..., n-1 (then 0 again for the next pass).
+ * The "purge" of the page becomes slot reuse: nothing is freed in the loop.
+ * ====================================================================== */
+typedef struct qz_pager qz_pager;
+
+/* host_layers: host array of n_layers pinned host pointers; bytes: host
+ * array of their sizes (each <= slot_bytes, multiple of 16); slot0/slot1:
+ * device buffers of slot_bytes each.  The pager creates its own events; it
+ * is destroyed with qz_pager_destroy.  *out receives the handle (host). */
+qz_status qz_pager_create(const void *const *host_layers, const size_t *bytes,
+                          int n_layers, void *slot0, void *slot1,
+                          size_t slot_bytes, qz_stream copy_stream,
+                          qz_stream compute_stream, qz_pager **out);
+/* *dev_ptr (host) receives the device slot that holds `layer`. */
+qz_status qz_pager_acquire(qz_pager *p, int layer, const void **dev_ptr);
+qz_status qz_pager_release(qz_pager *p, int layer);
+/* Waits for the pager's copies to finish, then frees its host state. */
+qz_status qz_pager_destroy(qz_pager *p);
+
+/* Host-side fault injection for tests: make the copy enqueue of layer
+ * `layer` (at its next prefetch) fail as if cudaMemcpyAsync had failed.
+ * The pager then drains its copy stream and acquire returns QZ_ERR_IO.
+ * layer = -1 clears the injection.  Touches no GPU state. */
+qz_status qz_pager_inject_copy_failure(qz_pager *p, int layer);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QZ_H */
