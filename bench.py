@@ -1,0 +1,427 @@
+"""Benchmark: batch-1 decode step through a quantized decoder stack.
+
+One step = every quantized linear of every layer (4 dependent launches per
+layer), replayed from a CUDA graph.  The stack (several GB) is far larger
+than the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--extra] [--no-cpu]
+
+Prints ONE JSON line.  Under torchrun (N > 1) every rank runs an independent
+replica (the method targets one GPU; no collectives) and rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized GEMV achieved HBM GB/s (% of GB300 peak); batch-1 us per decoder layer"
+FALLBACK_HBM_GBS = 6800.0
+DOMINANT_GROUP = 2  # {gate, up}: the largest launch of every layer
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gemma2_9b_int8")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--extra", action="store_true",
+                    help="also measure the other workloads (reported under 'workloads')")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if k in d and isinstance(d[k], (int, float)):
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait(timeout=10)
+
+    def summary(self):
+        if not self.proc:
+            return None
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(wl_name: str, budget_s: float = 12.0):
+    """The CPU oracle, as it stands, on a bounded sample: the products of one
+    layer's matrices (quantized by the oracle itself), repeated until about
+    budget_s of CPU work.  Returns (GB/s, seconds, sample text, threads)."""
+    import numpy as np
+
+    from oracle import qz_oracle as O
+    from weight_only_quantized_dequant_gb300 import synthetic as S
+
+    wl = S.WORKLOADS[wl_name]
+    mats = []
+    for m in S.MATS:
+        N, K = wl.shape(m)
+        W = S.weight(N, K, S.matrix_seed(wl, 0, m), dist=wl.dist).numpy()
+        x = S.activation(1, K, 11 + len(mats)).numpy()
+        if wl.fmt == "int8":
+            q, s = O.int8_quantize(W)
+            mats.append(("int8", (q, s), x, O.int8_weight_bytes(N, K)))
+        else:
+            n_out = O.default_n_out(K)
+            perm = O.select_outliers(O.saliency_fixed(W), np.abs(x[0]).astype(np.float32), n_out)
+            wo, q4, s = O.int4o_quantize(W, perm, n_out)
+            mats.append(("int4o", (wo, q4, s, perm, n_out, K), x, O.int4o_weight_bytes(N, K, n_out)))
+    done_bytes, t_total, reps = 0, 0.0, 0
+    while t_total < budget_s and reps < 50:
+        for kind, w, x, nbytes in mats:
+            t0 = time.perf_counter()
+            if kind == "int8":
+                O.int8_product_ref(w[0], w[1], x)
+            else:
+                O.int4o_product_ref(*w, x)
+            t_total += time.perf_counter() - t0
+            done_bytes += nbytes
+        reps += 1
+    threads = len(os.sched_getaffinity(0))
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            threads = max(i.get("num_threads", 1) for i in info)
+    except Exception:
+        pass
+    sample = (f"oracle fp64 products of all 7 matrices of layer 0 of {wl_name}, "
+              f"{reps} pass(es), {done_bytes / 1e9:.2f} GB of packed weights")
+    return done_bytes / t_total / 1e9, t_total, sample, threads
+
+
+def run_reference(a):
+    """--impl reference: the CPU oracle timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+
+    from oracle import qz_oracle as O
+    from weight_only_quantized_dequant_gb300 import synthetic as S
+
+    wl = S.WORKLOADS[a.workload]
+    N, K = wl.shape("down")
+    W = S.weight(N, K, S.matrix_seed(wl, 0, "down"), dist=wl.dist).numpy()
+    x = S.activation(1, K, 5).numpy()
+    if wl.fmt == "int8":
+        q, s = O.int8_quantize(W)
+        step = lambda: O.int8_product_ref(q, s, x)  # noqa: E731
+        nbytes = O.int8_weight_bytes(N, K)
+    else:
+        n_out = O.default_n_out(K)
+        perm = O.select_outliers(O.saliency_fixed(W), np.abs(x[0]).astype(np.float32), n_out)
+        wo, q4, s4 = O.int4o_quantize(W, perm, n_out)
+        step = lambda: O.int4o_product_ref(wo, q4, s4, perm, n_out, K, x)  # noqa: E731
+        nbytes = O.int4o_weight_bytes(N, K, n_out)
+    for _ in range(a.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        step()
+    dt = (time.perf_counter() - t0) / a.steps
+    gbs = nbytes / dt / 1e9
+    cores = len(os.sched_getaffinity(0))
+    sample = f"oracle fp64 product of the down projection ({N}x{K}) of layer 0, per step"
+    out = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+           "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+           "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": a.workload, "sample": "down projection of layer 0"},
+           "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
+            clocks=False, device=None):
+    """Build the stack, capture one step, time it.  Returns a dict."""
+    import torch
+
+    from weight_only_quantized_dequant_gb300 import stack as ST
+    from weight_only_quantized_dequant_gb300 import synthetic as S
+
+    wl = S.WORKLOADS[wl_name]
+    t_build = time.perf_counter()
+    st = ST.LayerStack(wl, batch=batch, device=device)
+    torch.cuda.synchronize()
+    t_build = time.perf_counter() - t_build
+
+    # one contiguous host<->device staging area per direction for e2e
+    xs = [x for xs in st.x for x in xs]
+    ys = [y for ys in st.y for yy in ys for y in yy]
+    x_dev = torch.cat([x.reshape(-1) for x in xs])
+    y_dev = torch.empty((sum(y.numel() for y in ys),), dtype=torch.float16, device=device)
+    off = 0
+    for l in range(st.n_layers):           # re-point inputs/outputs into the staging areas
+        for g in range(len(st.x[l])):
+            n = st.x[l][g].numel()
+            st.x[l][g] = x_dev[off:off + n].view_as(st.x[l][g])
+            off += n
+    off = 0
+    for l in range(st.n_layers):
+        for g in range(len(st.y[l])):
+            for k in range(len(st.y[l][g])):
+                n = st.y[l][g][k].numel()
+                st.y[l][g][k] = y_dev[off:off + n].view_as(st.y[l][g][k])
+                off += n
+    x_host = x_dev.cpu().pin_memory()
+    y_host = torch.empty(y_dev.shape, dtype=torch.float16).pin_memory()
+
+    # graph of one step with timing events around the dominant launch
+    s = torch.cuda.Stream(device=device)
+    def _ev():  # external: a timing node inside the captured graph
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return torch.cuda.Event(enable_timing=True)
+    ev = [(_ev(), _ev()) for _ in range(st.n_layers)]
+
+    def step(stream):
+        for l in range(st.n_layers):
+            for g in range(len(S.GROUPS)):
+                if g == DOMINANT_GROUP:
+                    ev[l][0].record(stream)
+                st.run_group(l, g, stream)
+                if g == DOMINANT_GROUP:
+                    ev[l][1].record(stream)
+
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        step(s)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(s)
+    torch.cuda.synchronize(device)
+
+    def barrier():
+        if dist_ctx is not None:
+            dist_ctx.barrier()
+        torch.cuda.synchronize(device)
+
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            graph.replay()
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clk = Clocks(device.index if device is not None else 0) if clocks else None
+    if clk:
+        clk.__enter__()
+        time.sleep(0.3)
+    with torch.cuda.stream(s):
+        t0.record(s)
+        for _ in range(steps):
+            graph.replay()
+        t1.record(s)
+    barrier()
+    if clk:
+        clk.__exit__(None, None, None)
+    ms = t0.elapsed_time(t1) / steps
+    dom_ms = [a.elapsed_time(b) for a, b in ev]          # last timed step
+    dom_avg_ms = sum(dom_ms) / len(dom_ms)
+
+    # e2e: pinned host inputs -> device, step, outputs -> pinned host
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            x_dev.copy_(x_host, non_blocking=True)
+            graph.replay()
+            y_host.copy_(y_dev, non_blocking=True)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(steps):
+            x_dev.copy_(x_host, non_blocking=True)
+            graph.replay()
+            y_host.copy_(y_dev, non_blocking=True)
+        e1.record(s)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / steps
+
+    dom_names = S.GROUPS[DOMINANT_GROUP]
+    dom_bytes = sum(st.layers[0].mats[m].nbytes() for m in dom_names)
+    K_dom = wl.shape(dom_names[0])[1]
+    dom_bytes += 2 * batch * K_dom + sum(2 * batch * wl.shape(m)[0] for m in dom_names)
+    if wl.fmt == "int4o":
+        dom_bytes += 4 * K_dom
+    out = {
+        "workload": wl_name, "batch": batch, "layers": st.n_layers,
+        "bytes_per_step": st.bytes_per_step(),
+        "weight_bytes_per_layer": st.weight_bytes_per_layer(),
+        "ms_per_step": ms, "us_per_layer": ms * 1e3 / st.n_layers,
+        "gbs": st.bytes_per_step() / (ms * 1e-3) / 1e9,
+        "dominant": {"group": "+".join(dom_names), "bytes_per_launch": dom_bytes,
+                     "avg_ms": dom_avg_ms, "gbs": dom_bytes / (dom_avg_ms * 1e-3) / 1e9},
+        "e2e_ms": e2e_ms, "e2e_gbs": st.bytes_per_step() / (e2e_ms * 1e-3) / 1e9,
+        "h2d": st.h2d_bytes_per_step(), "d2h": st.d2h_bytes_per_step(),
+        "launches_per_step": st.launches_per_step(), "build_s": t_build,
+        "stack_gb": st.n_layers * st.weight_bytes_per_layer() / 1e9,
+    }
+    if clk:
+        out["clocks"] = clk.summary()
+    del graph, st
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        return run_reference(a)
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_ctx = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        dist_ctx = dist
+
+    from weight_only_quantized_dequant_gb300 import build
+    if rank == 0:
+        build.build()
+    if dist_ctx is not None:
+        dist_ctx.barrier()
+
+    r = measure(a.workload, 1, a.steps, a.warmup, dist_ctx, clocks=(rank == 0), device=device)
+    ms_all = r["ms_per_step"]
+    e2e_all = r["e2e_ms"]
+    if dist_ctx is not None:
+        t = torch.tensor([r["ms_per_step"], r["e2e_ms"]], device=device)
+        dist_ctx.all_reduce(t, op=dist_ctx.ReduceOp.MAX)
+        ms_all, e2e_all = float(t[0]), float(t[1])
+
+    extra = {}
+    if a.extra and rank == 0:
+        for name, b in [("llama32_3b_int4o", 1), ("llama_7b_int4o", 1), ("llama_7b_int4o", 4),
+                        ("llama_70b_int4o", 1)]:
+            e = measure(name, b, max(5, a.steps // 2), a.warmup, None, device=device)
+            extra[f"{name}_b{b}"] = {k: e[k] for k in ("us_per_layer", "gbs", "ms_per_step",
+                                                          "stack_gb")}
+            extra[f"{name}_b{b}"]["dominant_gbs"] = e["dominant"]["gbs"]
+
+    cpu = None
+    if rank == 0 and not a.no_cpu:
+        gbs_cpu, t_cpu, sample, threads = cpu_baseline(a.workload)
+        cpu = {"value": round(gbs_cpu, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": sample, "seconds": round(t_cpu, 2)}
+
+    if rank != 0:
+        if dist_ctx is not None:
+            dist_ctx.destroy_process_group()
+        return 0
+    peak, peak_src = peaks()
+    value = world * r["bytes_per_step"] / (ms_all * 1e-3) / 1e9
+    dom = r["dominant"]
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_all, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": a.workload, "format": "int8 per-tensor", "batch": 1,
+                   "layers": r["layers"], "launches_per_layer": 4, "graph": True,
+                   "l2": f"inputs larger than L2 ({r['stack_gb']:.2f} GB stack > 129 MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_layer": round(ms_all * 1e3 / r["layers"], 3),
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "peak_source": f"{peak:.0f} GB/s of {peak_src}",
+        "roofline": {"bound": "hbm", "achieved": round(dom["gbs"], 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(dom["gbs"] / peak, 4), "traffic": None,
+                     "kernel": f"gemv ({dom['group']} grouped launch)",
+                     "bytes_per_launch": dom["bytes_per_launch"],
+                     "avg_launch_us": round(dom["avg_ms"] * 1e3, 3),
+                     "peak_kind": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * r["bytes_per_step"] / (e2e_all * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "ms_per_step": round(e2e_all, 4)},
+        "gpu_launches": r["launches_per_step"] * a.steps,
+        "clocks": r.get("clocks"),
+    }
+    if extra:
+        out["workloads"] = extra
+    print(json.dumps(out), flush=True)
+    if dist_ctx is not None:
+        dist_ctx.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main() or 0)

@@ -1,0 +1,187 @@
+"""The C ABI on the host: the library loads, exports every function that
+include/qz.h declares, and validates arguments before touching the GPU.
+No GPU needed (no call here reaches a launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import qz_oracle as O
+from weight_only_quantized_dequant_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qz.h")
+
+OK, INVAL, ALIGN, UNSUP = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from weight_only_quantized_dequant_gb300 import build
+        build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qz_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ["qz_quantize_int8", "qz_gemv_int8", "qz_gemm_int8", "qz_gemv_int8_grouped",
+                 "qz_int4o_layout", "qz_saliency_accumulate", "qz_select_outliers",
+                 "qz_check_perm", "qz_quantize_int4_outlier", "qz_gemv_int4_outlier",
+                 "qz_gemm_int4_outlier", "qz_gemv_int4_outlier_grouped", "qz_pager_create",
+                 "qz_pager_acquire", "qz_pager_release", "qz_pager_destroy"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding knows every one of them
+    assert set(declared_functions()) <= set(_lib._SIGS)
+
+
+def test_struct_layouts():
+    assert ctypes.sizeof(_lib.Int8Weight) == 40
+    assert ctypes.sizeof(_lib.Int4oWeight) == 72
+
+
+def test_version_and_status_strings(lib):
+    assert lib.qz_version() >= 10000
+    for code, name in _lib.STATUS.items():
+        assert lib.qz_status_string(code).decode() == name
+    assert lib.qz_status_string(99).decode() == "QZ_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("K,n_out", [(1, 0), (1, 1), (34, 1), (3072, 31), (4096, 41),
+                                     (8192, 82), (11008, 111), (28672, 287), (57344, 574)])
+def test_layout_matches_oracle(lib, K, n_out):
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.qz_int4o_layout(7, K, n_out, ctypes.byref(a), ctypes.byref(b)) == OK
+    assert (a.value, b.value) == O.int4o_layout(K, n_out)
+
+
+def test_layout_rejects_bad_sizes(lib):
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.qz_int4o_layout(7, 10, 11, ctypes.byref(a), ctypes.byref(b)) == INVAL
+    assert lib.qz_int4o_layout(0, 10, 1, ctypes.byref(a), ctypes.byref(b)) == INVAL
+    assert lib.qz_int4o_layout(7, 10, -1, ctypes.byref(a), ctypes.byref(b)) == INVAL
+    assert lib.qz_int4o_layout(7, 10, 1, None, ctypes.byref(b)) == INVAL
+
+
+# Fake device addresses: validation only inspects their values.
+P = 0x10000  # 16-byte aligned
+PU = 0x10008  # 8-byte aligned only
+
+
+def test_quantize_int8_validation(lib):
+    f = lib.qz_quantize_int8
+    assert f(None, 4, 16, 16, P, 16, P, None) == INVAL
+    assert f(P, 4, 16, 8, P, 16, P, None) == INVAL            # ldw < K
+    assert f(P, 4, 16, 16, P, 16, None, None) == INVAL        # no scale
+    assert f(PU, 4, 16, 16, P, 16, P, None) == ALIGN          # W misaligned
+    assert f(P, 4, 16, 20, P, 16, P, None) == ALIGN           # ldw*2 % 16
+    assert f(P, 4, 16, 16, P, 24, P, None) == ALIGN           # ldq % 16
+    assert f(P, 0, 16, 16, P, 16, P, None) == INVAL
+
+
+def _w8(N=8, K=32, ldq=32, q=P, scale=P):
+    return _lib.Int8Weight(q, scale, N, K, ldq)
+
+
+def test_gemv_int8_validation(lib):
+    w = _w8()
+    assert lib.qz_gemv_int8(None, P, P, None) == INVAL
+    assert lib.qz_gemv_int8(ctypes.byref(w), None, P, None) == INVAL
+    assert lib.qz_gemv_int8(ctypes.byref(w), P, None, None) == INVAL
+    assert lib.qz_gemv_int8(ctypes.byref(w), PU, P, None) == ALIGN
+    assert lib.qz_gemv_int8(ctypes.byref(_w8(ldq=40)), P, P, None) == ALIGN
+    assert lib.qz_gemv_int8(ctypes.byref(_w8(ldq=16)), P, P, None) == INVAL
+    assert lib.qz_gemv_int8(ctypes.byref(_w8(K=57360, ldq=57360)), P, P, None) == UNSUP
+    assert lib.qz_gemm_int8(ctypes.byref(w), 65, P, 32, P, 8, None) == UNSUP
+    assert lib.qz_gemm_int8(ctypes.byref(w), 0, P, 32, P, 8, None) == INVAL
+    assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 16, P, 8, None) == INVAL   # ldx < K
+    assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 36, P, 8, None) == ALIGN   # ldx*2 % 16
+
+
+def test_grouped_int8_validation(lib):
+    ws = (_lib.Int8Weight * 5)(*[_w8() for _ in range(5)])
+    ys = (ctypes.c_void_p * 5)(*[P] * 5)
+    assert lib.qz_gemv_int8_grouped(ws, 5, P, ys, None) == UNSUP
+    assert lib.qz_gemv_int8_grouped(ws, 0, P, ys, None) == INVAL
+    bad = (_lib.Int8Weight * 2)(_w8(K=32), _w8(K=48, ldq=48))
+    assert lib.qz_gemv_int8_grouped(bad, 2, P, ys, None) == INVAL
+
+
+def _w4(N=8, K=64, n_out=1, perm=P, w_out=P, q4=P, scale=P, ld_out=None, ld_q4=None):
+    lo, lq = O.int4o_layout(K, min(n_out, K))
+    return _lib.Int4oWeight(N, K, n_out, lo if ld_out is None else ld_out,
+                            lq if ld_q4 is None else ld_q4, perm, w_out, q4, scale)
+
+
+def test_gemv_int4_validation(lib):
+    g = lambda w: lib.qz_gemv_int4_outlier(ctypes.byref(w), P, P, None)  # noqa: E731
+    assert g(_w4(n_out=65)) == INVAL
+    assert g(_w4(perm=None)) == INVAL
+    assert g(_w4(w_out=None)) == INVAL                        # n_out > 0 needs w_out
+    assert g(_w4(q4=None)) == INVAL
+    assert g(_w4(ld_q4=16)) == INVAL                          # < ceil(kb/2)
+    assert g(_w4(ld_out=12)) == ALIGN
+    assert g(_w4(ld_q4=40)) == ALIGN
+    assert g(_w4(q4=PU)) == ALIGN
+    assert g(_w4(K=57345)) == UNSUP
+    w = _w4()
+    assert lib.qz_gemm_int4_outlier(ctypes.byref(w), 65, P, 64, P, 8, None) == UNSUP
+
+
+def test_grouped_int4_requires_shared_perm(lib):
+    ws = (_lib.Int4oWeight * 2)(_w4(), _w4(perm=P + 0x100))
+    ys = (ctypes.c_void_p * 2)(P, P)
+    assert lib.qz_gemv_int4_outlier_grouped(ws, 2, P, ys, None) == INVAL
+    ws = (_lib.Int4oWeight * 2)(_w4(), _w4(n_out=2))
+    assert lib.qz_gemv_int4_outlier_grouped(ws, 2, P, ys, None) == INVAL
+
+
+def test_quantizer_int4_validation(lib):
+    f = lib.qz_quantize_int4_outlier
+    lo, lq = O.int4o_layout(64, 1)
+    assert f(P, 64, P, 8, 64, 65, P, lo, P, lq, P, None) == INVAL   # n_out > K
+    assert f(P, 64, P, 8, 64, 1, None, lo, P, lq, P, None) == INVAL
+    assert f(P, 64, P, 8, 64, 1, P, lo, P, 16, P, None) == INVAL    # ld_q4 too small
+    assert f(P, 64, P, 8, 64, 1, P, 12, P, lq, P, None) == ALIGN
+    assert f(P, 64, None, 8, 64, 1, P, lo, P, lq, P, None) == INVAL
+    assert f(P, 64, P, 8, 1 << 17 + 1, 1, P, lo, P, lq, P, None) != OK
+    assert lib.qz_select_outliers(P, P, (1 << 20) + 1, 1, P, None) == UNSUP
+    assert lib.qz_select_outliers(P, P, 10, 11, P, None) == INVAL
+    assert lib.qz_select_outliers(PU + 4, P, 10, 1, P, None) == ALIGN
+    assert lib.qz_check_perm(None, 10, P, None) == INVAL
+    assert lib.qz_saliency_accumulate(P, 4, 16, 16, PU + 4, None) == ALIGN
+
+
+def test_pager_create_validation(lib):
+    hp = (ctypes.c_void_p * 2)(P, P + 0x1000)
+    sz = (ctypes.c_size_t * 2)(256, 256)
+    out = ctypes.c_void_p()
+    f = lib.qz_pager_create
+    assert f(hp, sz, 2, P, P, 256, None, None, ctypes.byref(out)) == INVAL     # same slot
+    assert f(hp, sz, 2, P, P + 0x800, 128, None, None, ctypes.byref(out)) == INVAL
+    assert f(hp, sz, 0, P, P + 0x800, 256, None, None, ctypes.byref(out)) == INVAL
+    assert f(hp, sz, 2, PU, P + 0x800, 256, None, None, ctypes.byref(out)) == ALIGN
+    sz_bad = (ctypes.c_size_t * 2)(250, 256)
+    assert f(hp, sz_bad, 2, P, P + 0x800, 256, None, None, ctypes.byref(out)) == ALIGN
+    assert lib.qz_pager_acquire(None, 0, ctypes.byref(out)) == INVAL
+    assert lib.qz_pager_release(None, 0) == INVAL
+    assert lib.qz_pager_destroy(None) == INVAL
+
+
+def test_python_api_refuses_cpu_tensors():
+    import torch
+    import weight_only_quantized_dequant_gb300 as qz
+    with pytest.raises(ValueError):
+        qz.quantize_int8(torch.zeros((4, 16), dtype=torch.float16))

@@ -1,0 +1,310 @@
+"""CUDA path vs the CPU oracle, element by element, on seeded inputs.
+
+Bit-exact: INT8 codes and scale, saliency sums, the permutation, INT4 codes,
+row scales, outlier copies and every padding byte.  Products: within
+|y - y_ref| <= 1e-3 * sum_j |w_ij x_j| + 1 fp16 ulp(y_ref), y_ref in fp64 on
+the same reconstructed weights.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import qz_oracle as O
+from weight_only_quantized_dequant_gb300 import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from weight_only_quantized_dequant_gb300 import build
+    build.build()
+
+
+def qz():
+    import weight_only_quantized_dequant_gb300 as m
+    return m
+
+
+def assert_close(y_gpu, y_ref, a_ref, what=""):
+    y = y_gpu.float().cpu().numpy().astype(np.float64).reshape(y_ref.shape)
+    tol = O.tolerance(y_ref, a_ref)
+    err = np.abs(y - y_ref)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())}/{bad.size} outside tolerance; "
+                           f"worst err/tol {float((err / tol).max()):.3g}")
+    return float((err / tol).max())
+
+
+def padded_rows(X: torch.Tensor) -> torch.Tensor:
+    """View of X whose rows start on 16-byte boundaries."""
+    B, K = X.shape
+    Kp = -(-K // 8) * 8
+    buf = torch.zeros((B, Kp), dtype=X.dtype, device=X.device)
+    buf[:, :K] = X
+    return buf[:, :K]
+
+
+# ----------------------------------------------------------------- INT8 ---
+def test_tiny_int8_256():
+    W, x = S.tiny_int8_inputs()
+    w = qz().quantize_int8(W.to(DEV))
+    y = qz().gemv_int8(w, x[0].to(DEV))
+    q_ref, s_ref = O.int8_quantize(W.numpy())
+    assert np.array_equal(w.q.cpu().numpy()[:, :256], q_ref)
+    assert w.scale.item() == float(s_ref)
+    y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, x.numpy())
+    assert_close(y, y_ref[0], a_ref[0], "tiny int8")
+
+
+INT8_SHAPES = [(1, 1), (3, 34), (37, 100), (257, 1000), (1024, 4096), (96, 14336), (8, 57344)]
+
+
+@pytest.mark.parametrize("N,K", INT8_SHAPES)
+def test_int8_quantize_bit_exact(N, K):
+    W = S.weight(N, K, 1000 + N + K, device=DEV)
+    w = qz().quantize_int8(W)
+    q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+    q = w.q.cpu().numpy()
+    assert w.scale.item() == float(s_ref)
+    assert np.array_equal(q[:, :K], q_ref)
+    assert not q[:, K:].any()
+
+
+@pytest.mark.parametrize("N,K", INT8_SHAPES)
+@pytest.mark.parametrize("B", [1, 2, 3, 4])
+def test_int8_gemm_cuda_cores(N, K, B):
+    W = S.weight(N, K, 2000 + N + K, device=DEV)
+    X = padded_rows(S.activation(B, K, 3000 + B, device=DEV))
+    w = qz().quantize_int8(W)
+    Y = qz().gemv_int8(w, X[0]).unsqueeze(0) if B == 1 else qz().gemm_int8(w, X)
+    q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+    y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, X.cpu().numpy())
+    assert_close(Y, y_ref, a_ref, f"int8 N={N} K={K} B={B}")
+
+
+def test_int8_zero_matrix():
+    W = torch.zeros((5, 40), dtype=torch.float16, device=DEV)
+    w = qz().quantize_int8(W)
+    assert w.scale.item() == 0.0 and not w.q.any()
+    y = qz().gemv_int8(w, S.activation(1, 40, 5, device=DEV)[0])
+    assert not y.float().abs().sum().item()
+
+
+def test_int8_grouped_matches_separate():
+    K = 3584
+    Ns = [4096, 2048, 2048]
+    Ws = [S.weight(n, K, 50 + i, device=DEV) for i, n in enumerate(Ns)]
+    x = S.activation(1, K, 60, device=DEV)
+    ws = [qz().quantize_int8(W) for W in Ws]
+    ys = qz().gemv_int8_grouped(ws, x[0])
+    for W, y in zip(Ws, ys):
+        q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+        y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, x.cpu().numpy())
+        assert_close(y, y_ref[0], a_ref[0], "grouped int8")
+
+
+# ------------------------------------------------------- INT4 quantizer ---
+@pytest.mark.parametrize("N,K", [(1, 1), (3, 34), (300, 1000), (700, 3072), (64, 28672)])
+def test_saliency_exact(N, K):
+    Ws = [S.weight(N, K, 70 + i, device=DEV) for i in range(2)]
+    colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+    for W in Ws:
+        qz().saliency_accumulate(W, colsum)
+    ref = O.saliency_fixed([W.cpu().numpy() for W in Ws])
+    assert np.array_equal(colsum.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("K", [1, 7, 300, 3072, 28672])
+def test_select_outliers_exact_with_ties(K):
+    g = torch.Generator().manual_seed(K)
+    colsum = torch.randint(0, 6, (K,), generator=g, dtype=torch.int64)
+    prof = torch.tensor([0.5, 1.0, -1.0, 2.0])[torch.randint(0, 4, (K,), generator=g)]
+    for n_out in sorted({0, 1, (K + 99) // 100, K // 2, K}):
+        perm = qz().select_outliers(colsum.to(DEV), prof.to(DEV), n_out)
+        ref = O.select_outliers(colsum.numpy(), prof.numpy(), n_out)
+        assert np.array_equal(perm.cpu().numpy(), ref), (K, n_out)
+
+
+def test_select_outliers_realistic_profile():
+    K, n_out = 11008, 111
+    W = S.weight(512, K, 90, device=DEV)
+    prof = S.x_profile(K, n_out, 91, device=DEV)
+    colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+    qz().saliency_accumulate(W, colsum)
+    perm = qz().select_outliers(colsum, prof, n_out)
+    ref = O.select_outliers(O.saliency_fixed(W.cpu().numpy()), prof.cpu().numpy(), n_out)
+    assert np.array_equal(perm.cpu().numpy(), ref)
+
+
+def test_check_perm_flags():
+    K = 1000
+    p = torch.randperm(K, generator=torch.Generator().manual_seed(1)).to(torch.int32)
+    assert qz().check_perm(p.to(DEV)) == 0
+    dup = p.clone()
+    dup[5] = dup[6]
+    assert qz().check_perm(dup.to(DEV)) == 2
+    oob = p.clone()
+    oob[7] = K
+    assert qz().check_perm(oob.to(DEV)) == 1
+    neg = p.clone()
+    neg[0] = -1
+    assert qz().check_perm(neg.to(DEV)) == 1
+
+
+INT4_SHAPES = [(1, 1, 0), (1, 1, 1), (3, 34, 1), (5, 34, 0), (7, 34, 34), (64, 520, 6),
+               (300, 3072, 31), (129, 4096, 41), (64, 11008, 111), (16, 28672, 287),
+               (8, 57344, 574)]
+
+
+def _int4_inputs(N, K, n_out, seed):
+    W = S.weight(N, K, seed, device=DEV)
+    prof = S.x_profile(K, max(n_out, 0), seed + 1, device=DEV)
+    colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+    qz().saliency_accumulate(W, colsum)
+    perm = qz().select_outliers(colsum, prof, n_out)
+    return W, prof, perm
+
+
+@pytest.mark.parametrize("N,K,n_out", INT4_SHAPES)
+def test_int4_quantize_bit_exact(N, K, n_out):
+    W, prof, perm = _int4_inputs(N, K, n_out, 4000 + K + n_out)
+    w = qz().quantize_int4_outlier(W, perm, n_out)
+    Wn = W.cpu().numpy()
+    perm_ref = O.select_outliers(O.saliency_fixed(Wn), prof.cpu().numpy(), n_out)
+    assert np.array_equal(perm.cpu().numpy(), perm_ref)
+    wo, q4, s = O.int4o_quantize(Wn, perm_ref, n_out)
+    assert np.array_equal(w.w_out.cpu().numpy().view(np.uint16), wo.view(np.uint16))
+    assert np.array_equal(w.q4.cpu().numpy(), q4)
+    assert np.array_equal(w.scale.cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K,n_out", INT4_SHAPES)
+@pytest.mark.parametrize("B", [1, 2, 3, 4])
+def test_int4_gemm_cuda_cores(N, K, n_out, B):
+    W, prof, perm = _int4_inputs(N, K, n_out, 5000 + K + n_out)
+    w = qz().quantize_int4_outlier(W, perm, n_out)
+    X = padded_rows(S.activation(B, K, 6000 + B, device=DEV))
+    Y = qz().gemv_int4_outlier(w, X[0]).unsqueeze(0) if B == 1 else qz().gemm_int4_outlier(w, X)
+    wo, q4, s = O.int4o_quantize(W.cpu().numpy(), perm.cpu().numpy(), n_out)
+    y_ref, a_ref = O.int4o_product_ref(wo, q4, s, perm.cpu().numpy(), n_out, K, X.cpu().numpy())
+    assert_close(Y, y_ref, a_ref, f"int4 N={N} K={K} n_out={n_out} B={B}")
+
+
+def test_int4_grouped_matches_separate():
+    K, n_out = 4096, 41
+    Ns = [4096, 1024, 1024]
+    Ws = [S.weight(n, K, 150 + i, device=DEV) for i, n in enumerate(Ns)]
+    prof = S.x_profile(K, n_out, 160, device=DEV)
+    colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+    for W in Ws:
+        qz().saliency_accumulate(W, colsum)
+    perm = qz().select_outliers(colsum, prof, n_out)
+    ws = [qz().quantize_int4_outlier(W, perm, n_out) for W in Ws]
+    x = S.activation(1, K, 170, device=DEV)
+    ys = qz().gemv_int4_outlier_grouped(ws, x[0])
+    pn = perm.cpu().numpy()
+    for W, y in zip(Ws, ys):
+        wo, q4, s = O.int4o_quantize(W.cpu().numpy(), pn, n_out)
+        y_ref, a_ref = O.int4o_product_ref(wo, q4, s, pn, n_out, K, x.cpu().numpy())
+        assert_close(y, y_ref[0], a_ref[0], "grouped int4")
+
+
+# --------------------------------------------------- full-size matrices ---
+@pytest.mark.slow
+def test_full_gemma_layer_int8():
+    """Every matrix of one Gemma-2-9B-shaped layer: codes bit-exact and the
+    grouped launches of the decode step within tolerance."""
+    wl = S.WORKLOADS["gemma2_9b_int8"]
+    mats = {}
+    for m in S.MATS:
+        N, K = wl.shape(m)
+        W = S.weight(N, K, S.matrix_seed(wl, 0, m), device=DEV)
+        mats[m] = (W, qz().quantize_int8(W))
+    for g, names in enumerate(S.GROUPS):
+        K = wl.shape(names[0])[1]
+        x = S.activation(1, K, S.input_seed(wl, 0, g), device=DEV)
+        ys = qz().gemv_int8_grouped([mats[m][1] for m in names], x[0])
+        for m, y in zip(names, ys):
+            W, w = mats[m]
+            q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+            assert w.scale.item() == float(s_ref)
+            assert np.array_equal(w.q.cpu().numpy()[:, :K], q_ref)
+            y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, x.cpu().numpy())
+            assert_close(y, y_ref[0], a_ref[0], f"gemma {m}")
+
+
+@pytest.mark.slow
+def test_full_70b_down_proj_int4_sampled():
+    """The largest matrix (8192 x 28672): saliency and permutation exact over
+    the whole matrix; codes and outputs checked on 64 sampled rows."""
+    N, K = 8192, 28672
+    n_out = O.default_n_out(K)
+    W = S.weight(N, K, 77, device=DEV)
+    prof = S.x_profile(K, n_out, 78, device=DEV)
+    colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+    qz().saliency_accumulate(W, colsum)
+    perm = qz().select_outliers(colsum, prof, n_out)
+    w = qz().quantize_int4_outlier(W, perm, n_out)
+    x = S.activation(1, K, 79, device=DEV)
+    y = qz().gemv_int4_outlier(w, x[0])
+    Wn = W.cpu().numpy()
+    assert np.array_equal(colsum.cpu().numpy(), O.saliency_fixed(Wn))
+    pn = O.select_outliers(O.saliency_fixed(Wn), prof.cpu().numpy(), n_out)
+    assert np.array_equal(perm.cpu().numpy(), pn)
+    rows = np.random.default_rng(0).choice(N, 64, replace=False)
+    wo, q4, s = O.int4o_quantize(Wn[rows], pn, n_out)
+    assert np.array_equal(w.q4.cpu().numpy()[rows], q4)
+    assert np.array_equal(w.w_out.cpu().numpy()[rows].view(np.uint16), wo.view(np.uint16))
+    assert np.array_equal(w.scale.cpu().numpy()[rows], s)
+    y_ref, a_ref = O.int4o_product_ref(wo, q4, s, pn, n_out, K, x.cpu().numpy())
+    assert_close(y[rows], y_ref[0], a_ref[0], "70b down sampled")
+
+
+# ----------------------------------------------------------------- pager ---
+def test_pager_streams_layers_and_reports_injected_failure():
+    import weight_only_quantized_dequant_gb300 as m
+    K, N, L = 1024, 512, 5
+    ws, hosts = [], []
+    for l in range(L):
+        W = S.weight(N, K, 300 + l, device=DEV)
+        w = m.quantize_int8(W)
+        ws.append(w)
+        # one packed layer = q bytes then the scale, padded to 16 bytes
+        blob = torch.zeros((N * w.ldq + 16,), dtype=torch.uint8)
+        blob[: N * w.ldq] = w.q.cpu().view(torch.uint8).reshape(-1)
+        blob[N * w.ldq: N * w.ldq + 4] = w.scale.cpu().view(torch.uint8)
+        hosts.append(blob.pin_memory())
+    slots = [torch.empty((hosts[0].numel(),), dtype=torch.uint8, device=DEV) for _ in range(2)]
+    copy_s, comp_s = torch.cuda.Stream(), torch.cuda.Stream()
+    x = S.activation(1, K, 400, device=DEV)[0]
+    ref = [m.gemv_int8(w, x) for w in ws]
+    torch.cuda.synchronize()
+    pager = m.Pager(hosts, slots, copy_s, comp_s)
+    outs = [torch.empty((N,), dtype=torch.float16, device=DEV) for _ in range(L)]
+    for rnd in range(2):
+        for l in range(L):
+            ptr = pager.acquire(l)
+            slot = slots[0] if ptr == slots[0].data_ptr() else slots[1]
+            assert ptr in (slots[0].data_ptr(), slots[1].data_ptr())
+            wq = m.Int8Matrix(slot[: N * ws[l].ldq].view(torch.int8).view(N, ws[l].ldq),
+                              slot[N * ws[l].ldq: N * ws[l].ldq + 4].view(torch.float32), N, K)
+            with torch.cuda.stream(comp_s):
+                m.gemv_int8(wq, x, outs[l], stream=comp_s)
+            pager.release(l)
+        comp_s.synchronize()
+        for l in range(L):
+            assert torch.equal(outs[l], ref[l]), (rnd, l)
+    # host-side injected copy failure: acquire reports QZ_ERR_IO, nothing hangs
+    pager.inject_copy_failure(2)
+    with pytest.raises(m.QzError) as ei:
+        for l in range(L):
+            pager.acquire(l)
+            pager.release(l)
+    assert ei.value.name == "QZ_ERR_IO"
+    pager.close()
+    torch.cuda.synchronize()

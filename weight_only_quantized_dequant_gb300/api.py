@@ -1,0 +1,287 @@
+"""Python API over libqz.  PyTorch supplies device memory and streams only:
+every step of quantization and every product runs in the library's kernels.
+
+Names follow the C ABI (include/qz.h): ``quantize_int8``, ``gemv_int8``,
+``gemm_int8``, ``gemv_int8_grouped``, ``saliency_accumulate``,
+``select_outliers``, ``check_perm``, ``quantize_int4_outlier``,
+``gemv_int4_outlier``, ``gemm_int4_outlier``, ``gemv_int4_outlier_grouped``
+and the ``Pager``.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import Int4oWeight, Int8Weight, QzError  # noqa: F401
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _round_up(v: int, m: int) -> int:
+    return -(-v // m) * m
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libqz works on CUDA tensors only (no CPU fallback)")
+
+
+# ------------------------------------------------------------------ INT8 ---
+@dataclass
+class Int8Matrix:
+    """Per-tensor INT8 matrix: q [N, ldq] int8 (columns >= K are 0), scale [1]."""
+    q: torch.Tensor
+    scale: torch.Tensor
+    N: int
+    K: int
+
+    @property
+    def ldq(self) -> int:
+        return self.q.stride(0)
+
+    def struct(self) -> Int8Weight:
+        return Int8Weight(self.q.data_ptr(), self.scale.data_ptr(), self.N, self.K, self.ldq)
+
+    def nbytes(self) -> int:
+        """Algorithmic bytes: N*K codes + one fp32 scale."""
+        return self.N * self.K + 4
+
+
+def quantize_int8(W: torch.Tensor, stream=None) -> Int8Matrix:
+    """scale = max|W|/127, q = round(W/scale) (half-to-even), on the GPU."""
+    _need_cuda(W)
+    assert W.dtype == torch.float16 and W.dim() == 2
+    N, K = W.shape
+    if W.stride(1) != 1 or W.stride(0) % 8 or W.data_ptr() % 16:
+        W = _padded_fp16(W)
+    q = torch.empty((N, _round_up(K, 16)), dtype=torch.int8, device=W.device)
+    scale = torch.empty((1,), dtype=torch.float32, device=W.device)
+    _lib.call("qz_quantize_int8", W.data_ptr(), N, K, W.stride(0), q.data_ptr(), q.stride(0),
+              scale.data_ptr(), _stream(stream))
+    return Int8Matrix(q, scale, N, K)
+
+
+def _padded_fp16(W: torch.Tensor) -> torch.Tensor:
+    """Copy W into rows padded to a multiple of 8 halves (16 bytes)."""
+    N, K = W.shape
+    buf = torch.zeros((N, _round_up(K, 8)), dtype=W.dtype, device=W.device)
+    buf[:, :K] = W
+    return buf
+
+
+def _vec_out(x: torch.Tensor, N: int, B: int | None = None) -> torch.Tensor:
+    if B is None:
+        return torch.empty((N,), dtype=torch.float16, device=x.device)
+    return torch.empty((B, N), dtype=torch.float16, device=x.device)
+
+
+def gemv_int8(w: Int8Matrix, x: torch.Tensor, y: torch.Tensor | None = None, stream=None):
+    """y = fp16(scale * q @ x) for one input vector x [K]."""
+    _need_cuda(x)
+    y = _vec_out(x, w.N) if y is None else y
+    _lib.call("qz_gemv_int8", ctypes.byref(w.struct()), x.data_ptr(), y.data_ptr(),
+              _stream(stream))
+    return y
+
+
+def gemm_int8(w: Int8Matrix, X: torch.Tensor, Y: torch.Tensor | None = None, stream=None):
+    """Y [B, N] = fp16(scale * X @ q^T) for X [B, K], B <= 64."""
+    _need_cuda(X)
+    B = X.shape[0]
+    Y = _vec_out(X, w.N, B) if Y is None else Y
+    _lib.call("qz_gemm_int8", ctypes.byref(w.struct()), B, X.data_ptr(), X.stride(0),
+              Y.data_ptr(), Y.stride(0), _stream(stream))
+    return Y
+
+
+def gemv_int8_grouped(ws, x: torch.Tensor, ys=None, stream=None):
+    """One launch for matrices sharing the input x (q/k/v, gate/up)."""
+    _need_cuda(x)
+    n = len(ws)
+    ys = [_vec_out(x, w.N) for w in ws] if ys is None else ys
+    arr = (Int8Weight * n)(*[w.struct() for w in ws])
+    yp = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    _lib.call("qz_gemv_int8_grouped", arr, n, x.data_ptr(), yp, _stream(stream))
+    return ys
+
+
+# ------------------------------------------------------------------ INT4 ---
+def int4o_layout(N: int, K: int, n_out: int) -> tuple[int, int]:
+    """(ld_out halves, ld_q4 bytes) of the packed INT4-outlier format."""
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _lib.call("qz_int4o_layout", N, K, n_out, ctypes.byref(a), ctypes.byref(b))
+    return a.value, b.value
+
+
+def default_n_out(K: int) -> int:
+    """Top-1% outlier channels, rounded up: ceil(K / 100)."""
+    return (K + 99) // 100
+
+
+@dataclass
+class Int4oMatrix:
+    """Outlier-aware INT4 matrix (format in include/qz.h)."""
+    perm: torch.Tensor     # int32 [K]
+    w_out: torch.Tensor    # fp16 [N, ld_out]
+    q4: torch.Tensor       # uint8 [N, ld_q4]
+    scale: torch.Tensor    # fp32 [N]
+    N: int
+    K: int
+    n_out: int
+
+    @property
+    def ld_out(self) -> int:
+        return self.w_out.shape[1]
+
+    @property
+    def ld_q4(self) -> int:
+        return self.q4.shape[1]
+
+    def struct(self) -> Int4oWeight:
+        return Int4oWeight(self.N, self.K, self.n_out, self.ld_out, self.ld_q4,
+                           self.perm.data_ptr(),
+                           self.w_out.data_ptr() if self.ld_out else None,
+                           self.q4.data_ptr() if self.ld_q4 else None,
+                           self.scale.data_ptr())
+
+    def nbytes(self) -> int:
+        """Algorithmic bytes: packed codes + fp16 outliers + fp32 row scales."""
+        kb = self.K - self.n_out
+        return self.N * ((kb + 1) // 2 + 2 * self.n_out + 4)
+
+    def padded_bytes(self) -> int:
+        return self.N * (self.ld_q4 + 2 * self.ld_out + 4)
+
+
+def saliency_accumulate(W: torch.Tensor, colsum: torch.Tensor, stream=None) -> torch.Tensor:
+    """colsum[j] += sum_i |W_ij| in units of 2^-24 (exact int64)."""
+    _need_cuda(W, colsum)
+    if W.stride(1) != 1 or W.stride(0) % 8 or W.data_ptr() % 16:
+        W = _padded_fp16(W)
+    N, K = W.shape
+    _lib.call("qz_saliency_accumulate", W.data_ptr(), N, K, W.stride(0), colsum.data_ptr(),
+              _stream(stream))
+    return colsum
+
+
+def select_outliers(colsum: torch.Tensor, x_profile: torch.Tensor, n_out: int,
+                    stream=None) -> torch.Tensor:
+    """global_perm_idx: top-n_out channels by colsum*|x_profile|, then the rest."""
+    _need_cuda(colsum, x_profile)
+    K = colsum.shape[0]
+    perm = torch.empty((K,), dtype=torch.int32, device=colsum.device)
+    _lib.call("qz_select_outliers", colsum.data_ptr(), x_profile.data_ptr(), K, n_out,
+              perm.data_ptr(), _stream(stream))
+    return perm
+
+
+def check_perm(perm: torch.Tensor, stream=None) -> int:
+    """0 if perm is a bijection of 0..K-1, 1 out of range, 2 duplicate (syncs)."""
+    _need_cuda(perm)
+    flag = torch.full((1,), -1, dtype=torch.int32, device=perm.device)
+    _lib.call("qz_check_perm", perm.data_ptr(), perm.shape[0], flag.data_ptr(),
+              _stream(stream))
+    return int(flag.item())
+
+
+def quantize_int4_outlier(W: torch.Tensor, perm: torch.Tensor, n_out: int,
+                          stream=None) -> Int4oMatrix:
+    """Split W by perm into fp16 outliers + per-row INT4 background, packed."""
+    _need_cuda(W, perm)
+    assert W.dtype == torch.float16 and W.dim() == 2
+    N, K = W.shape
+    if W.stride(1) != 1 or W.stride(0) % 8 or W.data_ptr() % 16:
+        W = _padded_fp16(W)
+    ld_out, ld_q4 = int4o_layout(N, K, n_out)
+    dev = W.device
+    w_out = torch.empty((N, ld_out), dtype=torch.float16, device=dev)
+    q4 = torch.empty((N, ld_q4), dtype=torch.uint8, device=dev)
+    scale = torch.empty((N,), dtype=torch.float32, device=dev)
+    _lib.call("qz_quantize_int4_outlier", W.data_ptr(), W.stride(0), perm.data_ptr(), N, K,
+              n_out, w_out.data_ptr() if ld_out else None, ld_out,
+              q4.data_ptr() if ld_q4 else None, ld_q4, scale.data_ptr(), _stream(stream))
+    return Int4oMatrix(perm, w_out, q4, scale, N, K, n_out)
+
+
+def gemv_int4_outlier(w: Int4oMatrix, x: torch.Tensor, y: torch.Tensor | None = None,
+                      stream=None):
+    """y = fp16(W_out @ x[perm[:n_out]] + s * (Q @ x[perm[n_out:]])), x [K]."""
+    _need_cuda(x)
+    y = _vec_out(x, w.N) if y is None else y
+    _lib.call("qz_gemv_int4_outlier", ctypes.byref(w.struct()), x.data_ptr(), y.data_ptr(),
+              _stream(stream))
+    return y
+
+
+def gemm_int4_outlier(w: Int4oMatrix, X: torch.Tensor, Y: torch.Tensor | None = None,
+                      stream=None):
+    _need_cuda(X)
+    B = X.shape[0]
+    Y = _vec_out(X, w.N, B) if Y is None else Y
+    _lib.call("qz_gemm_int4_outlier", ctypes.byref(w.struct()), B, X.data_ptr(), X.stride(0),
+              Y.data_ptr(), Y.stride(0), _stream(stream))
+    return Y
+
+
+def gemv_int4_outlier_grouped(ws, x: torch.Tensor, ys=None, stream=None):
+    _need_cuda(x)
+    n = len(ws)
+    ys = [_vec_out(x, w.N) for w in ws] if ys is None else ys
+    arr = (Int4oWeight * n)(*[w.struct() for w in ws])
+    yp = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    _lib.call("qz_gemv_int4_outlier_grouped", arr, n, x.data_ptr(), yp, _stream(stream))
+    return ys
+
+
+# ----------------------------------------------------------------- Pager ---
+class Pager:
+    """Double-buffered host->device layer streaming (qz_pager_*).
+
+    host_layers: pinned uint8 CPU tensors (one per layer); slots: two uint8
+    device tensors of equal size.  The tensors must outlive the pager.
+    """
+
+    def __init__(self, host_layers, slots, copy_stream, compute_stream):
+        self._keep = (list(host_layers), list(slots))
+        n = len(host_layers)
+        ptrs = (ctypes.c_void_p * n)(*[h.data_ptr() for h in host_layers])
+        sizes = (ctypes.c_size_t * n)(*[h.numel() for h in host_layers])
+        out = ctypes.c_void_p()
+        _lib.call("qz_pager_create", ptrs, sizes, n, slots[0].data_ptr(), slots[1].data_ptr(),
+                  slots[0].numel(), copy_stream.cuda_stream, compute_stream.cuda_stream,
+                  ctypes.byref(out))
+        self._h = out
+        self.slots = slots
+
+    def acquire(self, layer: int) -> int:
+        p = ctypes.c_void_p()
+        _lib.call("qz_pager_acquire", self._h, layer, ctypes.byref(p))
+        return p.value
+
+    def release(self, layer: int) -> None:
+        _lib.call("qz_pager_release", self._h, layer)
+
+    def inject_copy_failure(self, layer: int) -> None:
+        _lib.call("qz_pager_inject_copy_failure", self._h, layer)
+
+    def close(self) -> None:
+        if self._h:
+            _lib.call("qz_pager_destroy", self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

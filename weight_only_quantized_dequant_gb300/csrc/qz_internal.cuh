@@ -1,0 +1,69 @@
+// Internal declarations shared by the translation units of libqz.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/qz.h"
+
+namespace qz {
+
+// ---------------------------------------------------------------- errors --
+// Record a CUDA error for qz_last_cuda_error() and map it to a status.
+qz_status cuda_status(cudaError_t e);
+// cudaGetLastError() after a launch, mapped to a status.
+inline qz_status launch_status() { return cuda_status(cudaGetLastError()); }
+
+// Per-device facts, cached on first use (current device).
+struct DeviceInfo {
+  int sms = 0;
+  int max_smem_optin = 0;  // bytes of dynamic shared memory one CTA may use
+};
+qz_status device_info(DeviceInfo *out);
+
+// ------------------------------------------------------------ GEMV (CUDA cores)
+// One launch reads up to QZ_MAX_GROUP matrices that share the input.
+// Row r of the launch belongs to matrix m with row_end[m-1] <= r < row_end[m].
+struct GemvParams {
+  const __half *x;  // [B][ldx], original channel order
+  int64_t ldx;
+  const int32_t *perm;  // INT4 only: [K]
+  int K, n_out, kb;     // INT8: n_out = 0, kb = K
+  int cpr;              // 16-byte chunks per row of the code array that hold data
+  int ocpr;             // 16-byte chunks per row of w_out that hold data (INT4)
+  int n_mats;
+  int64_t total_rows;
+  int64_t row_end[QZ_MAX_GROUP];
+  const uint8_t *codes[QZ_MAX_GROUP];  // int8 codes or packed nibbles
+  int64_t ld_codes[QZ_MAX_GROUP];      // bytes between rows
+  const __half *w_out[QZ_MAX_GROUP];   // INT4 outlier block
+  int64_t ld_out[QZ_MAX_GROUP];        // halves between rows
+  const float *scale[QZ_MAX_GROUP];    // INT8: [1]; INT4: [N]
+  __half *y[QZ_MAX_GROUP];             // [B][ldy]
+  int64_t ldy;
+};
+
+// Shared-memory bytes the CUDA-core kernel needs for batch B.
+size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p);
+// Enqueue the CUDA-core GEMV for batch 1 <= B <= 4.
+qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s);
+
+// ------------------------------------------------------------ quantizers ---
+qz_status launch_quantize_int8(const __half *W, int64_t N, int64_t K,
+                               int64_t ldw, int8_t *q, int64_t ldq,
+                               float *scale, cudaStream_t s);
+qz_status launch_saliency(const __half *W, int64_t N, int64_t K, int64_t ldw,
+                          int64_t *colsum, cudaStream_t s);
+qz_status launch_select(const int64_t *colsum, const float *xprof, int64_t K,
+                        int64_t n_out, int32_t *perm, cudaStream_t s);
+qz_status launch_check_perm(const int32_t *perm, int64_t K, int32_t *flag,
+                            cudaStream_t s);
+qz_status launch_quantize_int4o(const __half *W, int64_t ldw,
+                                const int32_t *perm, int64_t N, int64_t K,
+                                int64_t n_out, __half *w_out, int64_t ld_out,
+                                uint8_t *q4, int64_t ld_q4, float *scale,
+                                cudaStream_t s);
+
+}  // namespace qz

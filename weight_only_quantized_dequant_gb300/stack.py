@@ -1,0 +1,150 @@
+"""Decoder-layer stack driver: one decode step = every quantized linear of
+every layer, four dependent launches per layer ({q,k,v}, {o}, {gate,up},
+{down}; matrices of one group share their input and run in one launch).
+
+The pages give no glue between the linears (attention, norms, activations are
+not part of the weight path), so each group reads its own seeded input
+vector.  Weights are generated, quantized and packed on the GPU by the
+library's own kernels; the fp16 originals are dropped after quantization.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+from . import api
+from . import synthetic as S
+
+
+@dataclass
+class Layer:
+    mats: dict                      # name -> Int8Matrix | Int4oMatrix
+    perms: dict = field(default_factory=dict)
+
+
+class LayerStack:
+    def __init__(self, wl: S.Workload, layers: int | None = None, batch: int = 1,
+                 device="cuda", keep_fp16: bool = False):
+        self.wl = wl
+        self.n_layers = wl.layers if layers is None else layers
+        self.batch = batch
+        self.device = torch.device(device)
+        self.layers: list[Layer] = []
+        self.fp16: list[dict] = []          # only if keep_fp16 (tests)
+        self.profiles: list[dict] = []
+        for l in range(self.n_layers):
+            self.layers.append(self._build_layer(l, keep_fp16))
+        self._alloc_io()
+
+    # ------------------------------------------------------------ build ---
+    def _build_layer(self, l: int, keep_fp16: bool) -> Layer:
+        wl, dev = self.wl, self.device
+        Ws = {m: S.weight(*wl.shape(m), S.matrix_seed(wl, l, m), device=dev, dist=wl.dist)
+              for m in S.MATS}
+        if keep_fp16:
+            self.fp16.append({m: W.cpu() for m, W in Ws.items()})
+        layer = Layer({})
+        if wl.fmt == "int8":
+            for m in S.MATS:
+                layer.mats[m] = api.quantize_int8(Ws[m])
+        else:
+            profs = {}
+            for table, members in S.PERM_TABLES.items():
+                K = wl.shape(members[0])[1]
+                n_out = api.default_n_out(K)
+                colsum = torch.zeros((K,), dtype=torch.int64, device=dev)
+                for m in members:
+                    api.saliency_accumulate(Ws[m], colsum)
+                prof = S.x_profile(K, n_out, S.profile_seed(wl, l, table), device=dev)
+                profs[table] = prof
+                perm = api.select_outliers(colsum, prof, n_out)
+                layer.perms[table] = perm
+                for m in members:
+                    layer.mats[m] = api.quantize_int4_outlier(Ws[m], perm, n_out)
+            if keep_fp16:
+                self.profiles.append({t: p.cpu() for t, p in profs.items()})
+        del Ws
+        return layer
+
+    def _alloc_io(self):
+        B, dev = self.batch, self.device
+        self.x = []   # [layer][group] -> [B, K] fp16
+        self.y = []   # [layer][group] -> list of [B, N] fp16
+        for l in range(self.n_layers):
+            xs, ys = [], []
+            for g, names in enumerate(S.GROUPS):
+                K = self.wl.shape(names[0])[1]
+                xs.append(S.activation(B, K, S.input_seed(self.wl, l, g), device=dev))
+                ys.append([torch.empty((B, self.wl.shape(m)[0]), dtype=torch.float16, device=dev)
+                           for m in names])
+            self.x.append(xs)
+            self.y.append(ys)
+
+    # ------------------------------------------------------------- run ----
+    def launches_per_step(self) -> int:
+        per_group = 1 if self.batch == 1 else None
+        if per_group is None:  # batched calls run one launch per matrix
+            return self.n_layers * len(S.MATS)
+        return self.n_layers * len(S.GROUPS)
+
+    def run_group(self, l: int, g: int, stream=None):
+        names = S.GROUPS[g]
+        mats = [self.layers[l].mats[m] for m in names]
+        x, ys = self.x[l][g], self.y[l][g]
+        int8 = self.wl.fmt == "int8"
+        if self.batch == 1:
+            outs = [y[0] for y in ys]
+            if len(mats) == 1:
+                fn = api.gemv_int8 if int8 else api.gemv_int4_outlier
+                fn(mats[0], x[0], outs[0], stream=stream)
+            else:
+                fn = api.gemv_int8_grouped if int8 else api.gemv_int4_outlier_grouped
+                fn(mats, x[0], outs, stream=stream)
+        else:
+            fn = api.gemm_int8 if int8 else api.gemm_int4_outlier
+            for w, y in zip(mats, ys):
+                fn(w, x, y, stream=stream)
+
+    def run_step(self, stream=None):
+        for l in range(self.n_layers):
+            for g in range(len(S.GROUPS)):
+                self.run_group(l, g, stream)
+
+    def capture(self) -> torch.cuda.CUDAGraph:
+        """CUDA graph of one decode step (all layers)."""
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self.run_step(s)          # warm-up outside capture
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        torch.cuda.synchronize(self.device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            self.run_step(s)
+        return graph
+
+    # --------------------------------------------------------- accounting --
+    def weight_bytes_per_layer(self) -> int:
+        """Algorithmic bytes of one layer's weights (codes, outliers, scales)."""
+        return sum(w.nbytes() for w in self.layers[0].mats.values())
+
+    def io_bytes_per_layer(self) -> int:
+        """Input and output vectors (+ the permutation tables for INT4)."""
+        B, wl = self.batch, self.wl
+        b = 0
+        for names in S.GROUPS:
+            K = wl.shape(names[0])[1]
+            b += 2 * B * K + sum(2 * B * wl.shape(m)[0] for m in names)
+            if wl.fmt == "int4o":
+                b += 4 * K
+        return b
+
+    def bytes_per_step(self) -> int:
+        return self.n_layers * (self.weight_bytes_per_layer() + self.io_bytes_per_layer())
+
+    def h2d_bytes_per_step(self) -> int:
+        return sum(x.numel() * 2 for xs in self.x for x in xs)
+
+    def d2h_bytes_per_step(self) -> int:
+        return sum(y.numel() * 2 for ys in self.y for yy in ys for y in yy)
