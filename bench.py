@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--extra", action="store_true",
                     help="also measure the other workloads (reported under 'workloads')")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="first L layers only (small case for profiling; not a bench line)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -200,8 +202,28 @@ def run_reference(a):
     print(json.dumps(out), flush=True)
 
 
+def copy_probe_gbs(device) -> float:
+    """Device-to-device copy of 2 GiB with torch (read + write bytes / time):
+    context for the HBM fallback peak, not a roofline denominator."""
+    import torch
+    a = torch.empty((1 << 31,), dtype=torch.uint8, device=device)
+    b = torch.empty_like(a)
+    for _ in range(3):
+        b.copy_(a)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        b.copy_(a)
+    e1.record()
+    torch.cuda.synchronize(device)
+    gbs = 2 * a.numel() * 10 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del a, b
+    torch.cuda.empty_cache()
+    return gbs
+
+
 def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
-            clocks=False, device=None):
+            clocks=False, device=None, layers=None):
     """Build the stack, capture one step, time it.  Returns a dict."""
     import torch
 
@@ -210,7 +232,7 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
 
     wl = S.WORKLOADS[wl_name]
     t_build = time.perf_counter()
-    st = ST.LayerStack(wl, batch=batch, device=device)
+    st = ST.LayerStack(wl, layers=layers, batch=batch, device=device)
     torch.cuda.synchronize()
     t_build = time.perf_counter() - t_build
 
@@ -360,7 +382,8 @@ def main():
     if dist_ctx is not None:
         dist_ctx.barrier()
 
-    r = measure(a.workload, 1, a.steps, a.warmup, dist_ctx, clocks=(rank == 0), device=device)
+    r = measure(a.workload, 1, a.steps, a.warmup, dist_ctx, clocks=(rank == 0), device=device,
+                layers=a.layers)
     ms_all = r["ms_per_step"]
     e2e_all = r["e2e_ms"]
     if dist_ctx is not None:
@@ -413,6 +436,7 @@ def main():
                 "unit": "GB/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "ms_per_step": round(e2e_all, 4)},
         "gpu_launches": r["launches_per_step"] * a.steps,
+        "copy_probe_gbs": round(copy_probe_gbs(device), 1) if a.layers is None else None,
         "clocks": r.get("clocks"),
     }
     if extra:

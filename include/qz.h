@@ -24,9 +24,11 @@
  *     that returns an error has enqueued nothing (QZ_ERR_CUDA excepted: the
  *     launch itself failed, and cudaGetLastError's code is kept in
  *     qz_last_cuda_error(), per host thread).
- *   - Alignment: every device pointer of a matrix or vector must be 16-byte
- *     aligned, and every ld* must make rows 16-byte multiples (ld % 8 == 0 for
- *     fp16, ld % 16 == 0 for int8/uint8).  Violations return QZ_ERR_ALIGNMENT.
+ *   - Alignment: every device pointer of a MATRIX (W, q, q4, w_out) must be
+ *     16-byte aligned and its ld* must make rows 16-byte multiples (ld % 8 == 0
+ *     for fp16, ld % 16 == 0 for int8/uint8); activation and output vectors
+ *     (x, X, y, Y) need only the 2-byte alignment of fp16, with any ld >= the
+ *     row length.  Violations return QZ_ERR_ALIGNMENT.
  *   - Inputs must be finite.  Non-finite weights or profiles give unspecified
  *     (but memory-safe) results.
  *   - No exception, abort or device trap is ever raised by the library.

@@ -100,14 +100,14 @@ def test_gemv_int8_validation(lib):
     assert lib.qz_gemv_int8(None, P, P, None) == INVAL
     assert lib.qz_gemv_int8(ctypes.byref(w), None, P, None) == INVAL
     assert lib.qz_gemv_int8(ctypes.byref(w), P, None, None) == INVAL
-    assert lib.qz_gemv_int8(ctypes.byref(w), PU, P, None) == ALIGN
+    assert lib.qz_gemv_int8(ctypes.byref(w), P + 1, P, None) == ALIGN     # odd fp16 pointer
     assert lib.qz_gemv_int8(ctypes.byref(_w8(ldq=40)), P, P, None) == ALIGN
     assert lib.qz_gemv_int8(ctypes.byref(_w8(ldq=16)), P, P, None) == INVAL
     assert lib.qz_gemv_int8(ctypes.byref(_w8(K=57360, ldq=57360)), P, P, None) == UNSUP
     assert lib.qz_gemm_int8(ctypes.byref(w), 65, P, 32, P, 8, None) == UNSUP
     assert lib.qz_gemm_int8(ctypes.byref(w), 0, P, 32, P, 8, None) == INVAL
     assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 16, P, 8, None) == INVAL   # ldx < K
-    assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 36, P, 8, None) == ALIGN   # ldx*2 % 16
+    assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 32, P + 1, 8, None) == ALIGN
 
 
 def test_grouped_int8_validation(lib):

@@ -40,6 +40,18 @@ def assert_close(y_gpu, y_ref, a_ref, what=""):
     return float((err / tol).max())
 
 
+def smem_limit() -> int:
+    return torch.cuda.get_device_properties(0).shared_memory_per_block_optin
+
+
+def cuda_core_smem(int4: bool, B: int, K: int, n_out: int = 0) -> int:
+    """Shared memory the CUDA-core kernel stages for a batch of B inputs."""
+    if not int4:
+        return B * (-(-K // 16)) * 64
+    kb = K - n_out
+    return B * ((-(-((kb + 1) // 2) // 16)) * 128 + (-(-n_out // 8)) * 32)
+
+
 def padded_rows(X: torch.Tensor) -> torch.Tensor:
     """View of X whose rows start on 16-byte boundaries."""
     B, K = X.shape
@@ -81,6 +93,11 @@ def test_int8_gemm_cuda_cores(N, K, B):
     W = S.weight(N, K, 2000 + N + K, device=DEV)
     X = padded_rows(S.activation(B, K, 3000 + B, device=DEV))
     w = qz().quantize_int8(W)
+    if cuda_core_smem(False, B, K) > smem_limit():
+        with pytest.raises(qz().QzError) as ei:
+            qz().gemm_int8(w, X)
+        assert ei.value.name == "QZ_ERR_UNSUPPORTED"
+        return
     Y = qz().gemv_int8(w, X[0]).unsqueeze(0) if B == 1 else qz().gemm_int8(w, X)
     q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
     y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, X.cpu().numpy())
@@ -189,6 +206,11 @@ def test_int4_gemm_cuda_cores(N, K, n_out, B):
     W, prof, perm = _int4_inputs(N, K, n_out, 5000 + K + n_out)
     w = qz().quantize_int4_outlier(W, perm, n_out)
     X = padded_rows(S.activation(B, K, 6000 + B, device=DEV))
+    if cuda_core_smem(True, B, K, n_out) > smem_limit():
+        with pytest.raises(qz().QzError) as ei:
+            qz().gemm_int4_outlier(w, X)
+        assert ei.value.name == "QZ_ERR_UNSUPPORTED"
+        return
     Y = qz().gemv_int4_outlier(w, X[0]).unsqueeze(0) if B == 1 else qz().gemm_int4_outlier(w, X)
     wo, q4, s = O.int4o_quantize(W.cpu().numpy(), perm.cpu().numpy(), n_out)
     y_ref, a_ref = O.int4o_product_ref(wo, q4, s, perm.cpu().numpy(), n_out, K, X.cpu().numpy())
