@@ -39,6 +39,10 @@ def parse():
     ap.add_argument("--extra", action="store_true",
                     help="also measure the other workloads (reported under 'workloads')")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--paged", action="store_true",
+                    help="also stream the 70B and Gemma stacks through the pager")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch without programmatic dependent launch")
     ap.add_argument("--layers", type=int, default=None,
                     help="first L layers only (small case for profiling; not a bench line)")
     a = ap.parse_args()
@@ -223,7 +227,7 @@ def copy_probe_gbs(device) -> float:
 
 
 def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
-            clocks=False, device=None, layers=None):
+            clocks=False, device=None, layers=None, overlap=True):
     """Build the stack, capture one step, time it.  Returns a dict."""
     import torch
 
@@ -257,8 +261,12 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
     x_host = x_dev.cpu().pin_memory()
     y_host = torch.empty(y_dev.shape, dtype=torch.float16).pin_memory()
 
-    # graph of one step with timing events around the dominant launch
+    # Two graphs of one step: the plain one is the timed step; the second
+    # brackets every launch of the dominant group with timing events (event
+    # nodes serialise their neighbours, so it is timed separately).
+    from weight_only_quantized_dequant_gb300 import api
     s = torch.cuda.Stream(device=device)
+
     def _ev():  # external: a timing node inside the captured graph
         try:
             return torch.cuda.Event(enable_timing=True, external=True)
@@ -266,22 +274,27 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
             return torch.cuda.Event(enable_timing=True)
     ev = [(_ev(), _ev()) for _ in range(st.n_layers)]
 
-    def step(stream):
+    def step(stream, events):
         for l in range(st.n_layers):
             for g in range(len(S.GROUPS)):
-                if g == DOMINANT_GROUP:
+                if events and g == DOMINANT_GROUP:
                     ev[l][0].record(stream)
                 st.run_group(l, g, stream)
-                if g == DOMINANT_GROUP:
+                if events and g == DOMINANT_GROUP:
                     ev[l][1].record(stream)
 
+    api.set_overlap(overlap)
     s.wait_stream(torch.cuda.current_stream(device))
     with torch.cuda.stream(s):
-        step(s)
+        step(s, False)
     torch.cuda.synchronize(device)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=s):
-        step(s)
+        step(s, False)
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev, stream=s):
+        step(s, True)
+    api.set_overlap(False)
     torch.cuda.synchronize(device)
 
     def barrier():
@@ -308,8 +321,20 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
     if clk:
         clk.__exit__(None, None, None)
     ms = t0.elapsed_time(t1) / steps
-    dom_ms = [a.elapsed_time(b) for a, b in ev]          # last timed step
-    dom_avg_ms = sum(dom_ms) / len(dom_ms)
+    # instrumented graph: same warm-up and step count, dominant launches timed
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            graph_ev.replay()
+    barrier()
+    dom_sum, n_dom = 0.0, 0
+    with torch.cuda.stream(s):
+        for _ in range(steps):
+            graph_ev.replay()
+            s.synchronize()
+            dom_sum += sum(a.elapsed_time(b) for a, b in ev)
+            n_dom += len(ev)
+    barrier()
+    dom_avg_ms = dom_sum / n_dom
 
     # e2e: pinned host inputs -> device, step, outputs -> pinned host
     with torch.cuda.stream(s):
@@ -356,6 +381,55 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
     return out
 
 
+def h2d_probe_gbs(device, nbytes=1 << 30) -> float:
+    """Pinned host -> device copy bandwidth of the link on this machine."""
+    import torch
+    h = torch.empty((nbytes,), dtype=torch.uint8).pin_memory()
+    d = torch.empty((nbytes,), dtype=torch.uint8, device=device)
+    for _ in range(2):
+        d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        d.copy_(h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize(device)
+    return nbytes * 5 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+
+def measure_paged(wl_name: str, steps: int, warmup: int, device, distinct: int = 4):
+    """Stack streamed layer by layer from pinned host memory through the
+    pager (two device slots, copy stream + compute stream)."""
+    import torch
+
+    from weight_only_quantized_dequant_gb300 import stack as ST
+    from weight_only_quantized_dequant_gb300 import synthetic as S
+
+    ps = ST.PagedStack(S.WORKLOADS[wl_name], distinct=distinct, device=device)
+    cs = ps.compute_stream
+    for _ in range(warmup):
+        ps.run_step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    for _ in range(steps):
+        ps.run_step()
+    e1.record(cs)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    out = {"workload": wl_name, "layers": ps.n_layers, "distinct_host_layers": ps.distinct,
+           "layer_bytes": ps.blob_bytes, "ms_per_step": ms,
+           "us_per_layer": ms * 1e3 / ps.n_layers,
+           "h2d_gbs": ps.n_layers * ps.blob_bytes / (ms * 1e-3) / 1e9,
+           "link_probe_gbs": h2d_probe_gbs(device)}
+    out["link_frac"] = out["h2d_gbs"] / out["link_probe_gbs"]
+    ps.close()
+    del ps
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     a = parse()
     if a.impl == "reference":
@@ -383,7 +457,7 @@ def main():
         dist_ctx.barrier()
 
     r = measure(a.workload, 1, a.steps, a.warmup, dist_ctx, clocks=(rank == 0), device=device,
-                layers=a.layers)
+                layers=a.layers, overlap=not a.no_overlap)
     ms_all = r["ms_per_step"]
     e2e_all = r["e2e_ms"]
     if dist_ctx is not None:
@@ -394,11 +468,16 @@ def main():
     extra = {}
     if a.extra and rank == 0:
         for name, b in [("llama32_3b_int4o", 1), ("llama_7b_int4o", 1), ("llama_7b_int4o", 4),
-                        ("llama_70b_int4o", 1)]:
-            e = measure(name, b, max(5, a.steps // 2), a.warmup, None, device=device)
+                        ("llama_7b_int4o", 16), ("llama_7b_int4o", 64), ("llama_70b_int4o", 1)]:
+            e = measure(name, b, max(5, a.steps // 2), a.warmup, None, device=device,
+                        overlap=not a.no_overlap)
             extra[f"{name}_b{b}"] = {k: e[k] for k in ("us_per_layer", "gbs", "ms_per_step",
                                                           "stack_gb")}
             extra[f"{name}_b{b}"]["dominant_gbs"] = e["dominant"]["gbs"]
+
+    if a.paged and rank == 0:
+        for name in ("llama_70b_int4o", "gemma2_9b_int8"):
+            extra[f"{name}_paged"] = measure_paged(name, max(2, a.steps // 10), 1, device)
 
     cpu = None
     if rank == 0 and not a.no_cpu:
@@ -418,8 +497,11 @@ def main():
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_all, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": a.workload, "format": "int8 per-tensor", "batch": 1,
+        "config": {"workload": a.workload,
+                   "format": "int8 per-tensor" if "int8" in a.workload else "int4 outlier-aware",
+                   "batch": 1,
                    "layers": r["layers"], "launches_per_layer": 4, "graph": True,
+                   "overlap": not a.no_overlap,
                    "l2": f"inputs larger than L2 ({r['stack_gb']:.2f} GB stack > 129 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_layer": round(ms_all * 1e3 / r["layers"], 3),

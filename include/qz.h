@@ -64,6 +64,23 @@ int qz_version(void);
 /* The cudaError_t of the last QZ_ERR_CUDA returned on this host thread. */
 int qz_last_cuda_error(void);
 
+/* Launch overlap for the GEMV/GEMM entry points, per host thread (off by
+ * default).  When on, each product kernel is launched with programmatic
+ * dependent launch: it may start while the preceding kernel on the stream is
+ * still running, prefetches the first weight rows of each CTA into L2, and
+ * waits for that kernel (griddepcontrol.wait) before it reads x or writes y.
+ * The caller promises that no work still in flight on the stream writes the
+ * WEIGHTS of the call (q/q4/w_out/scale/perm); inputs and outputs keep normal
+ * stream order.  Returns QZ_ERR_INVALID_ARG unless enable is 0 or 1. */
+qz_status qz_set_overlap(int enable);
+/* The current host thread's overlap setting (0 or 1). */
+int qz_get_overlap(void);
+
+/* The library's device error word: 0, or 1 if a kernel gave up a bounded
+ * wait (its output is then incomplete).  Synchronous (reads device memory);
+ * clear = 1 resets it.  Not for use during stream capture. */
+qz_status qz_device_error(int *code, int clear);
+
 /* Largest batch the GEMM entry points accept. */
 #define QZ_MAX_BATCH 64
 /* Largest number of matrices in one grouped launch. */
@@ -101,9 +118,10 @@ qz_status qz_gemv_int8(const qz_int8_weight *w, const qz_half *x, qz_half *y,
 
 /* Y[b][i] = fp16( scale * sum_j q[i][j] * X[b][j] ) for b < B.
  * X [B][ldx], Y [B][ldy]; 1 <= B <= QZ_MAX_BATCH.  B <= 4 runs on CUDA
- * cores; larger batches on the tensor cores.  QZ_ERR_UNSUPPORTED if the
- * batch's inputs do not fit in shared memory (4*B*K bytes > 200 KiB for
- * B <= 4). */
+ * cores when the batch's fp32 inputs fit in shared memory (about 4*B*K
+ * bytes <= 227 KiB); larger batches, and B = 2..4 beyond that, run on the
+ * tensor cores (tcgen05, fp16 x fp16 products of the exact codes, fp32
+ * accumulation in tensor memory). */
 qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X,
                        int64_t ldx, qz_half *Y, int64_t ldy, qz_stream s);
 
@@ -185,7 +203,9 @@ qz_status qz_gemv_int4_outlier(const qz_int4o_weight *w, const qz_half *x,
                                qz_half *y, qz_stream s);
 
 /* The same for a batch: X [B][ldx], Y [B][ldy], 1 <= B <= QZ_MAX_BATCH; same
- * CUDA-core / tensor-core split and shared-memory limit as qz_gemm_int8. */
+ * CUDA-core / tensor-core split as qz_gemm_int8.  On the tensor cores the
+ * outlier and background products accumulate separately (two accumulators)
+ * and meet as y = D_out + s_i * D_bg. */
 qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B,
                                const qz_half *X, int64_t ldx, qz_half *Y,
                                int64_t ldy, qz_stream s);

@@ -52,6 +52,19 @@ def test_struct_layouts():
     assert ctypes.sizeof(_lib.Int4oWeight) == 72
 
 
+def test_overlap_setting_is_per_thread_and_validated(lib):
+    import threading
+    assert lib.qz_get_overlap() == 0
+    assert lib.qz_set_overlap(2) == INVAL
+    assert lib.qz_set_overlap(1) == OK and lib.qz_get_overlap() == 1
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(lib.qz_get_overlap()))
+    t.start()
+    t.join()
+    assert seen == [0]
+    assert lib.qz_set_overlap(0) == OK and lib.qz_get_overlap() == 0
+
+
 def test_version_and_status_strings(lib):
     assert lib.qz_version() >= 10000
     for code, name in _lib.STATUS.items():

@@ -45,6 +45,9 @@ _SIGS = {
     "qz_status_string": (c_char_p, [c_int]),
     "qz_version": (c_int, []),
     "qz_last_cuda_error": (c_int, []),
+    "qz_set_overlap": (_S, [c_int]),
+    "qz_get_overlap": (c_int, []),
+    "qz_device_error": (_S, [POINTER(c_int), c_int]),
     "qz_quantize_int8": (_S, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_int64,
                               c_void_p, c_void_p]),
     "qz_gemv_int8": (_S, [POINTER(Int8Weight), c_void_p, c_void_p, c_void_p]),

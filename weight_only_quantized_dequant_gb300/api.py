@@ -37,6 +37,23 @@ def _need_cuda(*ts):
             raise ValueError("libqz works on CUDA tensors only (no CPU fallback)")
 
 
+def set_overlap(enable: bool) -> None:
+    """Programmatic dependent launch for this host thread's product calls
+    (see qz_set_overlap): only when no in-flight work writes the weights."""
+    _lib.call("qz_set_overlap", 1 if enable else 0)
+
+
+def get_overlap() -> bool:
+    return bool(_lib.load().qz_get_overlap())
+
+
+def device_error(clear: bool = True) -> int:
+    """The library's device error word (1 = a kernel gave up a bounded wait)."""
+    v = ctypes.c_int()
+    _lib.call("qz_device_error", ctypes.byref(v), 1 if clear else 0)
+    return v.value
+
+
 # ------------------------------------------------------------------ INT8 ---
 @dataclass
 class Int8Matrix:

@@ -29,7 +29,8 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;  // 16-byte chunks per lane in flight
+constexpr int kUnroll = 6;  // 16-byte chunks per lane in flight
+constexpr int64_t kPrefetchBytes = 64 * 1024;  // per CTA, issued before the wait
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   uint4 r;
@@ -51,32 +52,47 @@ __device__ __forceinline__ int gidx(int c, int g) {
   else return c * 2 + (g ^ ((c >> 2) & 1));
 }
 
+// (a & b) ^ c in one LOP3 (truth table 0x6A).
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Shared-memory read of one staged granule (4 fp32 inputs) at a byte offset.
+__device__ __forceinline__ float4 lds(const float4 *base, uint32_t byte_off) {
+  return *reinterpret_cast<const float4 *>(reinterpret_cast<const char *>(base) + byte_off);
+}
+
 // 32 nibbles of one chunk against the staged (pre-scaled) input.
 // For nibble p (0..3) of a half-word, (w & 0xF<<4p) ^ (0x4B000000 | 8<<4p) is
 // the fp32 number 2^23 + (q+8)*16^p; subtracting 2^23 + 8*16^p leaves q*16^p
 // exactly, and the input was staged as x*16^-p, so each FMA adds q*x exactly.
+// goff[g] is the lane's byte offset of granule g inside its chunk (the swizzle
+// only depends on the lane), cbase the byte offset of the chunk, bstride the
+// bytes between batch rows of the staged input.
 template <int B>
 __device__ __forceinline__ void int4_chunk(const uint4 v, const float4 *xs,
-                                           int gstride, int c,
-                                           float2 (&acc)[B][2]) {
+                                           const uint32_t (&goff)[8], uint32_t cbase,
+                                           uint32_t bstride, float2 (&acc)[B][2]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t ww = h ? (w[k] >> 16) : w[k];
-      const float f0 = __uint_as_float((ww & 0x000Fu) ^ 0x4B000008u);
-      const float f1 = __uint_as_float((ww & 0x00F0u) ^ 0x4B000080u);
-      const float f2 = __uint_as_float((ww & 0x0F00u) ^ 0x4B000800u);
-      const float f3 = __uint_as_float((ww & 0xF000u) ^ 0x4B008000u);
+      const float f0 = __uint_as_float(and_xor(ww, 0x000Fu, 0x4B000008u));
+      const float f1 = __uint_as_float(and_xor(ww, 0x00F0u, 0x4B000080u));
+      const float f2 = __uint_as_float(and_xor(ww, 0x0F00u, 0x4B000800u));
+      const float f3 = __uint_as_float(and_xor(ww, 0xF000u, 0x4B008000u));
       const float2 qa = __fadd2_rn(make_float2(f0, f1),
                                    make_float2(-8388616.0f, -8388736.0f));
       const float2 qb = __fadd2_rn(make_float2(f2, f3),
                                    make_float2(-8390656.0f, -8421376.0f));
-      const int g = gidx<8>(c, 2 * k + h);
+      const uint32_t o = cbase + goff[2 * k + h];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        const float4 xv = xs[b * gstride + g];
+        const float4 xv = lds(xs, o + b * bstride);
         acc[b][0] = __ffma2_rn(qa, make_float2(xv.x, xv.y), acc[b][0]);
         acc[b][1] = __ffma2_rn(qb, make_float2(xv.z, xv.w), acc[b][1]);
       }
@@ -89,8 +105,8 @@ __device__ __forceinline__ void int4_chunk(const uint4 v, const float4 *xs,
 // subtracting 2^23 + 128 leaves q exactly.
 template <int B>
 __device__ __forceinline__ void int8_chunk(const uint4 v, const float4 *xs,
-                                           int gstride, int c,
-                                           float2 (&acc)[B][2]) {
+                                           const uint32_t (&goff)[8], uint32_t cbase,
+                                           uint32_t bstride, float2 (&acc)[B][2]) {
   const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u,
                          v.z ^ 0x80808080u, v.w ^ 0x80808080u};
 #pragma unroll
@@ -103,10 +119,10 @@ __device__ __forceinline__ void int8_chunk(const uint4 v, const float4 *xs,
                                  make_float2(-8388736.0f, -8388736.0f));
     const float2 qb = __fadd2_rn(make_float2(f2, f3),
                                  make_float2(-8388736.0f, -8388736.0f));
-    const int g = gidx<4>(c, k);
+    const uint32_t o = cbase + goff[k];
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-      const float4 xv = xs[b * gstride + g];
+      const float4 xv = lds(xs, o + b * bstride);
       acc[b][0] = __ffma2_rn(qa, make_float2(xv.x, xv.y), acc[b][0]);
       acc[b][1] = __ffma2_rn(qb, make_float2(xv.z, xv.w), acc[b][1]);
     }
@@ -120,12 +136,13 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 template <bool INT4, int B>
-__global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1))
+__global__ void __launch_bounds__(kThreads, (B == 1 ? 2 : 1))
     gemv_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ float4 smem[];
   constexpr int GPC = INT4 ? 8 : 4;       // granules per code chunk
   constexpr int EPC = GPC * 4;            // elements per code chunk
-  const int gstride = p.cpr * GPC;        // background granules per batch row
+  const int cps = p.cpr > 32 ? p.cpr : 32;  // staged chunks (>= 32: one per lane)
+  const int gstride = cps * GPC;          // background granules per batch row
   const int ostride = p.ocpr * 2;         // outlier granules per batch row
   float4 *xs = smem;
   float4 *xo = smem + B * gstride;
@@ -133,13 +150,36 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1))
   const int64_t r0 = p.total_rows * blockIdx.x / gridDim.x;
   const int64_t r1 = p.total_rows * (blockIdx.x + 1) / gridDim.x;
 
-  // x may be produced by the previous kernel on the stream (no-op unless the
-  // launch allowed programmatic overlap).
+  // The first rows of this CTA are pulled into L2 right away.  With
+  // programmatic overlap this CTA may start while the previous kernel on the
+  // stream is still running; the weights are static by the caller's promise,
+  // and x (which that kernel may produce) is only read after the wait.
+  if (threadIdx.x == 0) {
+    int64_t budget = kPrefetchBytes;
+    int64_t r = r0;
+    for (int m = 0; m < p.n_mats && budget > 0 && r < r1; ++m) {
+      const int64_t m_lo = m ? p.row_end[m - 1] : 0, m_hi = p.row_end[m];
+      if (r >= m_hi) continue;
+      const int64_t e = r1 < m_hi ? r1 : m_hi;
+      int64_t bytes = (e - r) * p.ld_codes[m];
+      if (bytes > budget) bytes = budget;
+      bytes &= ~(int64_t)15;
+      if (bytes > 0) {
+        const uint8_t *src = p.codes[m] + (r - m_lo) * p.ld_codes[m];
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)bytes)
+                     : "memory");
+      }
+      budget -= bytes;
+      r = e;
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // let the next kernel on the stream get scheduled as SMs free up
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- stage x (gathered through perm for INT4) in shared memory ---------
   float *xsf = reinterpret_cast<float *>(xs);
-  const int elems = p.cpr * EPC;
+  const int elems = cps * EPC;
 #pragma unroll 1
   for (int b = 0; b < B; ++b) {
     const __half *xb = p.x + b * p.ldx;
@@ -174,6 +214,26 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1))
 
   // ---- one warp per row ----------------------------------------------------
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Lane L reads chunks c = L + 32j.  The staging swizzle of a granule only
+  // depends on c's low bits, i.e. on the lane, so the byte offsets of the
+  // GPC granules inside a chunk are fixed per lane.
+  uint32_t goff[8];
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int sw = GPC == 8 ? (lane & 7) : ((lane >> 1) & 3);
+    goff[g] = (uint32_t)((lane * GPC + ((g % GPC) ^ sw)) * 16);
+  }
+  const uint32_t bstride = (uint32_t)gstride * 16u;
+  constexpr uint32_t kChunkStep = 32u * GPC * 16u;  // bytes between a lane's chunks
+  // Warp-uniform trip counts: rounds where every lane has a chunk run without
+  // predicates; the last partial round (if any) runs predicated, and lanes
+  // past the row's end load zero codes against a valid staged slot (at least
+  // 32 chunks are always staged), so they add exact zeros.  No divergence.
+  const int cpr = p.cpr;
+  const int Jfull = cpr >> 5;             // rounds in which all 32 lanes have a chunk
+  const int Jw = (cpr + 31) >> 5;         // all rounds
+  const int64_t total_rows = p.total_rows;
+  (void)total_rows;
 #pragma unroll 1
   for (int64_t r = r0 + warp; r < r1; r += kWarps) {
     int m = 0;
@@ -182,26 +242,53 @@ __global__ void __launch_bounds__(kThreads, (B <= 2 ? 2 : 1))
       m += (t < p.n_mats - 1 && r >= p.row_end[t]) ? 1 : 0;
     const int64_t i = r - (m ? p.row_end[m - 1] : 0);
     const float s = INT4 ? __ldg(p.scale[m] + i) : __ldg(p.scale[m]);
-    const uint4 *row = reinterpret_cast<const uint4 *>(p.codes[m] + i * p.ld_codes[m]);
+    const int64_t ldc = p.ld_codes[m];
+    const uint4 *row = reinterpret_cast<const uint4 *>(p.codes[m] + i * ldc) + lane;
+    // Bulk-prefetch the warp's next row into L2 while this one is computed:
+    // DRAM keeps streaming independently of this warp's load-use latency.
+    // (Skipped when the next row belongs to the next matrix of a group.)
+    if (lane == 0 && cpr > 0 && r + kWarps < r1 && r + kWarps < p.row_end[m]) {
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       p.codes[m] + (i + kWarps) * ldc),
+                   "r"((uint32_t)cpr * 16u)
+                   : "memory");
+      if (INT4 && p.ocpr)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                         p.w_out[m] + (i + kWarps) * p.ld_out[m]),
+                     "r"((uint32_t)p.ocpr * 16u)
+                     : "memory");
+    }
 
     float2 acc[B][2];
 #pragma unroll
     for (int b = 0; b < B; ++b) acc[b][0] = acc[b][1] = make_float2(0.f, 0.f);
 
+    int j = 0;
+    uint32_t cbase = 0;
+    const uint4 *rp = row;
 #pragma unroll 1
-    for (int c0 = lane; c0 < p.cpr; c0 += 32 * kUnroll) {
+    for (; j + kUnroll <= Jfull; j += kUnroll, cbase += kUnroll * kChunkStep, rp += 32 * kUnroll) {
       uint4 v[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int c = c0 + 32 * u;
-        v[u] = c < p.cpr ? ld_stream(row + c) : make_uint4(0, 0, 0, 0);
-      }
+      for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream(rp + 32 * u);
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int c = c0 + 32 * u;
-        if (c < p.cpr) {
-          if constexpr (INT4) int4_chunk<B>(v[u], xs, gstride, c, acc);
-          else int8_chunk<B>(v[u], xs, gstride, c, acc);
+        if constexpr (INT4) int4_chunk<B>(v[u], xs, goff, cbase + u * kChunkStep, bstride, acc);
+        else int8_chunk<B>(v[u], xs, goff, cbase + u * kChunkStep, bstride, acc);
+      }
+    }
+    if (j < Jw) {  // tail: at most kUnroll rounds, the last one possibly partial
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        v[u] = (j + u < Jw && lane + 32 * (j + u) < cpr) ? ld_stream(rp + 32 * u)
+                                                         : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (j + u < Jw) {  // warp-uniform
+          const uint32_t cb = lane + 32 * (j + u) < cpr ? cbase + u * kChunkStep : 0u;
+          if constexpr (INT4) int4_chunk<B>(v[u], xs, goff, cb, bstride, acc);
+          else int8_chunk<B>(v[u], xs, goff, cb, bstride, acc);
         }
       }
     }
@@ -257,10 +344,23 @@ qz_status launch_t(const GemvParams &p, cudaStream_t s) {
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
   if (e != cudaSuccess) return cuda_status(e);
   if (occ < 1) return QZ_ERR_UNSUPPORTED;
-  int64_t want = (p.total_rows + kWarps - 1) / kWarps;
-  int64_t grid = (int64_t)di.sms * occ;
-  if (want < grid) grid = want;
-  kern<<<(unsigned)grid, kThreads, smem, s>>>(p);
+  // Whole waves only: every SM gets the same number of CTAs (and CTAs equal
+  // row ranges), so no SM carries a second CTA while another idles.
+  int64_t per_sm = occ;
+  while (per_sm > 1 && (int64_t)di.sms * per_sm * kWarps > p.total_rows * 2) --per_sm;
+  int64_t grid = (int64_t)di.sms * per_sm;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.overlap ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return cuda_status(e);
   return launch_status();
 }
 
@@ -268,7 +368,8 @@ qz_status launch_t(const GemvParams &p, cudaStream_t s) {
 
 size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p) {
   const size_t gpc = int4 ? 8 : 4;
-  const size_t per_b = ((size_t)p.cpr * gpc + (int4 ? (size_t)p.ocpr * 2 : 0)) * 16;
+  const size_t cps = p.cpr > 32 ? (size_t)p.cpr : 32;
+  const size_t per_b = (cps * gpc + (int4 ? (size_t)p.ocpr * 2 : 0)) * 16;
   return per_b * (size_t)B;
 }
 

@@ -1,0 +1,441 @@
+// Tensor-core dequant-GEMM (tcgen05 + TMEM) for batches the CUDA-core GEMV
+// does not cover: B > 4, or B in 2..4 when the staged inputs exceed shared
+// memory.  Same math as the GEMV ("Open Origin - ELG Stream Layer", INT8
+// Quantization & Direct Mapping; "On-The-Fly Weight Synthesizer (OTF-LLM
+// Engine)", Architecture & Key Innovations: outlier product + background
+// product), now a dense contraction Y[b][i] = sum_k A[i][k] * X[b][k]:
+//
+//  * A (weights) is the MMA's M side: a CTA owns a tile of 128 output rows.
+//    Producer warps turn packed codes into exact fp16 integers in registers
+//    (INT4: one LOP3 on the 0x6400 exponent per nibble pair; INT8: one PRMT
+//    per byte pair) and store them in the canonical K-major no-swizzle layout
+//    (8x16-byte core matrices).  No fp16 weight tensor exists in HBM.
+//  * B (activations, N = batch rounded up to 16) is gathered through the
+//    permutation straight into the same layout, in the k order the nibble
+//    conversion produces.
+//  * One thread issues tcgen05.mma (kind::f16, fp32 accumulate) into two
+//    TMEM accumulators: outlier channels and INT4 background, so that the
+//    per-row scale multiplies the background only: y = D_out + s_i * D_bg.
+//  * A 4-stage mbarrier ring decouples producers and the MMA thread; every
+//    wait is bounded in time and reports a timeout through a device flag.
+#include "qz_internal.cuh"
+
+namespace qz {
+
+// Device-side error word of the library (0 = none).  Written only when a
+// bounded wait gives up; read and cleared by qz_device_error().
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kM = 128;         // weight rows per tile (MMA M)
+constexpr int kKT = 64;         // K elements per pipeline stage
+constexpr int kStages = 4;
+constexpr int kProducers = 128;  // 4 warps, one weight row each
+constexpr int kThreadsTc = kProducers + 32;  // + the MMA warp
+constexpr int kABytes = kM * kKT * 2;         // 16 KiB per stage
+constexpr uint32_t kLBO = 128;   // bytes between core matrices along K
+constexpr uint32_t kSBO = 1024;  // bytes between 8-row groups (kKT/8 * 128)
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+
+struct TcParams {
+  GemvParams g;
+  int B;                // batch rows
+  int Np;               // MMA N: B rounded up to 16
+  int ko;               // K tiles of the outlier block
+  int kbt;              // K tiles of the background block
+  int n_tiles[QZ_MAX_GROUP];
+  int tile_end[QZ_MAX_GROUP];
+  int64_t mat_rows[QZ_MAX_GROUP];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of the given parity; false (and the error flag set) if
+// it does not complete within kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *abort_flag) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = gtimer();
+  for (;;) {
+    if (mbar_try(bar, parity)) return true;
+    if (*(volatile int *)abort_flag) return false;
+    if (gtimer() - t0 > kWaitNs) {
+      atomicExch(&g_device_error, 1);
+      *(volatile int *)abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+// Canonical K-major, no-swizzle shared-memory matrix descriptor.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(kLBO >> 4) << 16;
+  d |= (uint64_t)(kSBO >> 4) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  return d;                // base offset 0, relative LBO, no swizzle
+}
+
+// Instruction descriptor: kind::f16, A = B = f16, D = f32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Byte offset of (row r, k-slot c) in a canonical tile.
+__device__ __forceinline__ uint32_t core_off(int r, int c) {
+  return (uint32_t)((r >> 3) * kSBO + (c >> 3) * kLBO + (r & 7) * 16 + (c & 7) * 2);
+}
+
+// The nibble conversion below yields k slots in the order 0,4,1,5,2,6,3,7 of
+// every group of 8 elements; the activations are staged in the same order.
+__device__ __forceinline__ int slot_elem(int c) {
+  const int s = c & 7;
+  return (c & ~7) + ((s & 1) ? 4 + (s >> 1) : (s >> 1));
+}
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+template <bool INT4>
+__global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_constant__ TcParams tp) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const GemvParams &p = tp.g;
+  // 1024-byte aligned carve-up
+  uint8_t *base = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int bBytes = tp.Np * kKT * 2;
+  uint8_t *a_st = base;                              // kStages * kABytes
+  uint8_t *b_st = a_st + kStages * kABytes;          // kStages * bBytes
+  uint64_t *bars = reinterpret_cast<uint64_t *>(b_st + kStages * bBytes);
+  uint64_t *full = bars, *empty = bars + kStages, *done = bars + 2 * kStages;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // tile -> matrix m, first row
+  const int tile = blockIdx.x;
+  int m = 0;
+#pragma unroll
+  for (int t = 0; t < QZ_MAX_GROUP - 1; ++t) m += (t < p.n_mats - 1 && tile >= tp.tile_end[t]) ? 1 : 0;
+  const int64_t row0 = (int64_t)(tile - (m ? tp.tile_end[m - 1] : 0)) * kM;
+  const int64_t nrows = tp.mat_rows[m];
+  const int ktiles = tp.ko + tp.kbt;
+  const uint32_t ncols = tp.Np <= 16 ? 32 : (tp.Np <= 32 ? 64 : 128);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), kProducers);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t d_out = tmem, d_bg = tmem + (uint32_t)tp.Np;
+
+  // inputs may come from the previous kernel on the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp < 4) {
+    // ------------------------------------------------------ producers ----
+    const int r = tid;  // weight row of this thread inside the tile
+    const int64_t grow = row0 + r;
+    const bool live = grow < nrows;
+    for (int kt = 0; kt < ktiles; ++kt) {
+      const int s = kt % kStages;
+      if (kt >= kStages && !mbar_wait(smem_u32(&empty[s]), ((kt / kStages) - 1) & 1, abort_flag))
+        break;
+      uint8_t *A = a_st + s * kABytes;
+      uint8_t *Bt = b_st + s * bBytes;
+      const bool outl = kt < tp.ko;
+      // --- A: one row of 64 k slots = 8 core-matrix rows of 16 bytes
+      if (INT4 && outl) {
+        const int t0 = kt * kKT;
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.w_out[m] + grow * p.ld_out[m]);
+#pragma unroll
+        for (int kg = 0; kg < 8; ++kg) {
+          const int t = t0 + kg * 8;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (live && t < p.n_out) {
+            v = __ldg(src + t / 8);
+            // zero the slots past n_out inside the last group
+            const int valid = p.n_out - t;
+            if (valid < 8) {
+              uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int h = 0; h < 8; ++h)
+                if (h >= valid) w[h >> 1] &= (h & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+              v = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          *reinterpret_cast<uint4 *>(A + core_off(r, kg * 8)) = v;
+        }
+      } else if (INT4) {
+        const int e0 = (kt - tp.ko) * kKT;  // first background element of the tile
+        const uint8_t *src = p.codes[m] + grow * p.ld_codes[m] + e0 / 2;
+        uint4 q[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          q[h] = make_uint4(0, 0, 0, 0);
+          if (live && e0 / 2 + 16 * h < p.ld_codes[m]) q[h] = __ldg(reinterpret_cast<const uint4 *>(src) + h);
+        }
+        const uint32_t words[8] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w};
+        const uint32_t bias = 0x64086408u;   // 1032 in both halves after the XOR
+        const uint32_t k1032 = 0x64086408u;
+#pragma unroll
+        for (int kg = 0; kg < 8; ++kg) {
+          const uint32_t w = words[kg];
+          uint32_t h0 = ((w >> 0) & 0x000F000Fu) ^ bias;   // elements 0 and 4
+          uint32_t h1 = ((w >> 4) & 0x000F000Fu) ^ bias;   // 1 and 5
+          uint32_t h2 = ((w >> 8) & 0x000F000Fu) ^ bias;   // 2 and 6
+          uint32_t h3 = ((w >> 12) & 0x000F000Fu) ^ bias;  // 3 and 7
+          // 1024 + (q+8) - 1032 = q, exact in fp16; elements past kb hold
+          // zero nibbles (q = 0) from the row padding, and zero rows past N
+          h0 = hsub2_u32(h0, k1032);
+          h1 = hsub2_u32(h1, k1032);
+          h2 = hsub2_u32(h2, k1032);
+          h3 = hsub2_u32(h3, k1032);
+          if (!live) h0 = h1 = h2 = h3 = 0;
+          // slot order 0,4,1,5,2,6,3,7
+          *reinterpret_cast<uint4 *>(A + core_off(r, kg * 8)) = make_uint4(h0, h1, h2, h3);
+        }
+      } else {
+        const int e0 = kt * kKT;
+        const uint8_t *src = p.codes[m] + grow * p.ld_codes[m] + e0;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (live && e0 + 16 * h < p.ld_codes[m]) v = __ldg(reinterpret_cast<const uint4 *>(src) + h);
+          const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                                 v.w ^ 0x80808080u};
+          uint32_t o[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            // 0x64 above each offset-binary byte: 1024 + (q + 128); minus 1152
+            o[2 * k] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4140), 0x64806480u);
+            o[2 * k + 1] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4342), 0x64806480u);
+          }
+          if (!live) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = 0;
+          }
+          *reinterpret_cast<uint4 *>(A + core_off(r, 16 * h)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4 *>(A + core_off(r, 16 * h + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+      }
+      // --- B: Np x 64 activations, gathered through perm
+      for (int idx = tid; idx < tp.Np * kKT; idx += kProducers) {
+        const int c = idx % kKT, n = idx / kKT;
+        __half v = __float2half_rn(0.0f);
+        if (n < tp.B) {
+          const __half *xb = p.x + (int64_t)n * p.ldx;
+          if (INT4 && outl) {
+            const int t = kt * kKT + c;
+            if (t < p.n_out) v = xb[__ldg(p.perm + t)];
+          } else if (INT4) {
+            const int e = (kt - tp.ko) * kKT + slot_elem(c);
+            if (e < p.kb) v = xb[__ldg(p.perm + p.n_out + e)];
+          } else {
+            const int e = kt * kKT + c;
+            if (e < p.K) v = xb[e];
+          }
+        }
+        *reinterpret_cast<__half *>(Bt + core_off(n, c)) = v;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(smem_u32(&full[s]));
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------ MMA issuer ---
+    const uint32_t idesc = idesc_f16(kM, tp.Np);
+    for (int kt = 0; kt < ktiles; ++kt) {
+      const int s = kt % kStages;
+      if (!mbar_wait(smem_u32(&full[s]), (kt / kStages) & 1, abort_flag)) break;
+      fence_after();
+      const bool outl = kt < tp.ko;
+      const uint32_t d = outl ? d_out : d_bg;
+      const bool first = outl ? kt == 0 : kt == tp.ko;
+      const uint32_t a0 = smem_u32(a_st + s * kABytes), b0 = smem_u32(b_st + s * bBytes);
+#pragma unroll
+      for (int k16 = 0; k16 < kKT / 16; ++k16)
+        mma_f16(d, sdesc(a0 + k16 * 2 * kLBO), sdesc(b0 + k16 * 2 * kLBO), idesc,
+                (first && k16 == 0) ? 0u : 1u);
+      mma_commit(smem_u32(&empty[s]));
+    }
+    mma_commit(smem_u32(done));  // arrives once every issued MMA has completed
+  }
+
+  // ---------------------------------------------------------- epilogue ----
+  if (warp < 4) {
+    const bool ok = mbar_wait(smem_u32(done), 0, abort_flag);
+    fence_after();
+    const int r = tid;
+    const int64_t grow = row0 + r;
+    float s_i = 1.0f;
+    if (grow < nrows) s_i = INT4 ? __ldg(p.scale[m] + grow) : __ldg(p.scale[m]);
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    for (int c0 = 0; c0 < tp.Np; c0 += 16) {
+      float vb[16], vo[16];
+      tmem_ld16(d_bg + lane_base + c0, vb);
+      if (INT4 && tp.ko > 0) tmem_ld16(d_out + lane_base + c0, vo);
+      if (ok && grow < nrows) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int n = c0 + j;
+          if (n < tp.B) {
+            const float bg = tp.kbt > 0 ? vb[j] : 0.0f;
+            const float o = (INT4 && tp.ko > 0) ? vo[j] : 0.0f;
+            p.y[m][(int64_t)n * p.ldy + grow] = __float2half_rn(fmaf(s_i, bg, o));
+          }
+        }
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols)
+                 : "memory");
+}
+
+}  // namespace
+
+size_t tc_smem_bytes(int Np) {
+  return 1024 + (size_t)kStages * (kABytes + Np * kKT * 2) + (2 * kStages + 1) * 8 + 16;
+}
+
+qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_rows,
+                    cudaStream_t s) {
+  DeviceInfo di;
+  qz_status st = device_info(&di);
+  if (st != QZ_OK) return st;
+  TcParams tp;
+  tp.g = g;
+  tp.B = B;
+  tp.Np = (B + 15) / 16 * 16;
+  tp.ko = int4 ? (g.n_out + kKT - 1) / kKT : 0;
+  tp.kbt = int4 ? (g.kb + kKT - 1) / kKT : (g.K + kKT - 1) / kKT;
+  int tiles = 0;
+  for (int m = 0; m < QZ_MAX_GROUP; ++m) {
+    tp.mat_rows[m] = m < g.n_mats ? mat_rows[m] : 0;
+    tp.n_tiles[m] = m < g.n_mats ? (int)((mat_rows[m] + kM - 1) / kM) : 0;
+    tiles += tp.n_tiles[m];
+    tp.tile_end[m] = tiles;
+  }
+  const size_t smem = tc_smem_bytes(tp.Np);
+  if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
+  auto kern = int4 ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3(kThreadsTc);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = g.overlap ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, tp);
+  if (e != cudaSuccess) return cuda_status(e);
+  return launch_status();
+}
+
+qz_status read_device_error(int *code, int clear) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int));
+  if (e != cudaSuccess) return cuda_status(e);
+  if (clear && v) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  *code = v;
+  return QZ_OK;
+}
+
+}  // namespace qz

@@ -7,6 +7,9 @@
 namespace qz {
 
 static thread_local int g_last_cuda_error = 0;
+static thread_local int g_overlap = 0;
+
+int overlap_enabled() { return g_overlap; }
 
 qz_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return QZ_OK;
@@ -151,16 +154,22 @@ void fill_int4o(GemvParams &p, const qz_int4o_weight *ws, int n) {
 qz_status gemm_common(bool int4, GemvParams &p, int64_t B, const qz_half *X, int64_t ldx,
                       qz_half *const *Ys, int64_t ldy, int n, cudaStream_t s) {
   p.x = reinterpret_cast<const __half *>(X);
+  p.overlap = overlap_enabled();
   p.ldx = B > 1 ? ldx : 0;
   p.ldy = B > 1 ? ldy : 0;
   for (int m = 0; m < n; ++m) p.y[m] = reinterpret_cast<__half *>(Ys[m]);
-  if (B <= 4) {
-    DeviceInfo di;
-    QZ_TRY(device_info(&di));
-    if (gemv_smem_bytes(int4, (int)B, p) > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
+  DeviceInfo di;
+  QZ_TRY(device_info(&di));
+  // Batches of 1..4 run on CUDA cores when their staged inputs fit in shared
+  // memory; larger batches (and B = 2..4 at very large K) are dense enough
+  // for the tensor cores.
+  if (B <= 4 && gemv_smem_bytes(int4, (int)B, p) <= (size_t)di.max_smem_optin)
     return launch_gemv(int4, (int)B, p, s);
-  }
-  return QZ_ERR_UNSUPPORTED;  // batches above 4 run on the tensor-core path
+  if (B == 1) return QZ_ERR_UNSUPPORTED;
+  int64_t rows[QZ_MAX_GROUP];
+  for (int m = 0; m < QZ_MAX_GROUP; ++m)
+    rows[m] = m < n ? p.row_end[m] - (m ? p.row_end[m - 1] : 0) : 0;
+  return launch_tc(int4, (int)B, p, rows, s);
 }
 
 }  // namespace
@@ -186,6 +195,19 @@ const char *qz_status_string(qz_status st) {
 int qz_version(void) { return 1 * 10000 + 0 * 100 + 0; }
 
 int qz_last_cuda_error(void) { return g_last_cuda_error; }
+
+qz_status qz_set_overlap(int enable) {
+  if (enable != 0 && enable != 1) return QZ_ERR_INVALID_ARG;
+  g_overlap = enable;
+  return QZ_OK;
+}
+
+int qz_get_overlap(void) { return g_overlap; }
+
+qz_status qz_device_error(int *code, int clear) {
+  if (!code || (clear != 0 && clear != 1)) return QZ_ERR_INVALID_ARG;
+  return read_device_error(code, clear);
+}
 
 // ------------------------------------------------------------------ INT8 --
 qz_status qz_quantize_int8(const qz_half *W, int64_t N, int64_t K, int64_t ldw, int8_t *q,

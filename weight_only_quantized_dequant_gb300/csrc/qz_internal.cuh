@@ -43,12 +43,23 @@ struct GemvParams {
   const float *scale[QZ_MAX_GROUP];    // INT8: [1]; INT4: [N]
   __half *y[QZ_MAX_GROUP];             // [B][ldy]
   int64_t ldy;
+  int overlap;  // programmatic dependent launch + weight prefetch before the wait
 };
+
+// Per-host-thread launch option set by qz_set_overlap().
+int overlap_enabled();
 
 // Shared-memory bytes the CUDA-core kernel needs for batch B.
 size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p);
 // Enqueue the CUDA-core GEMV for batch 1 <= B <= 4.
 qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s);
+
+// Tensor-core (tcgen05) GEMM for any batch 1..64; rows of each matrix are
+// p.row_end differences.
+size_t tc_smem_bytes(int Np);
+qz_status launch_tc(bool int4, int B, const GemvParams &p, const int64_t *mat_rows,
+                    cudaStream_t s);
+qz_status read_device_error(int *code, int clear);
 
 // ------------------------------------------------------------ quantizers ---
 qz_status launch_quantize_int8(const __half *W, int64_t N, int64_t K,

@@ -111,8 +111,18 @@ class LayerStack:
             for g in range(len(S.GROUPS)):
                 self.run_group(l, g, stream)
 
-    def capture(self) -> torch.cuda.CUDAGraph:
-        """CUDA graph of one decode step (all layers)."""
+    def capture(self, overlap: bool = True) -> torch.cuda.CUDAGraph:
+        """CUDA graph of one decode step (all layers).  With overlap, each
+        launch may start while the previous one drains (weights are static
+        during decode)."""
+        prev = api.get_overlap()
+        api.set_overlap(overlap)
+        try:
+            return self._capture()
+        finally:
+            api.set_overlap(prev)
+
+    def _capture(self) -> torch.cuda.CUDAGraph:
         s = torch.cuda.Stream(device=self.device)
         s.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(s):
@@ -148,3 +158,113 @@ class LayerStack:
 
     def d2h_bytes_per_step(self) -> int:
         return sum(y.numel() * 2 for ys in self.y for yy in ys for y in yy)
+
+
+# ---------------------------------------------------------------- paging ---
+def _align16(n: int) -> int:
+    return (n + 15) // 16 * 16
+
+
+class PagedStack:
+    """A stack whose packed layers live in pinned host memory and stream
+    through the pager into two device slots ("Open Origin - ELG Stream
+    Layer", Key Features 2-3; "NTransformer", Tier B).
+
+    distinct: number of distinct host layers actually built; layer l of the
+    n_layers-deep stack reuses host blob l % distinct (bounds pinned memory).
+    """
+
+    def __init__(self, wl: S.Workload, n_layers: int | None = None, distinct: int = 4,
+                 device="cuda"):
+        self.wl = wl
+        self.n_layers = wl.layers if n_layers is None else n_layers
+        self.distinct = min(distinct, self.n_layers)
+        self.device = torch.device(device)
+        src = LayerStack(wl, layers=self.distinct, device=device)
+        self.x, self.y = src.x, src.y
+        # one blob layout shared by every layer (same shapes)
+        self.layout = []  # (kind, name, offset, nbytes, dtype, shape)
+        off = 0
+        lay0 = src.layers[0]
+        if wl.fmt == "int8":
+            for m in S.MATS:
+                w = lay0.mats[m]
+                for part, t in (("q", w.q), ("scale", w.scale)):
+                    self.layout.append((m, part, off, t.numel() * t.element_size(), t.dtype,
+                                        tuple(t.shape)))
+                    off = _align16(off + t.numel() * t.element_size())
+        else:
+            for table in S.PERM_TABLES:
+                t = lay0.perms[table]
+                self.layout.append((table, "perm", off, t.numel() * 4, t.dtype, tuple(t.shape)))
+                off = _align16(off + t.numel() * 4)
+            for m in S.MATS:
+                w = lay0.mats[m]
+                for part, t in (("w_out", w.w_out), ("q4", w.q4), ("scale", w.scale)):
+                    nb = t.numel() * t.element_size()
+                    self.layout.append((m, part, off, nb, t.dtype, tuple(t.shape)))
+                    off = _align16(off + nb)
+        self.blob_bytes = _align16(off)
+        self.blobs = []
+        for l in range(self.distinct):
+            blob = torch.zeros((self.blob_bytes,), dtype=torch.uint8).pin_memory()
+            lay = src.layers[l]
+            for key, part, o, nb, dt, shape in self.layout:
+                if part == "perm":
+                    t = lay.perms[key]
+                else:
+                    t = getattr(lay.mats[key], part)
+                blob[o:o + nb] = t.reshape(-1).view(torch.uint8).cpu()
+            self.blobs.append(blob)
+        self.weight_bytes_per_layer = src.weight_bytes_per_layer()
+        self.io_bytes_per_layer = src.io_bytes_per_layer()
+        del src
+        self.slots = [torch.empty((self.blob_bytes,), dtype=torch.uint8, device=self.device)
+                      for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(device=self.device)
+        self.compute_stream = torch.cuda.Stream(device=self.device)
+        hosts = [self.blobs[l % self.distinct] for l in range(self.n_layers)]
+        self.pager = api.Pager(hosts, self.slots, self.copy_stream, self.compute_stream)
+        self._views = [self._mats_in(slot) for slot in self.slots]
+
+    def _mats_in(self, slot: torch.Tensor) -> dict:
+        """The layer's matrices as views into a device slot."""
+        parts, perms = {}, {}
+        for key, part, o, nb, dt, shape in self.layout:
+            t = slot[o:o + nb].view(dt).view(shape)
+            if part == "perm":
+                perms[key] = t
+            else:
+                parts.setdefault(key, {})[part] = t
+        mats = {}
+        for m in S.MATS:
+            N, K = self.wl.shape(m)
+            if self.wl.fmt == "int8":
+                mats[m] = api.Int8Matrix(parts[m]["q"], parts[m]["scale"], N, K)
+            else:
+                table = next(t for t, mem in S.PERM_TABLES.items() if m in mem)
+                mats[m] = api.Int4oMatrix(perms[table], parts[m]["w_out"], parts[m]["q4"],
+                                          parts[m]["scale"], N, K, api.default_n_out(K))
+        return mats
+
+    def run_step(self):
+        """All n_layers layers once, each acquired from the pager."""
+        cs = self.compute_stream
+        int8 = self.wl.fmt == "int8"
+        for l in range(self.n_layers):
+            ptr = self.pager.acquire(l)
+            mats = self._views[0 if ptr == self.slots[0].data_ptr() else 1]
+            xs, ys = self.x[l % self.distinct], self.y[l % self.distinct]
+            for g, names in enumerate(S.GROUPS):
+                ws = [mats[m] for m in names]
+                outs = [y[0] for y in ys[g]]
+                if len(ws) == 1:
+                    (api.gemv_int8 if int8 else api.gemv_int4_outlier)(ws[0], xs[g][0], outs[0],
+                                                                       stream=cs)
+                else:
+                    (api.gemv_int8_grouped if int8 else api.gemv_int4_outlier_grouped)(
+                        ws, xs[g][0], outs, stream=cs)
+            self.pager.release(l)
+
+    def close(self):
+        self.pager.close()
