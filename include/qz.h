@@ -112,7 +112,9 @@ typedef struct {
 
 /* y[i] = fp16( scale * sum_j q[i][j] * x[j] ), fp32 accumulation, products of
  * the exact integer code with the fp16 input; no fp16 weight is formed.
- * x [K], y [N].  K <= 57344 (the permuted input is staged in shared memory). */
+ * x [K], y [N].  K <= 57344.  The CUDA-core kernel stages the input in
+ * shared memory; at the largest K, where it does not fit, the call runs on the
+ * tensor-core kernel instead (same result bound). */
 qz_status qz_gemv_int8(const qz_int8_weight *w, const qz_half *x, qz_half *y,
                        qz_stream s);
 

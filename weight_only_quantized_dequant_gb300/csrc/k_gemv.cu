@@ -11,14 +11,19 @@
 // Every product is exact in fp32 (an integer code of at most 8 bits times an
 // fp16 input) and products are summed in fp32; no fp16 weight is formed.
 //
-// Design (HBM-bound stream):
+// Design (HBM-bound stream; on GB300 the ALU and FMA pipes and the shared
+// memory pipe are close behind, so every instruction per weight counts):
 //  * x is gathered through the permutation into shared memory once per CTA,
-//    converted to fp32 and, for INT4, pre-scaled by 16^-(t' mod 4) so that a
-//    nibble can be turned into an exact fp32 multiple of 16^p with one LOP3
-//    (OR-ing it into the mantissa of 2^23) and one packed subtract.
-//  * Each warp streams whole rows with 16-byte non-allocating loads, four
-//    chunks per lane in flight; shared-memory reads of x are swizzled so the
-//    eight lanes of each 128-bit phase hit distinct banks.
+//    as fp32 and, for INT4, pre-scaled by 16^-(t' mod 4) so that one LOP3
+//    turns a nibble into the fp32 number 2^23 + (q+8)*16^p and one packed
+//    subtract leaves q*16^p exactly.  Staged chunks are padded by 16 bytes
+//    (conflict-free for the 8 lanes of a 128-bit phase), so every shared read
+//    is a per-lane base plus an immediate offset.
+//  * A warp computes R rows at once: each staged granule is read once for
+//    all R rows, halving the shared-memory traffic per weight.
+//  * Loads are software-pipelined in registers: the next group of chunks
+//    (possibly of the next rows) is issued before the current one is
+//    consumed, and each warp bulk-prefetches its following rows into L2.
 //  * Products use the sm_100+ packed fp32x2 add/FMA (two weights per issue).
 //  * CTAs own contiguous, equal row ranges; the grid is the SM count times
 //    the resident CTAs per SM.
@@ -29,7 +34,6 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 6;  // 16-byte chunks per lane in flight
 constexpr int64_t kPrefetchBytes = 64 * 1024;  // per CTA, issued before the wait
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
@@ -40,16 +44,8 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   return r;
 }
 
-// Index of 16-byte granule g of code chunk c in the staged input.  GPC is the
-// number of granules per chunk (8 for INT4: 32 nibbles -> 32 floats; 4 for
-// INT8: 16 bytes -> 16 floats; 2 for the fp16 outliers: 8 halves -> 8 floats).
-// Lane L reads chunk c = L + 32u, so the XOR keeps the 8 lanes of one LDS.128
-// phase on distinct bank groups.
-template <int GPC>
-__device__ __forceinline__ int gidx(int c, int g) {
-  if constexpr (GPC == 8) return c * 8 + (g ^ (c & 7));
-  else if constexpr (GPC == 4) return c * 4 + (g ^ ((c >> 1) & 3));
-  else return c * 2 + (g ^ ((c >> 2) & 1));
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // (a & b) ^ c in one LOP3 (truth table 0x6A).
@@ -59,72 +55,77 @@ __device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) 
   return d;
 }
 
-// Shared-memory read of one staged granule (4 fp32 inputs) at a byte offset.
 __device__ __forceinline__ float4 lds(const float4 *base, uint32_t byte_off) {
   return *reinterpret_cast<const float4 *>(reinterpret_cast<const char *>(base) + byte_off);
 }
 
-// 32 nibbles of one chunk against the staged (pre-scaled) input.
-// For nibble p (0..3) of a half-word, (w & 0xF<<4p) ^ (0x4B000000 | 8<<4p) is
-// the fp32 number 2^23 + (q+8)*16^p; subtracting 2^23 + 8*16^p leaves q*16^p
-// exactly, and the input was staged as x*16^-p, so each FMA adds q*x exactly.
-// goff[g] is the lane's byte offset of granule g inside its chunk (the swizzle
-// only depends on the lane), cbase the byte offset of the chunk, bstride the
-// bytes between batch rows of the staged input.
-template <int B>
-__device__ __forceinline__ void int4_chunk(const uint4 v, const float4 *xs,
-                                           const uint32_t (&goff)[8], uint32_t cbase,
-                                           uint32_t bstride, float2 (&acc)[B][2]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// Outlier inputs: granule g (0/1) of outlier chunk c, XOR-swizzled.
+__device__ __forceinline__ int ogidx(int c, int g) { return c * 2 + (g ^ ((c >> 2) & 1)); }
+
+// 32 nibbles of one chunk of each of R rows against the staged input at byte
+// offset `o` (granule g at o + 16 g).  For nibble p (0..3) of a half-word,
+// (w & 0xF<<4p) ^ (0x4B000000 | 8<<4p) is 2^23 + (q+8)*16^p; subtracting
+// 2^23 + 8*16^p leaves q*16^p, and the staged input is x*16^-p.
+template <int B, int R>
+__device__ __forceinline__ void int4_chunk(const uint4 (&v)[R], const float4 *xs, uint32_t o,
+                                           uint32_t bstride, float2 (&acc)[R][B][2]) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint32_t ww = h ? (w[k] >> 16) : w[k];
-      const float f0 = __uint_as_float(and_xor(ww, 0x000Fu, 0x4B000008u));
-      const float f1 = __uint_as_float(and_xor(ww, 0x00F0u, 0x4B000080u));
-      const float f2 = __uint_as_float(and_xor(ww, 0x0F00u, 0x4B000800u));
-      const float f3 = __uint_as_float(and_xor(ww, 0xF000u, 0x4B008000u));
-      const float2 qa = __fadd2_rn(make_float2(f0, f1),
-                                   make_float2(-8388616.0f, -8388736.0f));
-      const float2 qb = __fadd2_rn(make_float2(f2, f3),
-                                   make_float2(-8390656.0f, -8421376.0f));
-      const uint32_t o = cbase + goff[2 * k + h];
+      float4 xv[B];
 #pragma unroll
-      for (int b = 0; b < B; ++b) {
-        const float4 xv = lds(xs, o + b * bstride);
-        acc[b][0] = __ffma2_rn(qa, make_float2(xv.x, xv.y), acc[b][0]);
-        acc[b][1] = __ffma2_rn(qb, make_float2(xv.z, xv.w), acc[b][1]);
+      for (int b = 0; b < B; ++b) xv[b] = lds(xs, o + (2 * k + h) * 16 + b * bstride);
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) {
+        const uint32_t w = k == 0 ? v[rr].x : k == 1 ? v[rr].y : k == 2 ? v[rr].z : v[rr].w;
+        const uint32_t ww = h ? (w >> 16) : w;
+        const float f0 = __uint_as_float(and_xor(ww, 0x000Fu, 0x4B000008u));
+        const float f1 = __uint_as_float(and_xor(ww, 0x00F0u, 0x4B000080u));
+        const float f2 = __uint_as_float(and_xor(ww, 0x0F00u, 0x4B000800u));
+        const float f3 = __uint_as_float(and_xor(ww, 0xF000u, 0x4B008000u));
+        const float2 qa = __fadd2_rn(make_float2(f0, f1),
+                                     make_float2(-8388616.0f, -8388736.0f));
+        const float2 qb = __fadd2_rn(make_float2(f2, f3),
+                                     make_float2(-8390656.0f, -8421376.0f));
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          acc[rr][b][0] = __ffma2_rn(qa, make_float2(xv[b].x, xv[b].y), acc[rr][b][0]);
+          acc[rr][b][1] = __ffma2_rn(qb, make_float2(xv[b].z, xv[b].w), acc[rr][b][1]);
+        }
       }
     }
   }
 }
 
-// 16 int8 codes of one chunk.  XOR 0x80 makes each byte the offset-binary
-// u = q + 128; PRMT drops it into the low byte of 2^23's bit pattern, and
-// subtracting 2^23 + 128 leaves q exactly.
-template <int B>
-__device__ __forceinline__ void int8_chunk(const uint4 v, const float4 *xs,
-                                           const uint32_t (&goff)[8], uint32_t cbase,
-                                           uint32_t bstride, float2 (&acc)[B][2]) {
-  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u,
-                         v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+// 16 int8 codes of one chunk of each of R rows.  XOR 0x80 makes each byte the
+// offset-binary u = q + 128; PRMT drops it into the low byte of 2^23's bit
+// pattern, and subtracting 2^23 + 128 leaves q exactly.
+template <int B, int R>
+__device__ __forceinline__ void int8_chunk(const uint4 (&v)[R], const float4 *xs, uint32_t o,
+                                           uint32_t bstride, float2 (&acc)[R][B][2]) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float f0 = __uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7440));
-    const float f1 = __uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7441));
-    const float f2 = __uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7442));
-    const float f3 = __uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7443));
-    const float2 qa = __fadd2_rn(make_float2(f0, f1),
-                                 make_float2(-8388736.0f, -8388736.0f));
-    const float2 qb = __fadd2_rn(make_float2(f2, f3),
-                                 make_float2(-8388736.0f, -8388736.0f));
-    const uint32_t o = cbase + goff[k];
+    float4 xv[B];
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      const float4 xv = lds(xs, o + b * bstride);
-      acc[b][0] = __ffma2_rn(qa, make_float2(xv.x, xv.y), acc[b][0]);
-      acc[b][1] = __ffma2_rn(qb, make_float2(xv.z, xv.w), acc[b][1]);
+    for (int b = 0; b < B; ++b) xv[b] = lds(xs, o + k * 16 + b * bstride);
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+      const uint32_t w =
+          (k == 0 ? v[rr].x : k == 1 ? v[rr].y : k == 2 ? v[rr].z : v[rr].w) ^ 0x80808080u;
+      const float f0 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440));
+      const float f1 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7441));
+      const float f2 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7442));
+      const float f3 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7443));
+      const float2 qa = __fadd2_rn(make_float2(f0, f1),
+                                   make_float2(-8388736.0f, -8388736.0f));
+      const float2 qb = __fadd2_rn(make_float2(f2, f3),
+                                   make_float2(-8388736.0f, -8388736.0f));
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        acc[rr][b][0] = __ffma2_rn(qa, make_float2(xv[b].x, xv[b].y), acc[rr][b][0]);
+        acc[rr][b][1] = __ffma2_rn(qb, make_float2(xv[b].z, xv[b].w), acc[rr][b][1]);
+      }
     }
   }
 }
@@ -135,20 +136,91 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-copy ring.  Each warp streams its rows' codes through kNS stages of
+// shared memory: lane 0 issues cp.async.bulk copies (global -> shared, with
+// an mbarrier transaction count) kNS-1 stages ahead of the stage the lanes
+// are computing, so a warp keeps its next rows in flight without holding
+// them in registers.  A stage is kRPS rounds (32 chunks of 16 bytes) of each
+// of the warp's R rows.  Every wait is bounded in time.
+// ---------------------------------------------------------------------------
+__device__ int g_gemv_error = 0;  // 1 if a bounded wait gave up (read by qz_device_error)
+
+constexpr int kRPS = 2;                        // rounds per stage
+constexpr uint32_t kRoundBytes = 512;          // 32 chunks x 16 bytes
+constexpr uint32_t kStageRow = kRPS * kRoundBytes;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+template <int B>
+struct Ring {
+  static constexpr int NS = B == 1 ? 3 : 2;    // stages per warp
+  static constexpr int R = B == 1 ? 2 : 1;     // rows per warp
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
+  return (uint32_t)__cvta_generic_to_shared(ptr);
+}
+
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; on timeout the error word is set and false returned.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = gtimer();
+  for (;;) {
+    if (mbar_try(bar, parity)) return true;
+    if (gtimer() - t0 > kWaitNs) {
+      atomicExch(&g_gemv_error, 1);
+      return false;
+    }
+  }
+}
+
+// Row r of the launch -> (matrix, row inside it).
+__device__ __forceinline__ void locate(const GemvParams &p, int64_t r, int &m, int64_t &i) {
+  m = 0;
+#pragma unroll
+  for (int t = 0; t < QZ_MAX_GROUP - 1; ++t) m += (t < p.n_mats - 1 && r >= p.row_end[t]) ? 1 : 0;
+  i = r - (m ? p.row_end[m - 1] : 0);
+}
+
 template <bool INT4, int B>
-__global__ void __launch_bounds__(kThreads, (B == 1 ? 2 : 1))
+__global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvParams p) {
-  extern __shared__ float4 smem[];
-  constexpr int GPC = INT4 ? 8 : 4;       // granules per code chunk
-  constexpr int EPC = GPC * 4;            // elements per code chunk
-  const int cps = p.cpr > 32 ? p.cpr : 32;  // staged chunks (>= 32: one per lane)
-  const int gstride = cps * GPC;          // background granules per batch row
-  const int ostride = p.ocpr * 2;         // outlier granules per batch row
-  float4 *xs = smem;
-  float4 *xo = smem + B * gstride;
+  constexpr int R = Ring<B>::R, NS = Ring<B>::NS;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  constexpr int GPC = INT4 ? 8 : 4;        // 16-byte granules per code chunk
+  constexpr int EPC = GPC * 4;             // inputs per code chunk
+  constexpr uint32_t CS = (GPC + 1) * 16;  // staged bytes per chunk (padded)
+  const int cpr = p.cpr;
+  const int Jw = (cpr + 31) >> 5;          // rounds of 32 chunks per row
+  const int staged = (Jw > 0 ? Jw : 1) * 32;
+  const uint32_t bstride = (uint32_t)staged * CS;  // bytes per batch row
+  const int ostride = p.ocpr * 2;          // outlier granules per batch row
+  float4 *xs = reinterpret_cast<float4 *>(smem_raw);
+  float4 *xo = reinterpret_cast<float4 *>(smem_raw + B * bstride);
+  uint8_t *ring = smem_raw + (((size_t)B * bstride + (size_t)B * ostride * 16 + 127) & ~(size_t)127);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)kWarps * NS * R * kStageRow);
 
   const int64_t r0 = p.total_rows * blockIdx.x / gridDim.x;
   const int64_t r1 = p.total_rows * (blockIdx.x + 1) / gridDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // The first rows of this CTA are pulled into L2 right away.  With
   // programmatic overlap this CTA may start while the previous kernel on the
@@ -164,14 +236,16 @@ __global__ void __launch_bounds__(kThreads, (B == 1 ? 2 : 1))
       int64_t bytes = (e - r) * p.ld_codes[m];
       if (bytes > budget) bytes = budget;
       bytes &= ~(int64_t)15;
-      if (bytes > 0) {
-        const uint8_t *src = p.codes[m] + (r - m_lo) * p.ld_codes[m];
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)bytes)
-                     : "memory");
-      }
+      if (bytes > 0) prefetch_l2(p.codes[m] + (r - m_lo) * p.ld_codes[m], (uint32_t)bytes);
       budget -= bytes;
       r = e;
     }
+  }
+  if (lane == 0) {
+    for (int st = 0; st < NS; ++st)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[warp * NS + st]))
+                   : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // let the next kernel on the stream get scheduled as SMs free up
@@ -179,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, (B == 1 ? 2 : 1))
 
   // ---- stage x (gathered through perm for INT4) in shared memory ---------
   float *xsf = reinterpret_cast<float *>(xs);
-  const int elems = cps * EPC;
+  const int elems = staged * EPC;
 #pragma unroll 1
   for (int b = 0; b < B; ++b) {
     const __half *xb = p.x + b * p.ldx;
@@ -199,138 +273,186 @@ __global__ void __launch_bounds__(kThreads, (B == 1 ? 2 : 1))
         }
       }
       const int c = e / EPC, u = e % EPC;
-      xsf[(b * gstride + gidx<GPC>(c, u >> 2)) * 4 + (u & 3)] = val;
+      xsf[(b * bstride + c * CS + (u >> 2) * 16) / 4 + (u & 3)] = val;
     }
     if constexpr (INT4) {
       float *xof = reinterpret_cast<float *>(xo);
 #pragma unroll 1
       for (int e = threadIdx.x; e < ostride * 4; e += kThreads) {
         const float val = e < p.n_out ? __half2float(xb[__ldg(p.perm + e)]) : 0.0f;
-        xof[(b * ostride + gidx<2>(e >> 3, (e & 7) >> 2)) * 4 + (e & 3)] = val;
+        xof[(b * ostride + ogidx(e >> 3, (e & 7) >> 2)) * 4 + (e & 3)] = val;
       }
     }
   }
   __syncthreads();
 
-  // ---- one warp per row ----------------------------------------------------
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Lane L reads chunks c = L + 32j.  The staging swizzle of a granule only
-  // depends on c's low bits, i.e. on the lane, so the byte offsets of the
-  // GPC granules inside a chunk are fixed per lane.
-  uint32_t goff[8];
+  // ---- each warp: row groups of R rows, streamed through its ring -----------
+  const int64_t first = r0 + (int64_t)warp * R;
+  const int64_t stride = (int64_t)kWarps * R;
+  if (first >= r1) return;  // no barrier follows
+  const int64_t P = (r1 - first + stride - 1) / stride;  // row groups of this warp
+  const int SPR = (Jw + kRPS - 1) / kRPS;                 // stages per row group
+  const int64_t items = P * SPR;
+  const uint32_t lane_off = (uint32_t)lane * CS;
+  constexpr uint32_t kRound = 32u * CS;  // staged bytes per round of 32 chunks
+  const uint32_t ring_w = smem_u32(ring) + (uint32_t)warp * NS * R * kStageRow;
+  const uint32_t bar_w = smem_u32(&bars[warp * NS]);
+
+  // lane 0: copy stage `it` (row group it / SPR, rounds from (it % SPR) * kRPS)
+  auto issue = [&](int64_t it) {
+    const int64_t k = it / SPR;
+    const int j0 = (int)(it - k * SPR) * kRPS;
+    const int st = (int)(it % NS);
+    const int span = cpr - 32 * j0 < 32 * kRPS ? cpr - 32 * j0 : 32 * kRPS;  // chunks
+    const uint32_t bytes = (uint32_t)span * 16u;
+    const uint32_t bar = bar_w + st * 8;
+    asm volatile(
+        "{\n\t.reg .b64 t;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
+        "r"(bytes * R)
+        : "memory");
+    const int64_t rb = first + k * stride;
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const int sw = GPC == 8 ? (lane & 7) : ((lane >> 1) & 3);
-    goff[g] = (uint32_t)((lane * GPC + ((g % GPC) ^ sw)) * 16);
-  }
-  const uint32_t bstride = (uint32_t)gstride * 16u;
-  constexpr uint32_t kChunkStep = 32u * GPC * 16u;  // bytes between a lane's chunks
-  // Warp-uniform trip counts: rounds where every lane has a chunk run without
-  // predicates; the last partial round (if any) runs predicated, and lanes
-  // past the row's end load zero codes against a valid staged slot (at least
-  // 32 chunks are always staged), so they add exact zeros.  No divergence.
-  const int cpr = p.cpr;
-  const int Jfull = cpr >> 5;             // rounds in which all 32 lanes have a chunk
-  const int Jw = (cpr + 31) >> 5;         // all rounds
-  const int64_t total_rows = p.total_rows;
-  (void)total_rows;
-#pragma unroll 1
-  for (int64_t r = r0 + warp; r < r1; r += kWarps) {
-    int m = 0;
-#pragma unroll
-    for (int t = 0; t < QZ_MAX_GROUP - 1; ++t)
-      m += (t < p.n_mats - 1 && r >= p.row_end[t]) ? 1 : 0;
-    const int64_t i = r - (m ? p.row_end[m - 1] : 0);
-    const float s = INT4 ? __ldg(p.scale[m] + i) : __ldg(p.scale[m]);
-    const int64_t ldc = p.ld_codes[m];
-    const uint4 *row = reinterpret_cast<const uint4 *>(p.codes[m] + i * ldc) + lane;
-    // Bulk-prefetch the warp's next row into L2 while this one is computed:
-    // DRAM keeps streaming independently of this warp's load-use latency.
-    // (Skipped when the next row belongs to the next matrix of a group.)
-    if (lane == 0 && cpr > 0 && r + kWarps < r1 && r + kWarps < p.row_end[m]) {
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                       p.codes[m] + (i + kWarps) * ldc),
-                   "r"((uint32_t)cpr * 16u)
-                   : "memory");
-      if (INT4 && p.ocpr)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                         p.w_out[m] + (i + kWarps) * p.ld_out[m]),
-                     "r"((uint32_t)p.ocpr * 16u)
-                     : "memory");
+    for (int rr = 0; rr < R; ++rr) {
+      const int64_t rc = rb + rr < r1 ? rb + rr : r1 - 1;  // past the end: alias a valid row
+      int m;
+      int64_t i;
+      locate(p, rc, m, i);
+      const uint8_t *src = p.codes[m] + i * p.ld_codes[m] + (size_t)j0 * kRoundBytes;
+      const uint32_t dst = ring_w + (uint32_t)(st * R + rr) * kStageRow;
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+              "r"(dst),
+          "l"(src), "r"(bytes), "r"(bar)
+          : "memory");
     }
+  };
 
-    float2 acc[B][2];
-#pragma unroll
-    for (int b = 0; b < B; ++b) acc[b][0] = acc[b][1] = make_float2(0.f, 0.f);
+  if (lane == 0)
+    for (int64_t it = 0; it < NS - 1 && it < items; ++it) issue(it);
 
-    int j = 0;
-    uint32_t cbase = 0;
-    const uint4 *rp = row;
-#pragma unroll 1
-    for (; j + kUnroll <= Jfull; j += kUnroll, cbase += kUnroll * kChunkStep, rp += 32 * kUnroll) {
-      uint4 v[kUnroll];
+  float2 acc[R][B][2];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream(rp + 32 * u);
+  for (int rr = 0; rr < R; ++rr)
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if constexpr (INT4) int4_chunk<B>(v[u], xs, goff, cbase + u * kChunkStep, bstride, acc);
-        else int8_chunk<B>(v[u], xs, goff, cbase + u * kChunkStep, bstride, acc);
+    for (int b = 0; b < B; ++b) acc[rr][b][0] = acc[rr][b][1] = make_float2(0.f, 0.f);
+
+  bool ok = true;
+  int64_t k = 0;   // row group
+  int sj = 0;      // stage inside the row group
+  const int64_t groups_total = P;
+  for (int64_t g = 0; g < groups_total; ++g) {
+    // rows of this group: scales, matrix, and the outlier rows into L2
+    const int64_t rb = first + g * stride;
+    int mrow[R];
+    int64_t irow[R];
+    float srow[R];
+    bool live[R];
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+      live[rr] = rb + rr < r1;
+      locate(p, live[rr] ? rb + rr : r1 - 1, mrow[rr], irow[rr]);
+      srow[rr] = INT4 ? __ldg(p.scale[mrow[rr]] + irow[rr]) : __ldg(p.scale[mrow[rr]]);
+      if (INT4 && p.ocpr && lane == 8 + rr)
+        prefetch_l2(p.w_out[mrow[rr]] + irow[rr] * p.ld_out[mrow[rr]], (uint32_t)p.ocpr * 16u);
+    }
+    for (sj = 0; sj < SPR; ++sj) {
+      const int64_t it = g * SPR + sj;
+      if (ok && lane == 0 && it + NS - 1 < items) {
+        // the stage being refilled was read by every lane before the last
+        // __syncwarp; order those reads before the async-proxy write
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(it + NS - 1);
       }
-    }
-    if (j < Jw) {  // tail: at most kUnroll rounds, the last one possibly partial
-      uint4 v[kUnroll];
+      const int st = (int)(it % NS);
+      if (ok) ok = mbar_wait(bar_w + st * 8, (uint32_t)((it / NS) & 1));
+      if (ok) {
+        const uint32_t sbase = ring_w + (uint32_t)st * R * kStageRow;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        v[u] = (j + u < Jw && lane + 32 * (j + u) < cpr) ? ld_stream(rp + 32 * u)
-                                                         : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kRPS; ++u) {
+          const int j = sj * kRPS + u;
+          if (j < Jw) {  // warp-uniform
+            const bool in = lane + 32 * j < cpr;
+            uint4 v[R];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (j + u < Jw) {  // warp-uniform
-          const uint32_t cb = lane + 32 * (j + u) < cpr ? cbase + u * kChunkStep : 0u;
-          if constexpr (INT4) int4_chunk<B>(v[u], xs, goff, cb, bstride, acc);
-          else int8_chunk<B>(v[u], xs, goff, cb, bstride, acc);
+            for (int rr = 0; rr < R; ++rr) {
+              v[rr] = make_uint4(0, 0, 0, 0);
+              if (in) {
+                const uint32_t a = sbase + (uint32_t)rr * kStageRow + u * kRoundBytes + lane * 16;
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(v[rr].x), "=r"(v[rr].y), "=r"(v[rr].z), "=r"(v[rr].w)
+                             : "r"(a));
+              }
+            }
+            const uint32_t o = lane_off + (uint32_t)j * kRound;
+            if constexpr (INT4) int4_chunk<B, R>(v, xs, o, bstride, acc);
+            else int8_chunk<B, R>(v, xs, o, bstride, acc);
+          }
         }
       }
+      __syncwarp();
     }
-
-    float outl[B];
+    (void)k;
+    // ---- row epilogue: outliers, scale, reduction, store --------------------
+    float outl[R][B];
 #pragma unroll
-    for (int b = 0; b < B; ++b) outl[b] = 0.0f;
+    for (int rr = 0; rr < R; ++rr)
+#pragma unroll
+      for (int b = 0; b < B; ++b) outl[rr][b] = 0.0f;
     if constexpr (INT4) {
-      const uint4 *orow = reinterpret_cast<const uint4 *>(p.w_out[m] + i * p.ld_out[m]);
-#pragma unroll 1
-      for (int c = lane; c < p.ocpr; c += 32) {
-        const uint4 v = ld_stream(orow + c);
-        const float2 h0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-        const float2 h1 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-        const float2 h2 = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
-        const float2 h3 = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
 #pragma unroll
-        for (int b = 0; b < B; ++b) {
-          const float4 xa = xo[b * ostride + gidx<2>(c, 0)];
-          const float4 xc = xo[b * ostride + gidx<2>(c, 1)];
-          float a = outl[b];
-          a = fmaf(h0.x, xa.x, a); a = fmaf(h0.y, xa.y, a);
-          a = fmaf(h1.x, xa.z, a); a = fmaf(h1.y, xa.w, a);
-          a = fmaf(h2.x, xc.x, a); a = fmaf(h2.y, xc.y, a);
-          a = fmaf(h3.x, xc.z, a); a = fmaf(h3.y, xc.w, a);
-          outl[b] = a;
+      for (int rr = 0; rr < R; ++rr) {
+        const uint4 *orow =
+            reinterpret_cast<const uint4 *>(p.w_out[mrow[rr]] + irow[rr] * p.ld_out[mrow[rr]]);
+#pragma unroll 1
+        for (int c = lane; c < p.ocpr; c += 32) {
+          const uint4 v = ld_stream(orow + c);
+          const float2 h0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+          const float2 h1 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+          const float2 h2 = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
+          const float2 h3 = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+#pragma unroll
+          for (int b = 0; b < B; ++b) {
+            const float4 xa = xo[b * ostride + ogidx(c, 0)];
+            const float4 xc = xo[b * ostride + ogidx(c, 1)];
+            float a = outl[rr][b];
+            a = fmaf(h0.x, xa.x, a); a = fmaf(h0.y, xa.y, a);
+            a = fmaf(h1.x, xa.z, a); a = fmaf(h1.y, xa.w, a);
+            a = fmaf(h2.x, xc.x, a); a = fmaf(h2.y, xc.y, a);
+            a = fmaf(h3.x, xc.z, a); a = fmaf(h3.y, xc.w, a);
+            outl[rr][b] = a;
+          }
         }
       }
     }
-
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      float bgs = (acc[b][0].x + acc[b][0].y) + (acc[b][1].x + acc[b][1].y);
-      bgs = warp_sum(bgs);
-      float os = INT4 ? warp_sum(outl[b]) : 0.0f;
-      if (lane == 0) p.y[m][b * p.ldy + i] = __float2half_rn(fmaf(s, bgs, os));
+    for (int rr = 0; rr < R; ++rr) {
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const float bg =
+            (acc[rr][b][0].x + acc[rr][b][0].y) + (acc[rr][b][1].x + acc[rr][b][1].y);
+        // y = s_i * background + outliers, combined per lane, one reduction
+        const float yl = warp_sum(fmaf(srow[rr], bg, outl[rr][b]));
+        if (lane == 0 && live[rr]) p.y[mrow[rr]][b * p.ldy + irow[rr]] = __float2half_rn(yl);
+        acc[rr][b][0] = acc[rr][b][1] = make_float2(0.f, 0.f);
+      }
+    }
+  }
+  // A warp that gave up a wait still has copies in flight into its ring;
+  // give them a bounded time to land before the CTA's shared memory goes.
+  if (!ok && lane == 0) {
+    for (int st = 0; st < NS; ++st) {
+      const unsigned long long t0 = gtimer();
+      while (!mbar_try(bar_w + st * 8, 0) && !mbar_try(bar_w + st * 8, 1) &&
+             gtimer() - t0 < kWaitNs) {
+      }
     }
   }
 }
 
 template <bool INT4, int B>
 qz_status launch_t(const GemvParams &p, cudaStream_t s) {
+  constexpr int R = Ring<B>::R;
   auto kern = gemv_kernel<INT4, B>;
   DeviceInfo di;
   qz_status st = device_info(&di);
@@ -347,7 +469,7 @@ qz_status launch_t(const GemvParams &p, cudaStream_t s) {
   // Whole waves only: every SM gets the same number of CTAs (and CTAs equal
   // row ranges), so no SM carries a second CTA while another idles.
   int64_t per_sm = occ;
-  while (per_sm > 1 && (int64_t)di.sms * per_sm * kWarps > p.total_rows * 2) --per_sm;
+  while (per_sm > 1 && (int64_t)di.sms * per_sm * kWarps * R > p.total_rows * 2) --per_sm;
   int64_t grid = (int64_t)di.sms * per_sm;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -367,10 +489,25 @@ qz_status launch_t(const GemvParams &p, cudaStream_t s) {
 }  // namespace
 
 size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p) {
-  const size_t gpc = int4 ? 8 : 4;
-  const size_t cps = p.cpr > 32 ? (size_t)p.cpr : 32;
-  const size_t per_b = (cps * gpc + (int4 ? (size_t)p.ocpr * 2 : 0)) * 16;
-  return per_b * (size_t)B;
+  const size_t cs = int4 ? 144 : 80;  // padded staged bytes per chunk
+  const size_t rounds = p.cpr > 0 ? (size_t)(p.cpr + 31) / 32 : 1;
+  const size_t staged = (rounds * 32 * cs + (int4 ? (size_t)p.ocpr * 32 : 0)) * (size_t)B;
+  const size_t R = B == 1 ? 2 : 1, NS = B == 1 ? 3 : 2;
+  const size_t ring = (size_t)kWarps * NS * R * kStageRow;
+  return ((staged + 127) & ~(size_t)127) + ring + (size_t)kWarps * NS * 8;
+}
+
+qz_status read_gemv_error(int *code, int clear) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof(int));
+  if (e != cudaSuccess) return cuda_status(e);
+  if (clear && v) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  *code = v;
+  return QZ_OK;
 }
 
 qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s) {

@@ -161,11 +161,10 @@ qz_status gemm_common(bool int4, GemvParams &p, int64_t B, const qz_half *X, int
   DeviceInfo di;
   QZ_TRY(device_info(&di));
   // Batches of 1..4 run on CUDA cores when their staged inputs fit in shared
-  // memory; larger batches (and B = 2..4 at very large K) are dense enough
-  // for the tensor cores.
+  // memory; larger batches are dense enough for the tensor cores, which also
+  // take B <= 4 at the few K too large to stage (their inputs stream in tiles).
   if (B <= 4 && gemv_smem_bytes(int4, (int)B, p) <= (size_t)di.max_smem_optin)
     return launch_gemv(int4, (int)B, p, s);
-  if (B == 1) return QZ_ERR_UNSUPPORTED;
   int64_t rows[QZ_MAX_GROUP];
   for (int m = 0; m < QZ_MAX_GROUP; ++m)
     rows[m] = m < n ? p.row_end[m] - (m ? p.row_end[m - 1] : 0) : 0;
@@ -206,7 +205,11 @@ int qz_get_overlap(void) { return g_overlap; }
 
 qz_status qz_device_error(int *code, int clear) {
   if (!code || (clear != 0 && clear != 1)) return QZ_ERR_INVALID_ARG;
-  return read_device_error(code, clear);
+  int a = 0, b = 0;
+  QZ_TRY(read_device_error(&a, clear));
+  QZ_TRY(read_gemv_error(&b, clear));
+  *code = a | b;
+  return QZ_OK;
 }
 
 // ------------------------------------------------------------------ INT8 --

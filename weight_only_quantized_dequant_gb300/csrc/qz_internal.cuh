@@ -60,6 +60,7 @@ size_t tc_smem_bytes(int Np);
 qz_status launch_tc(bool int4, int B, const GemvParams &p, const int64_t *mat_rows,
                     cudaStream_t s);
 qz_status read_device_error(int *code, int clear);
+qz_status read_gemv_error(int *code, int clear);
 
 // ------------------------------------------------------------ quantizers ---
 qz_status launch_quantize_int8(const __half *W, int64_t N, int64_t K,
