@@ -43,11 +43,33 @@ def parse():
                     help="also stream the 70B and Gemma stacks through the pager")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch without programmatic dependent launch")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="batch of the measured stack (1 = the decode headline)")
     ap.add_argument("--layers", type=int, default=None,
                     help="first L layers only (small case for profiling; not a bench line)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
+
+
+def profiled_traffic(profile_md: str, kernel_src: str):
+    """DRAM bytes per launch of the dominant kernel, from the committed ncu
+    summary, if it was taken on the kernel source as it is now (else None).
+    The summary carries 'traffic_bytes_per_launch: N' and 'source_sha256: H'."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", profile_md)
+    src = os.path.join(ROOT, kernel_src)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    want = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    got, traffic = None, None
+    for line in open(path):
+        line = line.strip().strip("`- ")
+        if line.startswith("source_sha256:"):
+            got = line.split(":", 1)[1].strip()
+        elif line.startswith("traffic_bytes_per_launch:"):
+            traffic = int(line.split(":", 1)[1].strip().replace(",", ""))
+    return traffic if got == want else None
 
 
 def peaks():
@@ -456,7 +478,7 @@ def main():
     if dist_ctx is not None:
         dist_ctx.barrier()
 
-    r = measure(a.workload, 1, a.steps, a.warmup, dist_ctx, clocks=(rank == 0), device=device,
+    r = measure(a.workload, a.batch, a.steps, a.warmup, dist_ctx, clocks=(rank == 0), device=device,
                 layers=a.layers, overlap=not a.no_overlap)
     ms_all = r["ms_per_step"]
     e2e_all = r["e2e_ms"]
@@ -499,7 +521,7 @@ def main():
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": a.workload,
                    "format": "int8 per-tensor" if "int8" in a.workload else "int4 outlier-aware",
-                   "batch": 1,
+                   "batch": a.batch,
                    "layers": r["layers"], "launches_per_layer": 4, "graph": True,
                    "overlap": not a.no_overlap,
                    "l2": f"inputs larger than L2 ({r['stack_gb']:.2f} GB stack > 129 MB)",
@@ -508,7 +530,10 @@ def main():
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "peak_source": f"{peak:.0f} GB/s of {peak_src}",
         "roofline": {"bound": "hbm", "achieved": round(dom["gbs"], 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(dom["gbs"] / peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(dom["gbs"] / peak, 4),
+                     "traffic": profiled_traffic(
+                         f"gemv_{a.workload}_gateup.md",
+                         "weight_only_quantized_dequant_gb300/csrc/k_gemv.cu"),
                      "kernel": f"gemv ({dom['group']} grouped launch)",
                      "bytes_per_launch": dom["bytes_per_launch"],
                      "avg_launch_us": round(dom["avg_ms"] * 1e3, 3),

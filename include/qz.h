@@ -125,7 +125,18 @@ qz_status qz_gemv_int8(const qz_int8_weight *w, const qz_half *x, qz_half *y,
  * tensor cores (tcgen05, fp16 x fp16 products of the exact codes, fp32
  * accumulation in tensor memory). */
 qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X,
-                       int64_t ldx, qz_half *Y, int64_t ldy, qz_stream s);
+                       int64_t ldx, qz_half *Y, int64_t ldy, void *workspace,
+                       size_t workspace_bytes, qz_stream s);
+
+/* Device workspace the batched calls use on the tensor-core path: the
+ * permuted inputs are gathered once per call into tensor-core tiles there,
+ * then streamed into the GEMM by bulk copies.  B inputs of K channels with
+ * n_out outlier channels (0 for INT8); 0 for invalid sizes.  Host only.
+ * The workspace argument of qz_gemm_* may be NULL (the tensor-core kernel then
+ * gathers its inputs itself, much more slowly); if given it must be 16-byte
+ * aligned and at least this many bytes, caller-owned, and not used by other
+ * work while the call runs.  The CUDA-core path ignores it. */
+size_t qz_gemm_workspace_bytes(int64_t B, int64_t K, int64_t n_out);
 
 /* n matrices (1 <= n <= QZ_MAX_GROUP) that read the same input x, in one
  * launch (q/k/v, gate/up).  Each keeps its own scale.  ws: host array of n
@@ -210,7 +221,8 @@ qz_status qz_gemv_int4_outlier(const qz_int4o_weight *w, const qz_half *x,
  * and meet as y = D_out + s_i * D_bg. */
 qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B,
                                const qz_half *X, int64_t ldx, qz_half *Y,
-                               int64_t ldy, qz_stream s);
+                               int64_t ldy, void *workspace,
+                               size_t workspace_bytes, qz_stream s);
 
 /* n matrices sharing one input and one permutation (same perm pointer, K and
  * n_out), one launch.  ws: host array; ys: host array of device pointers. */

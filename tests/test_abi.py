@@ -65,6 +65,14 @@ def test_overlap_setting_is_per_thread_and_validated(lib):
     assert lib.qz_set_overlap(0) == OK and lib.qz_get_overlap() == 0
 
 
+def test_workspace_bytes(lib):
+    # ceil(n_out/64) + ceil((K-n_out)/64) tiles of Np x 64 fp16, Np = B rounded to 16
+    assert lib.qz_gemm_workspace_bytes(64, 4096, 41) == (1 + 64) * 64 * 64 * 2
+    assert lib.qz_gemm_workspace_bytes(5, 100, 0) == 2 * 16 * 64 * 2
+    assert lib.qz_gemm_workspace_bytes(65, 100, 0) == 0
+    assert lib.qz_gemm_workspace_bytes(1, 100, 101) == 0
+
+
 def test_version_and_status_strings(lib):
     assert lib.qz_version() >= 10000
     for code, name in _lib.STATUS.items():
@@ -117,10 +125,10 @@ def test_gemv_int8_validation(lib):
     assert lib.qz_gemv_int8(ctypes.byref(_w8(ldq=40)), P, P, None) == ALIGN
     assert lib.qz_gemv_int8(ctypes.byref(_w8(ldq=16)), P, P, None) == INVAL
     assert lib.qz_gemv_int8(ctypes.byref(_w8(K=57360, ldq=57360)), P, P, None) == UNSUP
-    assert lib.qz_gemm_int8(ctypes.byref(w), 65, P, 32, P, 8, None) == UNSUP
-    assert lib.qz_gemm_int8(ctypes.byref(w), 0, P, 32, P, 8, None) == INVAL
-    assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 16, P, 8, None) == INVAL   # ldx < K
-    assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 32, P + 1, 8, None) == ALIGN
+    assert lib.qz_gemm_int8(ctypes.byref(w), 65, P, 32, P, 8, None, 0, None) == UNSUP
+    assert lib.qz_gemm_int8(ctypes.byref(w), 0, P, 32, P, 8, None, 0, None) == INVAL
+    assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 16, P, 8, None, 0, None) == INVAL  # ldx < K
+    assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 32, P + 1, 8, None, 0, None) == ALIGN
 
 
 def test_grouped_int8_validation(lib):
@@ -150,7 +158,7 @@ def test_gemv_int4_validation(lib):
     assert g(_w4(q4=PU)) == ALIGN
     assert g(_w4(K=57345)) == UNSUP
     w = _w4()
-    assert lib.qz_gemm_int4_outlier(ctypes.byref(w), 65, P, 64, P, 8, None) == UNSUP
+    assert lib.qz_gemm_int4_outlier(ctypes.byref(w), 65, P, 64, P, 8, None, 0, None) == UNSUP
 
 
 def test_grouped_int4_requires_shared_perm(lib):

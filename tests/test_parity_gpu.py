@@ -221,6 +221,26 @@ def test_int4_grouped_matches_separate():
         assert_close(y, y_ref[0], a_ref[0], "grouped int4")
 
 
+@pytest.mark.parametrize("fmt", ["int8", "int4o"])
+@pytest.mark.parametrize("B", [5, 64])
+def test_tensor_core_without_workspace(fmt, B):
+    """The tensor-core kernel also works without a workspace (it gathers the
+    permuted inputs itself) and gives the same bits as with one."""
+    N, K = 300, 3072
+    X = S.activation(B, K, 9100 + B, device=DEV)
+    if fmt == "int8":
+        w = qz().quantize_int8(S.weight(N, K, 9101, device=DEV))
+        a = qz().gemm_int8(w, X, workspace=False)
+        b = qz().gemm_int8(w, X)
+    else:
+        W, prof, perm = _int4_inputs(N, K, 31, 9102)
+        w = qz().quantize_int4_outlier(W, perm, 31)
+        a = qz().gemm_int4_outlier(w, X, workspace=False)
+        b = qz().gemm_int4_outlier(w, X)
+    assert qz().device_error() == 0
+    assert torch.equal(a, b)
+
+
 def test_tensor_core_7b_batch64_full_matrix():
     """The 7B gate projection (11008 x 4096) at batch 64 on the tensor
     cores, every output checked."""

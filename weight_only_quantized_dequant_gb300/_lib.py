@@ -52,7 +52,8 @@ _SIGS = {
                               c_void_p, c_void_p]),
     "qz_gemv_int8": (_S, [POINTER(Int8Weight), c_void_p, c_void_p, c_void_p]),
     "qz_gemm_int8": (_S, [POINTER(Int8Weight), c_int64, c_void_p, c_int64, c_void_p,
-                          c_int64, c_void_p]),
+                          c_int64, c_void_p, c_size_t, c_void_p]),
+    "qz_gemm_workspace_bytes": (c_size_t, [c_int64, c_int64, c_int64]),
     "qz_gemv_int8_grouped": (_S, [POINTER(Int8Weight), c_int, c_void_p, POINTER(c_void_p),
                                   c_void_p]),
     "qz_int4o_layout": (_S, [c_int64, c_int64, c_int64, POINTER(c_int64), POINTER(c_int64)]),
@@ -64,7 +65,7 @@ _SIGS = {
                                       c_void_p]),
     "qz_gemv_int4_outlier": (_S, [POINTER(Int4oWeight), c_void_p, c_void_p, c_void_p]),
     "qz_gemm_int4_outlier": (_S, [POINTER(Int4oWeight), c_int64, c_void_p, c_int64,
-                                  c_void_p, c_int64, c_void_p]),
+                                  c_void_p, c_int64, c_void_p, c_size_t, c_void_p]),
     "qz_gemv_int4_outlier_grouped": (_S, [POINTER(Int4oWeight), c_int, c_void_p,
                                           POINTER(c_void_p), c_void_p]),
     "qz_pager_create": (_S, [POINTER(c_void_p), POINTER(c_size_t), c_int, c_void_p, c_void_p,

@@ -112,13 +112,35 @@ def gemv_int8(w: Int8Matrix, x: torch.Tensor, y: torch.Tensor | None = None, str
     return y
 
 
-def gemm_int8(w: Int8Matrix, X: torch.Tensor, Y: torch.Tensor | None = None, stream=None):
-    """Y [B, N] = fp16(scale * X @ q^T) for X [B, K], B <= 64."""
+def gemm_workspace_bytes(B: int, K: int, n_out: int = 0) -> int:
+    """Device workspace of the tensor-core path for B inputs of K channels."""
+    return int(_lib.load().qz_gemm_workspace_bytes(B, K, n_out))
+
+
+def _workspace(X: torch.Tensor, K: int, n_out: int, workspace):
+    """The caller's workspace, a fresh one (B > 4), or None."""
+    B = X.shape[0]
+    if workspace is False:  # explicitly none: the kernel gathers its inputs itself
+        return None, 0
+    if workspace is None:
+        if B <= 4:
+            return None, 0
+        nbytes = gemm_workspace_bytes(B, K, n_out)
+        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=X.device)
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def gemm_int8(w: Int8Matrix, X: torch.Tensor, Y: torch.Tensor | None = None, stream=None,
+              workspace=None):
+    """Y [B, N] = fp16(scale * X @ q^T) for X [B, K], B <= 64.  workspace: a
+    uint8 device tensor of gemm_workspace_bytes(B, K) bytes (allocated here if
+    None and B > 4; False to let the tensor-core kernel gather by itself)."""
     _need_cuda(X)
     B = X.shape[0]
     Y = _vec_out(X, w.N, B) if Y is None else Y
+    wp, wb = _workspace(X, w.K, 0, workspace)
     _lib.call("qz_gemm_int8", ctypes.byref(w.struct()), B, X.data_ptr(), X.stride(0),
-              Y.data_ptr(), Y.stride(0), _stream(stream))
+              Y.data_ptr(), Y.stride(0), wp, wb, _stream(stream))
     return Y
 
 
@@ -242,12 +264,14 @@ def gemv_int4_outlier(w: Int4oMatrix, x: torch.Tensor, y: torch.Tensor | None = 
 
 
 def gemm_int4_outlier(w: Int4oMatrix, X: torch.Tensor, Y: torch.Tensor | None = None,
-                      stream=None):
+                      stream=None, workspace=None):
+    """Y [B, N] for X [B, K]; workspace as for gemm_int8."""
     _need_cuda(X)
     B = X.shape[0]
     Y = _vec_out(X, w.N, B) if Y is None else Y
+    wp, wb = _workspace(X, w.K, w.n_out, workspace)
     _lib.call("qz_gemm_int4_outlier", ctypes.byref(w.struct()), B, X.data_ptr(), X.stride(0),
-              Y.data_ptr(), Y.stride(0), _stream(stream))
+              Y.data_ptr(), Y.stride(0), wp, wb, _stream(stream))
     return Y
 
 

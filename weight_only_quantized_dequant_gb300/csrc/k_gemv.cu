@@ -14,17 +14,19 @@
 // Design (HBM-bound stream; on GB300 the ALU and FMA pipes and the shared
 // memory pipe are close behind, so every instruction per weight counts):
 //  * x is gathered through the permutation into shared memory once per CTA,
-//    as fp32 and, for INT4, pre-scaled by 16^-(t' mod 4) so that one LOP3
-//    turns a nibble into the fp32 number 2^23 + (q+8)*16^p and one packed
-//    subtract leaves q*16^p exactly.  Staged chunks are padded by 16 bytes
-//    (conflict-free for the 8 lanes of a 128-bit phase), so every shared read
-//    is a per-lane base plus an immediate offset.
+//    in fp16.  Codes become exact fp16 integers two at a time: one LOP3 puts
+//    a nibble pair (or, via PRMT, a byte pair) under the 0x6400 exponent and
+//    one packed fp16 subtract removes the offset.  Products use the
+//    mixed-precision fma.rn.f32.f16 (fp16 x fp16, exact, added in fp32; one
+//    full-rate instruction), so no code or input is ever widened to fp32.
+//    Staged chunks are padded by 16 bytes (conflict-free for the 8 lanes of a
+//    128-bit phase), so every shared read is a per-lane base plus an
+//    immediate offset.
 //  * A warp computes R rows at once: each staged granule is read once for
 //    all R rows, halving the shared-memory traffic per weight.
 //  * Loads are software-pipelined in registers: the next group of chunks
 //    (possibly of the next rows) is issued before the current one is
 //    consumed, and each warp bulk-prefetches its following rows into L2.
-//  * Products use the sm_100+ packed fp32x2 add/FMA (two weights per issue).
 //  * CTAs own contiguous, equal row ranges; the grid is the SM count times
 //    the resident CTAs per SM.
 #include "qz_internal.cuh"
@@ -55,76 +57,103 @@ __device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) 
   return d;
 }
 
-__device__ __forceinline__ float4 lds(const float4 *base, uint32_t byte_off) {
-  return *reinterpret_cast<const float4 *>(reinterpret_cast<const char *>(base) + byte_off);
+// c0 += q.lo * x.lo, c1 += q'.lo * x.hi, c2 += q.hi * y.lo, c3 += q'.hi * y.hi
+// with fp16 pairs q, q', x, y and fp32 accumulators (fma.rn.f32.f16).
+__device__ __forceinline__ void fhfma4(float &c0, float &c1, float &c2, float &c3, uint32_t q,
+                                       uint32_t qq, uint32_t x, uint32_t y) {
+  asm("{\n\t.reg .f16 q0,q1,r0,r1,x0,x1,y0,y1;\n\t"
+      "mov.b32 {q0,q1}, %4;\n\tmov.b32 {r0,r1}, %5;\n\t"
+      "mov.b32 {x0,x1}, %6;\n\tmov.b32 {y0,y1}, %7;\n\t"
+      "fma.rn.f32.f16 %0, q0, x0, %0;\n\tfma.rn.f32.f16 %1, r0, x1, %1;\n\t"
+      "fma.rn.f32.f16 %2, q1, y0, %2;\n\tfma.rn.f32.f16 %3, r1, y1, %3;\n\t}"
+      : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
+      : "r"(q), "r"(qq), "r"(x), "r"(y));
 }
 
-// Outlier inputs: granule g (0/1) of outlier chunk c, XOR-swizzled.
-__device__ __forceinline__ int ogidx(int c, int g) { return c * 2 + (g ^ ((c >> 2) & 1)); }
+// c0 += q.lo * x.lo, c1 += q.hi * x.hi
+__device__ __forceinline__ void fhfma2(float &c0, float &c1, uint32_t q, uint32_t x) {
+  asm("{\n\t.reg .f16 q0,q1,x0,x1;\n\t"
+      "mov.b32 {q0,q1}, %2;\n\tmov.b32 {x0,x1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, q0, x0, %0;\n\tfma.rn.f32.f16 %1, q1, x1, %1;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(q), "r"(x));
+}
 
-// 32 nibbles of one chunk of each of R rows against the staged input at byte
-// offset `o` (granule g at o + 16 g).  For nibble p (0..3) of a half-word,
-// (w & 0xF<<4p) ^ (0x4B000000 | 8<<4p) is 2^23 + (q+8)*16^p; subtracting
-// 2^23 + 8*16^p leaves q*16^p, and the staged input is x*16^-p.
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Accumulators of one row and batch row: [0],[2] collect unscaled products,
+// [1],[3] products of codes taken at 16x (INT4 odd nibbles); the background
+// sum is (a0 + a2) + (a1 + a3) / 16.
+using Acc4 = float[4];
+
+// 32 nibbles of one chunk of each of R rows against the staged fp16 input at
+// byte offset `o` (8 inputs per 16-byte granule).  In a word of 8 nibbles
+// (elements e0..e7 at bits 4e..4e+3):
+//   (w & 0x000F000F) ^ 0x64086408 = fp16 pair (1024 + q0 + 8, 1024 + q4 + 8)
+//   (w & 0x00F000F0) ^ 0x64806480 = (1152 + 16 q1, 1152 + 16 q5)
+// and the same on w >> 8 for e2,e6 and e3,e7; subtracting 1032 resp. 1152
+// leaves q resp. 16 q exactly.
 template <int B, int R>
-__device__ __forceinline__ void int4_chunk(const uint4 (&v)[R], const float4 *xs, uint32_t o,
-                                           uint32_t bstride, float2 (&acc)[R][B][2]) {
+__device__ __forceinline__ void int4_chunk(const uint4 (&v)[R], const void *xs, uint32_t o,
+                                           uint32_t bstride, Acc4 (&acc)[R][B]) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < 4; ++k) {  // word k: elements 8k .. 8k+7 = granule k
+    uint4 xv[B];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float4 xv[B];
+    for (int b = 0; b < B; ++b)
+      xv[b] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(xs) + o + k * 16 +
+                                               b * bstride);
 #pragma unroll
-      for (int b = 0; b < B; ++b) xv[b] = lds(xs, o + (2 * k + h) * 16 + b * bstride);
+    for (int rr = 0; rr < R; ++rr) {
+      const uint32_t w = k == 0 ? v[rr].x : k == 1 ? v[rr].y : k == 2 ? v[rr].z : v[rr].w;
+      const uint32_t w8 = w >> 8;
+      const uint32_t qa = hsub2_bits(and_xor(w, 0x000F000Fu, 0x64086408u), 0x64086408u);
+      const uint32_t qb = hsub2_bits(and_xor(w, 0x00F000F0u, 0x64806480u), 0x64806480u);
+      const uint32_t qc = hsub2_bits(and_xor(w8, 0x000F000Fu, 0x64086408u), 0x64086408u);
+      const uint32_t qd = hsub2_bits(and_xor(w8, 0x00F000F0u, 0x64806480u), 0x64806480u);
 #pragma unroll
-      for (int rr = 0; rr < R; ++rr) {
-        const uint32_t w = k == 0 ? v[rr].x : k == 1 ? v[rr].y : k == 2 ? v[rr].z : v[rr].w;
-        const uint32_t ww = h ? (w >> 16) : w;
-        const float f0 = __uint_as_float(and_xor(ww, 0x000Fu, 0x4B000008u));
-        const float f1 = __uint_as_float(and_xor(ww, 0x00F0u, 0x4B000080u));
-        const float f2 = __uint_as_float(and_xor(ww, 0x0F00u, 0x4B000800u));
-        const float f3 = __uint_as_float(and_xor(ww, 0xF000u, 0x4B008000u));
-        const float2 qa = __fadd2_rn(make_float2(f0, f1),
-                                     make_float2(-8388616.0f, -8388736.0f));
-        const float2 qb = __fadd2_rn(make_float2(f2, f3),
-                                     make_float2(-8390656.0f, -8421376.0f));
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-          acc[rr][b][0] = __ffma2_rn(qa, make_float2(xv[b].x, xv[b].y), acc[rr][b][0]);
-          acc[rr][b][1] = __ffma2_rn(qb, make_float2(xv[b].z, xv[b].w), acc[rr][b][1]);
-        }
+      for (int b = 0; b < B; ++b) {
+        // xv.x = (x0,x1), .y = (x2,x3), .z = (x4,x5), .w = (x6,x7)
+        fhfma4(acc[rr][b][0], acc[rr][b][1], acc[rr][b][2], acc[rr][b][3], qa, qb, xv[b].x,
+               xv[b].z);
+        fhfma4(acc[rr][b][0], acc[rr][b][1], acc[rr][b][2], acc[rr][b][3], qc, qd, xv[b].y,
+               xv[b].w);
       }
     }
   }
 }
 
 // 16 int8 codes of one chunk of each of R rows.  XOR 0x80 makes each byte the
-// offset-binary u = q + 128; PRMT drops it into the low byte of 2^23's bit
-// pattern, and subtracting 2^23 + 128 leaves q exactly.
+// offset-binary u = q + 128; PRMT puts two of them under the 0x6400 exponent
+// (fp16 1024 + u) and subtracting 1152 leaves q exactly.
 template <int B, int R>
-__device__ __forceinline__ void int8_chunk(const uint4 (&v)[R], const float4 *xs, uint32_t o,
-                                           uint32_t bstride, float2 (&acc)[R][B][2]) {
+__device__ __forceinline__ void int8_chunk(const uint4 (&v)[R], const void *xs, uint32_t o,
+                                           uint32_t bstride, Acc4 (&acc)[R][B]) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float4 xv[B];
+  for (int k2 = 0; k2 < 2; ++k2) {  // words 2k2, 2k2+1: elements 8k2 .. 8k2+7
+    uint4 xv[B];
 #pragma unroll
-    for (int b = 0; b < B; ++b) xv[b] = lds(xs, o + k * 16 + b * bstride);
+    for (int b = 0; b < B; ++b)
+      xv[b] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(xs) + o + k2 * 16 +
+                                               b * bstride);
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
-      const uint32_t w =
-          (k == 0 ? v[rr].x : k == 1 ? v[rr].y : k == 2 ? v[rr].z : v[rr].w) ^ 0x80808080u;
-      const float f0 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440));
-      const float f1 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7441));
-      const float f2 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7442));
-      const float f3 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7443));
-      const float2 qa = __fadd2_rn(make_float2(f0, f1),
-                                   make_float2(-8388736.0f, -8388736.0f));
-      const float2 qb = __fadd2_rn(make_float2(f2, f3),
-                                   make_float2(-8388736.0f, -8388736.0f));
+      const uint32_t w0 = (k2 == 0 ? v[rr].x : v[rr].z) ^ 0x80808080u;
+      const uint32_t w1 = (k2 == 0 ? v[rr].y : v[rr].w) ^ 0x80808080u;
+      const uint32_t q01 = hsub2_bits(__byte_perm(w0, 0x64646464u, 0x4140), 0x64806480u);
+      const uint32_t q23 = hsub2_bits(__byte_perm(w0, 0x64646464u, 0x4342), 0x64806480u);
+      const uint32_t q45 = hsub2_bits(__byte_perm(w1, 0x64646464u, 0x4140), 0x64806480u);
+      const uint32_t q67 = hsub2_bits(__byte_perm(w1, 0x64646464u, 0x4342), 0x64806480u);
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        acc[rr][b][0] = __ffma2_rn(qa, make_float2(xv[b].x, xv[b].y), acc[rr][b][0]);
-        acc[rr][b][1] = __ffma2_rn(qb, make_float2(xv[b].z, xv[b].w), acc[rr][b][1]);
+        fhfma2(acc[rr][b][0], acc[rr][b][2], q01, xv[b].x);
+        fhfma2(acc[rr][b][0], acc[rr][b][2], q23, xv[b].y);
+        fhfma2(acc[rr][b][0], acc[rr][b][2], q45, xv[b].z);
+        fhfma2(acc[rr][b][0], acc[rr][b][2], q67, xv[b].w);
       }
     }
   }
@@ -153,8 +182,9 @@ constexpr unsigned long long kWaitNs = 2000000000ull;
 
 template <int B>
 struct Ring {
-  static constexpr int NS = B == 1 ? 3 : 2;    // stages per warp
+  static constexpr int NS = 2;                 // stages per warp
   static constexpr int R = B == 1 ? 2 : 1;     // rows per warp
+  static constexpr int MINB = B == 1 ? 2 : 1;  // CTAs per SM the registers allow
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
@@ -192,30 +222,39 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Row boundaries of the grouped matrices, kept in registers (32-bit rows:
+// the host limits a launch to < 2^31 rows).
+struct Bounds {
+  int end[QZ_MAX_GROUP];
+  int n;
+};
+
 // Row r of the launch -> (matrix, row inside it).
-__device__ __forceinline__ void locate(const GemvParams &p, int64_t r, int &m, int64_t &i) {
+__device__ __forceinline__ void locate(const Bounds &bd, int r, int &m, int &i) {
   m = 0;
 #pragma unroll
-  for (int t = 0; t < QZ_MAX_GROUP - 1; ++t) m += (t < p.n_mats - 1 && r >= p.row_end[t]) ? 1 : 0;
-  i = r - (m ? p.row_end[m - 1] : 0);
+  for (int t = 0; t < QZ_MAX_GROUP - 1; ++t) m += (t < bd.n - 1 && r >= bd.end[t]) ? 1 : 0;
+  int lo = 0;
+#pragma unroll
+  for (int t = 0; t < QZ_MAX_GROUP - 1; ++t) lo = (t < m) ? bd.end[t] : lo;
+  i = r - lo;
 }
 
 template <bool INT4, int B>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
     gemv_kernel(const __grid_constant__ GemvParams p) {
   constexpr int R = Ring<B>::R, NS = Ring<B>::NS;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  constexpr int GPC = INT4 ? 8 : 4;        // 16-byte granules per code chunk
-  constexpr int EPC = GPC * 4;             // inputs per code chunk
-  constexpr uint32_t CS = (GPC + 1) * 16;  // staged bytes per chunk (padded)
+  constexpr int EPC = INT4 ? 32 : 16;      // fp16 inputs per code chunk
+  constexpr uint32_t CS = EPC * 2 + 16;    // staged bytes per chunk (padded by 16)
   const int cpr = p.cpr;
   const int Jw = (cpr + 31) >> 5;          // rounds of 32 chunks per row
   const int staged = (Jw > 0 ? Jw : 1) * 32;
   const uint32_t bstride = (uint32_t)staged * CS;  // bytes per batch row
-  const int ostride = p.ocpr * 2;          // outlier granules per batch row
-  float4 *xs = reinterpret_cast<float4 *>(smem_raw);
-  float4 *xo = reinterpret_cast<float4 *>(smem_raw + B * bstride);
-  uint8_t *ring = smem_raw + (((size_t)B * bstride + (size_t)B * ostride * 16 + 127) & ~(size_t)127);
+  const uint32_t ostride = (uint32_t)p.ocpr * 16;  // outlier input bytes per batch row
+  __half *xs = reinterpret_cast<__half *>(smem_raw);
+  __half *xo = reinterpret_cast<__half *>(smem_raw + B * bstride);
+  uint8_t *ring = smem_raw + (((size_t)B * bstride + (size_t)B * ostride + 127) & ~(size_t)127);
   uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)kWarps * NS * R * kStageRow);
 
   const int64_t r0 = p.total_rows * blockIdx.x / gridDim.x;
@@ -251,138 +290,138 @@ __global__ void __launch_bounds__(kThreads, 1)
   // let the next kernel on the stream get scheduled as SMs free up
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- stage x (gathered through perm for INT4) in shared memory ---------
-  float *xsf = reinterpret_cast<float *>(xs);
+  // ---- stage x (gathered through perm for INT4) in shared memory, fp16 ----
   const int elems = staged * EPC;
+  const __half hzero = __ushort_as_half((unsigned short)0);
 #pragma unroll 1
   for (int b = 0; b < B; ++b) {
     const __half *xb = p.x + b * p.ldx;
 #pragma unroll 1
     for (int e = threadIdx.x; e < elems; e += kThreads) {
-      float val = 0.0f;
-      if (e < p.kb) {
-        if constexpr (INT4) {
-          const int ch = __ldg(p.perm + p.n_out + e);
-          const float sc = (e & 3) == 0   ? 1.0f
-                           : (e & 3) == 1 ? 0.0625f
-                           : (e & 3) == 2 ? 0.00390625f
-                                          : 0.000244140625f;
-          val = __half2float(xb[ch]) * sc;  // exact: power-of-two scaling
-        } else {
-          val = __half2float(xb[e]);
-        }
-      }
-      const int c = e / EPC, u = e % EPC;
-      xsf[(b * bstride + c * CS + (u >> 2) * 16) / 4 + (u & 3)] = val;
+      __half val = hzero;
+      if (e < p.kb) val = INT4 ? xb[__ldg(p.perm + p.n_out + e)] : xb[e];
+      xs[(b * bstride + (e / EPC) * CS) / 2 + e % EPC] = val;
     }
     if constexpr (INT4) {
-      float *xof = reinterpret_cast<float *>(xo);
 #pragma unroll 1
-      for (int e = threadIdx.x; e < ostride * 4; e += kThreads) {
-        const float val = e < p.n_out ? __half2float(xb[__ldg(p.perm + e)]) : 0.0f;
-        xof[(b * ostride + ogidx(e >> 3, (e & 7) >> 2)) * 4 + (e & 3)] = val;
-      }
+      for (int e = threadIdx.x; e < p.ocpr * 8; e += kThreads)
+        xo[b * ostride / 2 + e] = e < p.n_out ? xb[__ldg(p.perm + e)] : hzero;
     }
   }
   __syncthreads();
 
   // ---- each warp: row groups of R rows, streamed through its ring -----------
-  const int64_t first = r0 + (int64_t)warp * R;
-  const int64_t stride = (int64_t)kWarps * R;
-  if (first >= r1) return;  // no barrier follows
-  const int64_t P = (r1 - first + stride - 1) / stride;  // row groups of this warp
-  const int SPR = (Jw + kRPS - 1) / kRPS;                 // stages per row group
-  const int64_t items = P * SPR;
+  Bounds bd;
+#pragma unroll
+  for (int t = 0; t < QZ_MAX_GROUP; ++t) bd.end[t] = (int)p.row_end[t];
+  bd.n = p.n_mats;
+  const int rlo = (int)r0, rhi = (int)r1;
+  const int first = rlo + warp * R;
+  constexpr int stride = kWarps * R;
+  if (first >= rhi) return;  // no barrier follows
+  const int P = (rhi - first + stride - 1) / stride;  // row groups of this warp
+  const int SPR = (Jw + kRPS - 1) / kRPS;             // stages per row group
+  const int items = P * SPR;
   const uint32_t lane_off = (uint32_t)lane * CS;
   constexpr uint32_t kRound = 32u * CS;  // staged bytes per round of 32 chunks
   const uint32_t ring_w = smem_u32(ring) + (uint32_t)warp * NS * R * kStageRow;
   const uint32_t bar_w = smem_u32(&bars[warp * NS]);
 
-  // lane 0: copy stage `it` (row group it / SPR, rounds from (it % SPR) * kRPS)
-  auto issue = [&](int64_t it) {
-    const int64_t k = it / SPR;
-    const int j0 = (int)(it - k * SPR) * kRPS;
-    const int st = (int)(it % NS);
-    const int span = cpr - 32 * j0 < 32 * kRPS ? cpr - 32 * j0 : 32 * kRPS;  // chunks
-    const uint32_t bytes = (uint32_t)span * 16u;
-    const uint32_t bar = bar_w + st * 8;
-    asm volatile(
-        "{\n\t.reg .b64 t;\n\t"
-        "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
-        "r"(bytes * R)
-        : "memory");
-    const int64_t rb = first + k * stride;
+  // Producer state (tracked by every lane so control flow stays uniform;
+  // only lane 0 issues): next stage to fill = row group pg, stage psj of it,
+  // ring slot pst; pptr = the rows' code pointers of group pg.
+  int pg = 0, psj = 0, pst = 0;
+  int pleft = items;
+  const uint8_t *pptr[R];
+  auto prow_setup = [&](int gidx) {
+    const int rb = first + gidx * stride;
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
-      const int64_t rc = rb + rr < r1 ? rb + rr : r1 - 1;  // past the end: alias a valid row
-      int m;
-      int64_t i;
-      locate(p, rc, m, i);
-      const uint8_t *src = p.codes[m] + i * p.ld_codes[m] + (size_t)j0 * kRoundBytes;
-      const uint32_t dst = ring_w + (uint32_t)(st * R + rr) * kStageRow;
+      const int rc = rb + rr < rhi ? rb + rr : rhi - 1;  // past the end: alias a valid row
+      int m, i;
+      locate(bd, rc, m, i);
+      pptr[rr] = p.codes[m] + (int64_t)i * p.ld_codes[m];
+    }
+  };
+  auto issue_next = [&]() {
+    if (lane == 0) {
+      const int j0 = psj * kRPS;
+      const int span = cpr - 32 * j0 < 32 * kRPS ? cpr - 32 * j0 : 32 * kRPS;  // chunks
+      const uint32_t bytes = (uint32_t)span * 16u;
+      const uint32_t bar = bar_w + pst * 8;
       asm volatile(
-          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-              "r"(dst),
-          "l"(src), "r"(bytes), "r"(bar)
+          "{\n\t.reg .b64 t;\n\t"
+          "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
+          "r"(bytes * R)
           : "memory");
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) {
+        const uint32_t dst = ring_w + (uint32_t)(pst * R + rr) * kStageRow;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+                "r"(dst),
+            "l"(pptr[rr] + j0 * kRoundBytes), "r"(bytes), "r"(bar)
+            : "memory");
+      }
+    }
+    --pleft;
+    pst = pst + 1 == NS ? 0 : pst + 1;
+    if (++psj == SPR) {
+      psj = 0;
+      if (++pg < P) prow_setup(pg);
     }
   };
 
-  if (lane == 0)
-    for (int64_t it = 0; it < NS - 1 && it < items; ++it) issue(it);
+  if (items > 0) prow_setup(0);
+  for (int it = 0; it < NS - 1 && pleft > 0; ++it) issue_next();
 
-  float2 acc[R][B][2];
+  Acc4 acc[R][B];
 #pragma unroll
   for (int rr = 0; rr < R; ++rr)
 #pragma unroll
-    for (int b = 0; b < B; ++b) acc[rr][b][0] = acc[rr][b][1] = make_float2(0.f, 0.f);
+    for (int b = 0; b < B; ++b) acc[rr][b][0] = acc[rr][b][1] = acc[rr][b][2] = acc[rr][b][3] = 0.f;
 
   bool ok = true;
-  int64_t k = 0;   // row group
-  int sj = 0;      // stage inside the row group
-  const int64_t groups_total = P;
-  for (int64_t g = 0; g < groups_total; ++g) {
+  int cst = 0;            // consumer ring slot
+  uint32_t cphase = 0;    // parity of the slot's current use
+  for (int g = 0; g < P; ++g) {
     // rows of this group: scales, matrix, and the outlier rows into L2
-    const int64_t rb = first + g * stride;
-    int mrow[R];
-    int64_t irow[R];
+    const int rb = first + g * stride;
+    int mrow[R], irow[R];
     float srow[R];
     bool live[R];
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
-      live[rr] = rb + rr < r1;
-      locate(p, live[rr] ? rb + rr : r1 - 1, mrow[rr], irow[rr]);
+      live[rr] = rb + rr < rhi;
+      locate(bd, live[rr] ? rb + rr : rhi - 1, mrow[rr], irow[rr]);
       srow[rr] = INT4 ? __ldg(p.scale[mrow[rr]] + irow[rr]) : __ldg(p.scale[mrow[rr]]);
       if (INT4 && p.ocpr && lane == 8 + rr)
-        prefetch_l2(p.w_out[mrow[rr]] + irow[rr] * p.ld_out[mrow[rr]], (uint32_t)p.ocpr * 16u);
+        prefetch_l2(p.w_out[mrow[rr]] + (int64_t)irow[rr] * p.ld_out[mrow[rr]],
+                    (uint32_t)p.ocpr * 16u);
     }
-    for (sj = 0; sj < SPR; ++sj) {
-      const int64_t it = g * SPR + sj;
-      if (ok && lane == 0 && it + NS - 1 < items) {
-        // the stage being refilled was read by every lane before the last
+    for (int sj = 0; sj < SPR; ++sj) {
+      if (ok && pleft > 0) {
+        // the slot being refilled was read by every lane before the last
         // __syncwarp; order those reads before the async-proxy write
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(it + NS - 1);
+        if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_next();
       }
-      const int st = (int)(it % NS);
-      if (ok) ok = mbar_wait(bar_w + st * 8, (uint32_t)((it / NS) & 1));
+      if (ok) ok = mbar_wait(bar_w + cst * 8, cphase);
       if (ok) {
-        const uint32_t sbase = ring_w + (uint32_t)st * R * kStageRow;
+        // Lanes whose chunk lies past the row's end read stale (finite) codes
+        // of the slot; their staged inputs are zero, so they add exact zeros.
+        const uint32_t sbase = ring_w + (uint32_t)cst * R * kStageRow + lane * 16;
 #pragma unroll
         for (int u = 0; u < kRPS; ++u) {
           const int j = sj * kRPS + u;
           if (j < Jw) {  // warp-uniform
-            const bool in = lane + 32 * j < cpr;
             uint4 v[R];
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) {
-              v[rr] = make_uint4(0, 0, 0, 0);
-              if (in) {
-                const uint32_t a = sbase + (uint32_t)rr * kStageRow + u * kRoundBytes + lane * 16;
-                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(v[rr].x), "=r"(v[rr].y), "=r"(v[rr].z), "=r"(v[rr].w)
-                             : "r"(a));
-              }
+              const uint32_t a = sbase + (uint32_t)rr * kStageRow + u * kRoundBytes;
+              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(v[rr].x), "=r"(v[rr].y), "=r"(v[rr].z), "=r"(v[rr].w)
+                           : "r"(a));
             }
             const uint32_t o = lane_off + (uint32_t)j * kRound;
             if constexpr (INT4) int4_chunk<B, R>(v, xs, o, bstride, acc);
@@ -391,36 +430,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
+      if (++cst == NS) {
+        cst = 0;
+        cphase ^= 1u;
+      }
     }
-    (void)k;
     // ---- row epilogue: outliers, scale, reduction, store --------------------
-    float outl[R][B];
+    float outl[R][B][2];
 #pragma unroll
     for (int rr = 0; rr < R; ++rr)
 #pragma unroll
-      for (int b = 0; b < B; ++b) outl[rr][b] = 0.0f;
+      for (int b = 0; b < B; ++b) outl[rr][b][0] = outl[rr][b][1] = 0.0f;
     if constexpr (INT4) {
 #pragma unroll
       for (int rr = 0; rr < R; ++rr) {
-        const uint4 *orow =
-            reinterpret_cast<const uint4 *>(p.w_out[mrow[rr]] + irow[rr] * p.ld_out[mrow[rr]]);
+        const uint4 *orow = reinterpret_cast<const uint4 *>(p.w_out[mrow[rr]] +
+                                                            (int64_t)irow[rr] * p.ld_out[mrow[rr]]);
 #pragma unroll 1
         for (int c = lane; c < p.ocpr; c += 32) {
           const uint4 v = ld_stream(orow + c);
-          const float2 h0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-          const float2 h1 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-          const float2 h2 = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
-          const float2 h3 = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
 #pragma unroll
           for (int b = 0; b < B; ++b) {
-            const float4 xa = xo[b * ostride + ogidx(c, 0)];
-            const float4 xc = xo[b * ostride + ogidx(c, 1)];
-            float a = outl[rr][b];
-            a = fmaf(h0.x, xa.x, a); a = fmaf(h0.y, xa.y, a);
-            a = fmaf(h1.x, xa.z, a); a = fmaf(h1.y, xa.w, a);
-            a = fmaf(h2.x, xc.x, a); a = fmaf(h2.y, xc.y, a);
-            a = fmaf(h3.x, xc.z, a); a = fmaf(h3.y, xc.w, a);
-            outl[rr][b] = a;
+            const uint4 xv = *reinterpret_cast<const uint4 *>(
+                reinterpret_cast<const char *>(xo) + b * ostride + c * 16);
+            fhfma2(outl[rr][b][0], outl[rr][b][1], v.x, xv.x);
+            fhfma2(outl[rr][b][0], outl[rr][b][1], v.y, xv.y);
+            fhfma2(outl[rr][b][0], outl[rr][b][1], v.z, xv.z);
+            fhfma2(outl[rr][b][0], outl[rr][b][1], v.w, xv.w);
           }
         }
       }
@@ -429,12 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rr = 0; rr < R; ++rr) {
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        const float bg =
-            (acc[rr][b][0].x + acc[rr][b][0].y) + (acc[rr][b][1].x + acc[rr][b][1].y);
+        const float bg = (acc[rr][b][0] + acc[rr][b][2]) + (acc[rr][b][1] + acc[rr][b][3]) * 0.0625f;
         // y = s_i * background + outliers, combined per lane, one reduction
-        const float yl = warp_sum(fmaf(srow[rr], bg, outl[rr][b]));
+        const float yl = warp_sum(fmaf(srow[rr], bg, outl[rr][b][0] + outl[rr][b][1]));
         if (lane == 0 && live[rr]) p.y[mrow[rr]][b * p.ldy + irow[rr]] = __float2half_rn(yl);
-        acc[rr][b][0] = acc[rr][b][1] = make_float2(0.f, 0.f);
+        acc[rr][b][0] = acc[rr][b][1] = acc[rr][b][2] = acc[rr][b][3] = 0.f;
       }
     }
   }
@@ -489,10 +524,10 @@ qz_status launch_t(const GemvParams &p, cudaStream_t s) {
 }  // namespace
 
 size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p) {
-  const size_t cs = int4 ? 144 : 80;  // padded staged bytes per chunk
+  const size_t cs = int4 ? 80 : 48;  // padded staged fp16 bytes per chunk
   const size_t rounds = p.cpr > 0 ? (size_t)(p.cpr + 31) / 32 : 1;
-  const size_t staged = (rounds * 32 * cs + (int4 ? (size_t)p.ocpr * 32 : 0)) * (size_t)B;
-  const size_t R = B == 1 ? 2 : 1, NS = B == 1 ? 3 : 2;
+  const size_t staged = (rounds * 32 * cs + (int4 ? (size_t)p.ocpr * 16 : 0)) * (size_t)B;
+  const size_t R = B == 1 ? 2 : 1, NS = 2;
   const size_t ring = (size_t)kWarps * NS * R * kStageRow;
   return ((staged + 127) & ~(size_t)127) + ring + (size_t)kWarps * NS * 8;
 }

@@ -42,6 +42,8 @@ struct TcParams {
   GemvParams g;
   int B;                // batch rows
   int Np;               // MMA N: B rounded up to 16
+  int S;                // CTAs per tile (cluster size): each does 1/S of the K tiles
+  const uint8_t *ws;    // gathered activations, one canonical B tile per K tile (or null)
   int ko;               // K tiles of the outlier block
   int kbt;              // K tiles of the background block
   int n_tiles[QZ_MAX_GROUP];
@@ -183,19 +185,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // tile -> matrix m, first row
-  const int tile = blockIdx.x;
+  // cluster of S CTAs per tile; this CTA takes K tiles [kt_begin, kt_end)
+  const int S = tp.S;
+  const int rank = (int)(blockIdx.x % (unsigned)S);
+  const int tile = (int)(blockIdx.x / (unsigned)S);
   int m = 0;
 #pragma unroll
   for (int t = 0; t < QZ_MAX_GROUP - 1; ++t) m += (t < p.n_mats - 1 && tile >= tp.tile_end[t]) ? 1 : 0;
   const int64_t row0 = (int64_t)(tile - (m ? tp.tile_end[m - 1] : 0)) * kM;
   const int64_t nrows = tp.mat_rows[m];
   const int ktiles = tp.ko + tp.kbt;
+  const int kt_begin = ktiles * rank / S, kt_end = ktiles * (rank + 1) / S;
+  const bool has_out = kt_begin < (kt_end < tp.ko ? kt_end : tp.ko);
+  const bool has_bg = (kt_begin > tp.ko ? kt_begin : tp.ko) < kt_end;
   const uint32_t ncols = tp.Np <= 16 ? 32 : (tp.Np <= 32 ? 64 : 128);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&full[s]), kProducers);
+      mbar_init(smem_u32(&full[s]), kProducers + (tp.ws ? 1 : 0));
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(done), 1);
@@ -223,9 +230,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     const int r = tid;  // weight row of this thread inside the tile
     const int64_t grow = row0 + r;
     const bool live = grow < nrows;
-    for (int kt = 0; kt < ktiles; ++kt) {
-      const int s = kt % kStages;
-      if (kt >= kStages && !mbar_wait(smem_u32(&empty[s]), ((kt / kStages) - 1) & 1, abort_flag))
+    for (int kt = kt_begin; kt < kt_end; ++kt) {
+      const int q = kt - kt_begin;  // position in this CTA's ring sequence
+      const int s = q % kStages;
+      if (q >= kStages && !mbar_wait(smem_u32(&empty[s]), ((q / kStages) - 1) & 1, abort_flag))
         break;
       uint8_t *A = a_st + s * kABytes;
       uint8_t *Bt = b_st + s * bBytes;
@@ -305,7 +313,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
           *reinterpret_cast<uint4 *>(A + core_off(r, 16 * h + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
-      // --- B: Np x 64 activations, gathered through perm
+      // --- B: Np x 64 activations.  With a workspace the tile was gathered
+      // once per call by tc_xprep_kernel and arrives by one bulk copy.
+      if (tp.ws) {
+        if (tid == 0) {
+          const uint32_t bar = smem_u32(&full[s]);
+          asm volatile(
+              "{\n\t.reg .b64 t;\n\t"
+              "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
+              "r"((uint32_t)bBytes)
+              : "memory");
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+              "[%3];" ::"r"(smem_u32(Bt)),
+              "l"(tp.ws + (size_t)kt * bBytes), "r"((uint32_t)bBytes), "r"(bar)
+              : "memory");
+        }
+      } else
       for (int idx = tid; idx < tp.Np * kKT; idx += kProducers) {
         const int c = idx % kKT, n = idx / kKT;
         __half v = __float2half_rn(0.0f);
@@ -330,13 +354,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   } else if (lane == 0) {
     // ------------------------------------------------------ MMA issuer ---
     const uint32_t idesc = idesc_f16(kM, tp.Np);
-    for (int kt = 0; kt < ktiles; ++kt) {
-      const int s = kt % kStages;
-      if (!mbar_wait(smem_u32(&full[s]), (kt / kStages) & 1, abort_flag)) break;
+    for (int kt = kt_begin; kt < kt_end; ++kt) {
+      const int q = kt - kt_begin;
+      const int s = q % kStages;
+      if (!mbar_wait(smem_u32(&full[s]), (q / kStages) & 1, abort_flag)) break;
       fence_after();
       const bool outl = kt < tp.ko;
       const uint32_t d = outl ? d_out : d_bg;
-      const bool first = outl ? kt == 0 : kt == tp.ko;
+      const bool first = outl ? kt == kt_begin : kt == (kt_begin > tp.ko ? kt_begin : tp.ko);
       const uint32_t a0 = smem_u32(a_st + s * kABytes), b0 = smem_u32(b_st + s * bBytes);
 #pragma unroll
       for (int k16 = 0; k16 < kKT / 16; ++k16)
@@ -348,6 +373,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   }
 
   // ---------------------------------------------------------- epilogue ----
+  // Each thread of warps 0-3 owns one row of the tile (its TMEM lane).
+  float *part = reinterpret_cast<float *>(a_st);  // S > 1: partials [Np][kM]
   if (warp < 4) {
     const bool ok = mbar_wait(smem_u32(done), 0, abort_flag);
     fence_after();
@@ -359,19 +386,48 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     for (int c0 = 0; c0 < tp.Np; c0 += 16) {
       float vb[16], vo[16];
       tmem_ld16(d_bg + lane_base + c0, vb);
-      if (INT4 && tp.ko > 0) tmem_ld16(d_out + lane_base + c0, vo);
-      if (ok && grow < nrows) {
+      if (INT4) tmem_ld16(d_out + lane_base + c0, vo);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = c0 + j;
-          if (n < tp.B) {
-            const float bg = tp.kbt > 0 ? vb[j] : 0.0f;
-            const float o = (INT4 && tp.ko > 0) ? vo[j] : 0.0f;
-            p.y[m][(int64_t)n * p.ldy + grow] = __float2half_rn(fmaf(s_i, bg, o));
-          }
+      for (int j = 0; j < 16; ++j) {
+        const int n = c0 + j;
+        const float bg = has_bg ? vb[j] : 0.0f;
+        const float o = (INT4 && has_out) ? vo[j] : 0.0f;
+        const float y = fmaf(s_i, bg, o);  // partial of this CTA's K tiles
+        if (S == 1) {
+          if (ok && grow < nrows && n < tp.B)
+            p.y[m][(int64_t)n * p.ldy + grow] = __float2half_rn(y);
+        } else {
+          part[n * kM + r] = ok ? y : 0.0f;
         }
       }
     }
+  }
+  if (S > 1) {
+    // Cluster reduction through distributed shared memory: every CTA has its
+    // partials in its own shared memory; CTA k sums rows [k*kM/S, (k+1)*kM/S)
+    // over all S CTAs and stores them.
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+    const int rlo = kM * rank / S, rhi = kM * (rank + 1) / S;
+    const int cnt = (rhi - rlo) * tp.Np;
+    const uint32_t part_local = smem_u32(part);
+    for (int e = tid; e < cnt; e += kThreadsTc) {
+      const int n = e / (rhi - rlo), r = rlo + e % (rhi - rlo);
+      const uint32_t off = (uint32_t)(n * kM + r) * 4u;
+      float acc = 0.0f;
+      for (int q = 0; q < S; ++q) {
+        uint32_t ra;
+        float v;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(part_local + off), "r"(q));
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+        acc += v;
+      }
+      const int64_t grow = row0 + r;
+      if (grow < nrows && n < tp.B) p.y[m][(int64_t)n * p.ldy + grow] = __float2half_rn(acc);
+    }
+    // keep every CTA's shared memory alive until all remote reads are done
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
   }
   fence_before();
   __syncthreads();
@@ -381,14 +437,54 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                  : "memory");
 }
 
+// The B operand of every K tile, gathered through the permutation (INT4:
+// in the k order of the nibble conversion) into the canonical K-major layout,
+// one contiguous tile of Np x 64 fp16 per K tile.  One CTA per K tile.
+template <bool INT4>
+__global__ void __launch_bounds__(256) tc_xprep_kernel(const __grid_constant__ TcParams tp,
+                                                       uint8_t *ws) {
+  const GemvParams &p = tp.g;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int kt = blockIdx.x;
+  const int bBytes = tp.Np * kKT * 2;
+  uint8_t *tile = ws + (size_t)kt * bBytes;
+  const bool outl = kt < tp.ko;
+  for (int idx = threadIdx.x; idx < tp.Np * kKT; idx += 256) {
+    const int c = idx % kKT, n = idx / kKT;
+    __half v = __ushort_as_half((unsigned short)0);
+    if (n < tp.B) {
+      const __half *xb = p.x + (int64_t)n * p.ldx;
+      if (INT4 && outl) {
+        const int t = kt * kKT + c;
+        if (t < p.n_out) v = xb[__ldg(p.perm + t)];
+      } else if (INT4) {
+        const int e = (kt - tp.ko) * kKT + slot_elem(c);
+        if (e < p.kb) v = xb[__ldg(p.perm + p.n_out + e)];
+      } else {
+        const int e = kt * kKT + c;
+        if (e < p.K) v = xb[e];
+      }
+    }
+    *reinterpret_cast<__half *>(tile + core_off(n, c)) = v;
+  }
+}
+
 }  // namespace
+
+size_t tc_workspace_bytes(bool int4, int64_t B, int64_t K, int64_t n_out) {
+  const int64_t Np = (B + 15) / 16 * 16;
+  const int64_t tiles = int4 ? (n_out + kKT - 1) / kKT + (K - n_out + kKT - 1) / kKT
+                             : (K + kKT - 1) / kKT;
+  return (size_t)(tiles * Np * kKT * 2);
+}
 
 size_t tc_smem_bytes(int Np) {
   return 1024 + (size_t)kStages * (kABytes + Np * kKT * 2) + (2 * kStages + 1) * 8 + 16;
 }
 
 qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_rows,
-                    cudaStream_t s) {
+                    void *workspace, size_t workspace_bytes, cudaStream_t s) {
   DeviceInfo di;
   qz_status st = device_info(&di);
   if (st != QZ_OK) return st;
@@ -398,6 +494,13 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   tp.Np = (B + 15) / 16 * 16;
   tp.ko = int4 ? (g.n_out + kKT - 1) / kKT : 0;
   tp.kbt = int4 ? (g.kb + kKT - 1) / kKT : (g.K + kKT - 1) / kKT;
+  tp.S = 1;
+  tp.ws = nullptr;
+  if (workspace) {
+    if (workspace_bytes < tc_workspace_bytes(int4, B, g.K, g.n_out)) return QZ_ERR_INVALID_ARG;
+    if ((uintptr_t)workspace & 15u) return QZ_ERR_ALIGNMENT;
+    tp.ws = reinterpret_cast<const uint8_t *>(workspace);
+  }
   int tiles = 0;
   for (int m = 0; m < QZ_MAX_GROUP; ++m) {
     tp.mat_rows[m] = m < g.n_mats ? mat_rows[m] : 0;
@@ -407,19 +510,62 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   }
   const size_t smem = tc_smem_bytes(tp.Np);
   if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
+  // Split K over a cluster of S CTAs per tile so that small matrices still
+  // fill the GPU: pick S in {1,2,4,8} minimising waves/S (the time of a
+  // wave shrinks with S), keeping at least two K tiles per CTA.
+  {
+    const int per_sm_smem = (int)(233472 / (smem + 1024));
+    const int per_sm_tmem = 512 / (tp.Np <= 16 ? 32 : (tp.Np <= 32 ? 64 : 128));
+    const int per_sm = per_sm_smem < per_sm_tmem ? per_sm_smem : per_sm_tmem;
+    const long slots = (long)di.sms * (per_sm > 0 ? per_sm : 1);
+    const int kt_total = tp.ko + tp.kbt;
+    double best = 1e30;
+    for (int S = 1; S <= 8; S *= 2) {
+      if (S > 1 && kt_total < 2 * S) break;
+      const long ctas = (long)tiles * S;
+      const double t = (double)((ctas + slots - 1) / slots) / S;
+      if (t < best - 1e-9) {
+        best = t;
+        tp.S = S;
+      }
+    }
+  }
   auto kern = int4 ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_status(e);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.gridDim = dim3((unsigned)(tiles * tp.S));
   cfg.blockDim = dim3(kThreadsTc);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = (unsigned)tp.S;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (g.overlap) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = g.overlap ? 1 : 0;
+  cfg.numAttrs = na;
+  if (tp.ws) {  // gather the activations once, then the GEMM
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3((unsigned)(tp.ko + tp.kbt));
+    pc.blockDim = dim3(256);
+    pc.stream = s;
+    cudaLaunchAttribute pa[1];
+    pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pa[0].val.programmaticStreamSerializationAllowed = 1;
+    pc.attrs = pa;
+    pc.numAttrs = g.overlap ? 1 : 0;
+    auto prep = int4 ? tc_xprep_kernel<true> : tc_xprep_kernel<false>;
+    e = cudaLaunchKernelEx(&pc, prep, tp, reinterpret_cast<uint8_t *>(workspace));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   e = cudaLaunchKernelEx(&cfg, kern, tp);
   if (e != cudaSuccess) return cuda_status(e);
   return launch_status();

@@ -64,7 +64,7 @@ qz_status check_int8_weight(const qz_int8_weight *w) {
   if (!w) return QZ_ERR_INVALID_ARG;
   QZ_TRY(check_mat(w->q, w->N, w->K, w->ldq, 1));
   if (!w->scale) return QZ_ERR_INVALID_ARG;
-  if (w->K > kMaxGemvK || w->N > (int64_t)1 << 40) return QZ_ERR_UNSUPPORTED;
+  if (w->K > kMaxGemvK || w->N > ((int64_t)1 << 30)) return QZ_ERR_UNSUPPORTED;
   return QZ_OK;
 }
 
@@ -80,7 +80,7 @@ qz_status check_int4o_weight(const qz_int4o_weight *w) {
   if ((w->w_out && !aligned16(w->w_out)) || (w->q4 && !aligned16(w->q4)) ||
       !aligned16(w->scale) || !aligned16(w->perm))
     return QZ_ERR_ALIGNMENT;
-  if (w->K > kMaxGemvK) return QZ_ERR_UNSUPPORTED;
+  if (w->K > kMaxGemvK || w->N > ((int64_t)1 << 30)) return QZ_ERR_UNSUPPORTED;
   return QZ_OK;
 }
 
@@ -152,7 +152,8 @@ void fill_int4o(GemvParams &p, const qz_int4o_weight *ws, int n) {
 }
 
 qz_status gemm_common(bool int4, GemvParams &p, int64_t B, const qz_half *X, int64_t ldx,
-                      qz_half *const *Ys, int64_t ldy, int n, cudaStream_t s) {
+                      qz_half *const *Ys, int64_t ldy, int n, void *ws, size_t ws_bytes,
+                      cudaStream_t s) {
   p.x = reinterpret_cast<const __half *>(X);
   p.overlap = overlap_enabled();
   p.ldx = B > 1 ? ldx : 0;
@@ -168,7 +169,7 @@ qz_status gemm_common(bool int4, GemvParams &p, int64_t B, const qz_half *X, int
   int64_t rows[QZ_MAX_GROUP];
   for (int m = 0; m < QZ_MAX_GROUP; ++m)
     rows[m] = m < n ? p.row_end[m] - (m ? p.row_end[m - 1] : 0) : 0;
-  return launch_tc(int4, (int)B, p, rows, s);
+  return launch_tc(int4, (int)B, p, rows, ws, ws_bytes, s);
 }
 
 }  // namespace
@@ -224,11 +225,12 @@ qz_status qz_quantize_int8(const qz_half *W, int64_t N, int64_t K, int64_t ldw, 
 }
 
 qz_status qz_gemv_int8(const qz_int8_weight *w, const qz_half *x, qz_half *y, qz_stream s) {
-  return qz_gemm_int8(w, 1, x, 0, y, 0, s);
+  return qz_gemm_int8(w, 1, x, 0, y, 0, nullptr, 0, s);
 }
 
 qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X, int64_t ldx,
-                       qz_half *Y, int64_t ldy, qz_stream s) {
+                       qz_half *Y, int64_t ldy, void *workspace, size_t workspace_bytes,
+                       qz_stream s) {
   QZ_TRY(check_int8_weight(w));
   if (B < 1) return QZ_ERR_INVALID_ARG;
   if (B > QZ_MAX_BATCH) return QZ_ERR_UNSUPPORTED;
@@ -237,7 +239,8 @@ qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X, int
   GemvParams p;
   fill_int8(p, w, 1);
   qz_half *ys[1] = {Y};
-  return gemm_common(false, p, B, X, ldx, ys, ldy, 1, (cudaStream_t)s);
+  return gemm_common(false, p, B, X, ldx, ys, ldy, 1, workspace, workspace_bytes,
+                     (cudaStream_t)s);
 }
 
 qz_status qz_gemv_int8_grouped(const qz_int8_weight *ws, int n, const qz_half *x,
@@ -252,7 +255,13 @@ qz_status qz_gemv_int8_grouped(const qz_int8_weight *ws, int n, const qz_half *x
   QZ_TRY(check_vec(x, 1, ws[0].K, 0));
   GemvParams p;
   fill_int8(p, ws, n);
-  return gemm_common(false, p, 1, x, 0, ys, 0, n, (cudaStream_t)s);
+  return gemm_common(false, p, 1, x, 0, ys, 0, n, nullptr, 0, (cudaStream_t)s);
+}
+
+size_t qz_gemm_workspace_bytes(int64_t B, int64_t K, int64_t n_out) {
+  if (B < 1 || B > QZ_MAX_BATCH || K < 1 || n_out < 0 || n_out > K) return 0;
+  // n_out = 0 gives the INT8 size (ceil(K/64) tiles of the gathered input)
+  return tc_workspace_bytes(true, B, K, n_out);
 }
 
 // ------------------------------------------------------------------ INT4 --
@@ -313,11 +322,12 @@ qz_status qz_quantize_int4_outlier(const qz_half *W, int64_t ldw, const int32_t 
 
 qz_status qz_gemv_int4_outlier(const qz_int4o_weight *w, const qz_half *x, qz_half *y,
                                qz_stream s) {
-  return qz_gemm_int4_outlier(w, 1, x, 0, y, 0, s);
+  return qz_gemm_int4_outlier(w, 1, x, 0, y, 0, nullptr, 0, s);
 }
 
 qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B, const qz_half *X,
-                               int64_t ldx, qz_half *Y, int64_t ldy, qz_stream s) {
+                               int64_t ldx, qz_half *Y, int64_t ldy, void *workspace,
+                               size_t workspace_bytes, qz_stream s) {
   QZ_TRY(check_int4o_weight(w));
   if (B < 1) return QZ_ERR_INVALID_ARG;
   if (B > QZ_MAX_BATCH) return QZ_ERR_UNSUPPORTED;
@@ -326,7 +336,8 @@ qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B, const qz_hal
   GemvParams p;
   fill_int4o(p, w, 1);
   qz_half *ys[1] = {Y};
-  return gemm_common(true, p, B, X, ldx, ys, ldy, 1, (cudaStream_t)s);
+  return gemm_common(true, p, B, X, ldx, ys, ldy, 1, workspace, workspace_bytes,
+                     (cudaStream_t)s);
 }
 
 qz_status qz_gemv_int4_outlier_grouped(const qz_int4o_weight *ws, int n, const qz_half *x,
@@ -342,7 +353,7 @@ qz_status qz_gemv_int4_outlier_grouped(const qz_int4o_weight *ws, int n, const q
   QZ_TRY(check_vec(x, 1, ws[0].K, 0));
   GemvParams p;
   fill_int4o(p, ws, n);
-  return gemm_common(true, p, 1, x, 0, ys, 0, n, (cudaStream_t)s);
+  return gemm_common(true, p, 1, x, 0, ys, 0, n, nullptr, 0, (cudaStream_t)s);
 }
 
 }  // extern "C"

@@ -36,6 +36,11 @@ class LayerStack:
         for l in range(self.n_layers):
             self.layers.append(self._build_layer(l, keep_fp16))
         self._alloc_io()
+        self.workspace = None
+        if batch > 1:  # one workspace for every batched call of the step
+            nb = max(api.gemm_workspace_bytes(batch, K, api.default_n_out(K) if wl.fmt == "int4o" else 0)
+                     for K in {wl.shape(m)[1] for m in S.MATS})
+            self.workspace = torch.empty((nb,), dtype=torch.uint8, device=self.device)
 
     # ------------------------------------------------------------ build ---
     def _build_layer(self, l: int, keep_fp16: bool) -> Layer:
@@ -104,7 +109,7 @@ class LayerStack:
         else:
             fn = api.gemm_int8 if int8 else api.gemm_int4_outlier
             for w, y in zip(mats, ys):
-                fn(w, x, y, stream=stream)
+                fn(w, x, y, stream=stream, workspace=self.workspace)
 
     def run_step(self, stream=None):
         for l in range(self.n_layers):
