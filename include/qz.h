@@ -224,6 +224,26 @@ qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B,
                                int64_t ldy, void *workspace,
                                size_t workspace_bytes, qz_stream s);
 
+/* Allocation-free variant of qz_gemm_int4_outlier.  The pages have no
+ * counterpart; it exists for callers that cannot allocate device memory at
+ * the point of the call (code running during CUDA-graph capture, where
+ * cudaMalloc is not allowed; plugins inside a host application that owns the
+ * device memory budget; loops that must not touch an allocator after
+ * start-up).  Instead of a caller workspace it uses a library-owned static
+ * device array of QZ_NOALLOC_SCRATCH_BYTES, which every GPU that loads the
+ * library holds until the process exits; it allocates nothing itself.
+ * Limit: qz_gemm_workspace_bytes(B, K, n_out) must not exceed
+ * QZ_NOALLOC_SCRATCH_BYTES (e.g. B = 64 up to K ~ 32k), else
+ * QZ_ERR_UNSUPPORTED.  All calls share the array (it keeps the last call's
+ * contents, every call rewrites what it reads): calls that overlap on the
+ * GPU, on any stream, race.  The first call on a device looks the array's
+ * device address up (cudaGetSymbolAddress) and should come before any stream
+ * capture.  Same arguments and result as qz_gemm_int4_outlier otherwise. */
+#define QZ_NOALLOC_SCRATCH_BYTES (4u << 20)
+qz_status qz_gemm_int4_outlier_noalloc(const qz_int4o_weight *w, int64_t B,
+                                       const qz_half *X, int64_t ldx,
+                                       qz_half *Y, int64_t ldy, qz_stream s);
+
 /* n matrices sharing one input and one permutation (same perm pointer, K and
  * n_out), one launch.  ws: host array; ys: host array of device pointers. */
 qz_status qz_gemv_int4_outlier_grouped(const qz_int4o_weight *ws, int n,

@@ -66,6 +66,8 @@ _SIGS = {
     "qz_gemv_int4_outlier": (_S, [POINTER(Int4oWeight), c_void_p, c_void_p, c_void_p]),
     "qz_gemm_int4_outlier": (_S, [POINTER(Int4oWeight), c_int64, c_void_p, c_int64,
                                   c_void_p, c_int64, c_void_p, c_size_t, c_void_p]),
+    "qz_gemm_int4_outlier_noalloc": (_S, [POINTER(Int4oWeight), c_int64, c_void_p, c_int64,
+                                          c_void_p, c_int64, c_void_p]),
     "qz_gemv_int4_outlier_grouped": (_S, [POINTER(Int4oWeight), c_int, c_void_p,
                                           POINTER(c_void_p), c_void_p]),
     "qz_pager_create": (_S, [POINTER(c_void_p), POINTER(c_size_t), c_int, c_void_p, c_void_p,

@@ -18,6 +18,8 @@
 //    per-row scale multiplies the background only: y = D_out + s_i * D_bg.
 //  * A 4-stage mbarrier ring decouples producers and the MMA thread; every
 //    wait is bounded in time and reports a timeout through a device flag.
+#include <mutex>
+
 #include "qz_internal.cuh"
 
 namespace qz {
@@ -585,3 +587,60 @@ qz_status read_device_error(int *code, int clear) {
 }
 
 }  // namespace qz
+
+// ---------------------------------------------------------------------------
+// Allocation-free batched INT4-outlier product.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// product: code that runs while a CUDA graph is being captured (cudaMalloc is
+// not a capturable operation), plugins that live inside a host application
+// which owns the device memory budget and hands out no allocator, and
+// real-time loops that must not touch the allocator after start-up.  For them
+// the tensor-core path's gathered-input workspace lives in a library-owned,
+// fixed-size device array instead of caller memory.  Every GPU that loads the
+// library holds this array until the process exits.
+// ---------------------------------------------------------------------------
+namespace qz {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB, QZ_NOALLOC_SCRATCH_BYTES
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array on the current device.  The name of a
+// __device__ array is only a host-side stand-in in host code, so its address
+// is looked up once per device with that device current.
+qz_status noalloc_scratch(void **out) {
+  constexpr int kMaxDev = 64;
+  static void *addr[kMaxDev];
+  static cudaError_t err[kMaxDev];
+  static std::once_flag once[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kMaxDev) return QZ_ERR_UNSUPPORTED;
+  std::call_once(once[dev], [&] {
+    err[dev] = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
+  });
+  if (err[dev] != cudaSuccess) return cuda_status(err[dev]);
+  *out = addr[dev];
+  return QZ_OK;
+}
+
+}  // namespace
+}  // namespace qz
+
+extern "C" qz_status qz_gemm_int4_outlier_noalloc(const qz_int4o_weight *w, int64_t B,
+                                                  const qz_half *X, int64_t ldx, qz_half *Y,
+                                                  int64_t ldy, qz_stream s) {
+  if (!w) return QZ_ERR_INVALID_ARG;
+  const size_t need = qz_gemm_workspace_bytes(B, w->K, w->n_out);
+  if (need == 0) return QZ_ERR_INVALID_ARG;  // B, K or n_out out of range
+  if (need > qz::kNoAllocScratchBytes) return QZ_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  qz_status st = qz::noalloc_scratch(&scratch);
+  if (st != QZ_OK) return st;
+  // The existing entry point with the scratch array as its workspace: the
+  // gather kernel rewrites every byte of the tiles it uses, so nothing needs
+  // clearing between calls.
+  return qz_gemm_int4_outlier(w, B, X, ldx, Y, ldy, scratch, qz::kNoAllocScratchBytes, s);
+}
