@@ -170,21 +170,21 @@ __device__ __forceinline__ float warp_sum(float v) {
 // shared memory: lane 0 issues cp.async.bulk copies (global -> shared, with
 // an mbarrier transaction count) kNS-1 stages ahead of the stage the lanes
 // are computing, so a warp keeps its next rows in flight without holding
-// them in registers.  A stage is kRPS rounds (32 chunks of 16 bytes) of each
+// them in registers.  A stage is RPS rounds (32 chunks of 16 bytes) of each
 // of the warp's R rows.  Every wait is bounded in time.
 // ---------------------------------------------------------------------------
 __device__ int g_gemv_error = 0;  // 1 if a bounded wait gave up (read by qz_device_error)
 
-constexpr int kRPS = 2;                        // rounds per stage
 constexpr uint32_t kRoundBytes = 512;          // 32 chunks x 16 bytes
-constexpr uint32_t kStageRow = kRPS * kRoundBytes;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 template <int B>
 struct Ring {
   static constexpr int NS = 2;                 // stages per warp
   static constexpr int R = B == 1 ? 2 : 1;     // rows per warp
-  static constexpr int MINB = B == 1 ? 2 : 1;  // CTAs per SM the registers allow
+  static constexpr int RPS = B == 1 ? 4 : 2;   // rounds per stage
+  static constexpr int MINB = 1;               // CTAs per SM the registers allow
+  static constexpr uint32_t STAGE_ROW = RPS * kRoundBytes;  // bytes of one row in a stage
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
@@ -243,7 +243,8 @@ __device__ __forceinline__ void locate(const Bounds &bd, int r, int &m, int &i) 
 template <bool INT4, int B>
 __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
     gemv_kernel(const __grid_constant__ GemvParams p) {
-  constexpr int R = Ring<B>::R, NS = Ring<B>::NS;
+  constexpr int R = Ring<B>::R, NS = Ring<B>::NS, kRPS = Ring<B>::RPS;
+  constexpr uint32_t kStageRow = Ring<B>::STAGE_ROW;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   constexpr int EPC = INT4 ? 32 : 16;      // fp16 inputs per code chunk
   constexpr uint32_t CS = EPC * 2 + 16;    // staged bytes per chunk (padded by 16)
@@ -527,8 +528,8 @@ size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p) {
   const size_t cs = int4 ? 80 : 48;  // padded staged fp16 bytes per chunk
   const size_t rounds = p.cpr > 0 ? (size_t)(p.cpr + 31) / 32 : 1;
   const size_t staged = (rounds * 32 * cs + (int4 ? (size_t)p.ocpr * 16 : 0)) * (size_t)B;
-  const size_t R = B == 1 ? 2 : 1, NS = 2;
-  const size_t ring = (size_t)kWarps * NS * R * kStageRow;
+  const size_t R = B == 1 ? 2 : 1, NS = 2, RPS = B == 1 ? 4 : 2;
+  const size_t ring = (size_t)kWarps * NS * R * RPS * kRoundBytes;
   return ((staged + 127) & ~(size_t)127) + ring + (size_t)kWarps * NS * 8;
 }
 
