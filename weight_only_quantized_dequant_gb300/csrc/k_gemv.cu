@@ -292,16 +292,38 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- stage x (gathered through perm for INT4) in shared memory, fp16 ----
-  const int elems = staged * EPC;
+  // Eight consecutive inputs per step and thread: eight perm entries, eight
+  // independent gathers, one 16-byte shared store (8 inputs never straddle a
+  // staged chunk); INT8 inputs are read in order.
+  const int elems = staged * EPC;           // multiple of 8
   const __half hzero = __ushort_as_half((unsigned short)0);
+  const int step8 = kThreads * 8;
 #pragma unroll 1
   for (int b = 0; b < B; ++b) {
     const __half *xb = p.x + b * p.ldx;
 #pragma unroll 1
-    for (int e = threadIdx.x; e < elems; e += kThreads) {
-      __half val = hzero;
-      if (e < p.kb) val = INT4 ? xb[__ldg(p.perm + p.n_out + e)] : xb[e];
-      xs[(b * bstride + (e / EPC) * CS) / 2 + e % EPC] = val;
+    for (int e0 = threadIdx.x * 8; e0 < elems; e0 += step8) {
+      uint32_t h[4];
+      if constexpr (INT4) {
+        int idx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) idx[k] = e0 + k < p.kb ? __ldg(p.perm + p.n_out + e0 + k) : -1;
+        __half v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = idx[k] >= 0 ? xb[idx[k]] : hzero;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          h[k] = (uint32_t)__half_as_ushort(v[2 * k]) | ((uint32_t)__half_as_ushort(v[2 * k + 1]) << 16);
+      } else {
+        __half v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = e0 + k < p.kb ? xb[e0 + k] : hzero;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          h[k] = (uint32_t)__half_as_ushort(v[2 * k]) | ((uint32_t)__half_as_ushort(v[2 * k + 1]) << 16);
+      }
+      *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(xs) + b * bstride + (e0 / EPC) * CS +
+                                 (e0 % EPC) * 2) = make_uint4(h[0], h[1], h[2], h[3]);
     }
     if constexpr (INT4) {
 #pragma unroll 1

@@ -39,6 +39,14 @@ constexpr int kABytes = kM * kKT * 2;         // 16 KiB per stage
 constexpr uint32_t kLBO = 128;   // bytes between core matrices along K
 constexpr uint32_t kSBO = 1024;  // bytes between 8-row groups (kKT/8 * 128)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+// Raw-code prefetch ring (cp.async, per producer thread = per weight row):
+// K tiles of packed codes in flight ahead of the fp16 A stages.
+template <bool INT4>
+struct RawRing {
+  static constexpr int DEPTH = INT4 ? 4 : 2;        // K tiles in flight
+  static constexpr int ROWB = INT4 ? kKT / 2 : kKT;  // packed bytes per row per K tile
+  static constexpr int BYTES = DEPTH * kM * ROWB;
+};
 
 struct TcParams {
   GemvParams g;
@@ -181,7 +189,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   const int bBytes = tp.Np * kKT * 2;
   uint8_t *a_st = base;                              // kStages * kABytes
   uint8_t *b_st = a_st + kStages * kABytes;          // kStages * bBytes
-  uint64_t *bars = reinterpret_cast<uint64_t *>(b_st + kStages * bBytes);
+  uint8_t *raw = b_st + kStages * bBytes;            // RawRing<INT4>::BYTES
+  uint64_t *bars = reinterpret_cast<uint64_t *>(raw + RawRing<INT4>::BYTES);
   uint64_t *full = bars, *empty = bars + kStages, *done = bars + 2 * kStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
@@ -224,14 +233,38 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   const uint32_t tmem = *tmem_slot;
   const uint32_t d_out = tmem, d_bg = tmem + (uint32_t)tp.Np;
 
-  // inputs may come from the previous kernel on the stream
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
   if (warp < 4) {
     // ------------------------------------------------------ producers ----
     const int r = tid;  // weight row of this thread inside the tile
     const int64_t grow = row0 + r;
     const bool live = grow < nrows;
+    // Background (INT4) or all (INT8) K tiles stream their packed codes
+    // through a per-thread cp.async ring DEPTH tiles ahead; each thread reads
+    // back only its own row's bytes, so cp.async.wait_group orders it.
+    constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
+    const int bgb = kt_begin > tp.ko ? kt_begin : tp.ko;  // first code tile
+    const int nbg = kt_end > bgb ? kt_end - bgb : 0;
+    const uint8_t *crow = p.codes[m] + (live ? grow : 0) * p.ld_codes[m];
+    const uint32_t raw_me = smem_u32(raw) + (uint32_t)r * RB;
+    auto raw_issue = [&](int i) {  // i-th code tile of this CTA
+      if (i < nbg) {
+        const int kt = bgb + i;
+        const int64_t b0 = INT4 ? (int64_t)(kt - tp.ko) * (kKT / 2) : (int64_t)kt * kKT;
+        const uint32_t dst = raw_me + (uint32_t)(i % DR) * (kM * RB);
+#pragma unroll
+        for (int h = 0; h < RB / 16; ++h) {
+          const bool ok = live && b0 + 16 * h < p.ld_codes[m];
+          const uint8_t *src = ok ? crow + b0 + 16 * h : p.codes[m];
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + 16 * h),
+                       "l"(src), "r"(ok ? 16 : 0)
+                       : "memory");
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    for (int i = 0; i < DR - 1; ++i) raw_issue(i);
+    // inputs (and the gathered B tiles) may come from earlier kernels
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int kt = kt_begin; kt < kt_end; ++kt) {
       const int q = kt - kt_begin;  // position in this CTA's ring sequence
       const int s = q % kStages;
@@ -263,14 +296,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
           *reinterpret_cast<uint4 *>(A + core_off(r, kg * 8)) = v;
         }
       } else if (INT4) {
-        const int e0 = (kt - tp.ko) * kKT;  // first background element of the tile
-        const uint8_t *src = p.codes[m] + grow * p.ld_codes[m] + e0 / 2;
+        const int i = kt - bgb;
+        raw_issue(i + DR - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(DR - 1) : "memory");
+        const uint32_t rsrc = raw_me + (uint32_t)(i % DR) * (kM * RB);
         uint4 q[2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          q[h] = make_uint4(0, 0, 0, 0);
-          if (live && e0 / 2 + 16 * h < p.ld_codes[m]) q[h] = __ldg(reinterpret_cast<const uint4 *>(src) + h);
-        }
+        for (int h = 0; h < 2; ++h)
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(q[h].x), "=r"(q[h].y), "=r"(q[h].z), "=r"(q[h].w)
+                       : "r"(rsrc + 16 * h));
         const uint32_t words[8] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w};
         const uint32_t bias = 0x64086408u;   // 1032 in both halves after the XOR
         const uint32_t k1032 = 0x64086408u;
@@ -292,12 +327,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
           *reinterpret_cast<uint4 *>(A + core_off(r, kg * 8)) = make_uint4(h0, h1, h2, h3);
         }
       } else {
-        const int e0 = kt * kKT;
-        const uint8_t *src = p.codes[m] + grow * p.ld_codes[m] + e0;
+        const int i = kt - bgb;
+        raw_issue(i + DR - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(DR - 1) : "memory");
+        const uint32_t rsrc = raw_me + (uint32_t)(i % DR) * (kM * RB);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (live && e0 + 16 * h < p.ld_codes[m]) v = __ldg(reinterpret_cast<const uint4 *>(src) + h);
+          uint4 v;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(rsrc + 16 * h));
           const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
                                  v.w ^ 0x80808080u};
           uint32_t o[8];
@@ -354,6 +393,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       mbar_arrive(smem_u32(&full[s]));
     }
   } else if (lane == 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // ------------------------------------------------------ MMA issuer ---
     const uint32_t idesc = idesc_f16(kM, tp.Np);
     for (int kt = kt_begin; kt < kt_end; ++kt) {
@@ -481,8 +521,9 @@ size_t tc_workspace_bytes(bool int4, int64_t B, int64_t K, int64_t n_out) {
   return (size_t)(tiles * Np * kKT * 2);
 }
 
-size_t tc_smem_bytes(int Np) {
-  return 1024 + (size_t)kStages * (kABytes + Np * kKT * 2) + (2 * kStages + 1) * 8 + 16;
+size_t tc_smem_bytes(bool int4, int Np) {
+  return 1024 + (size_t)kStages * (kABytes + Np * kKT * 2) +
+         (int4 ? RawRing<true>::BYTES : RawRing<false>::BYTES) + (2 * kStages + 1) * 8 + 16;
 }
 
 qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_rows,
@@ -510,11 +551,12 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
     tiles += tp.n_tiles[m];
     tp.tile_end[m] = tiles;
   }
-  const size_t smem = tc_smem_bytes(tp.Np);
+  const size_t smem = tc_smem_bytes(int4, tp.Np);
   if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
   // Split K over a cluster of S CTAs per tile so that small matrices still
-  // fill the GPU: pick S in {1,2,4,8} minimising waves/S (the time of a
-  // wave shrinks with S), keeping at least two K tiles per CTA.
+  // fill the GPU.  A CTA costs a fixed start/epilogue of about 8 K tiles plus
+  // its share of the K tiles; pick S in {1,2,4,8} minimising
+  // waves * (8 + tiles_of_K / S), keeping at least two K tiles per CTA.
   {
     const int per_sm_smem = (int)(233472 / (smem + 1024));
     const int per_sm_tmem = 512 / (tp.Np <= 16 ? 32 : (tp.Np <= 32 ? 64 : 128));
@@ -525,7 +567,7 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
     for (int S = 1; S <= 8; S *= 2) {
       if (S > 1 && kt_total < 2 * S) break;
       const long ctas = (long)tiles * S;
-      const double t = (double)((ctas + slots - 1) / slots) / S;
+      const double t = (double)((ctas + slots - 1) / slots) * (8.0 + (double)kt_total / S);
       if (t < best - 1e-9) {
         best = t;
         tp.S = S;

@@ -56,7 +56,7 @@ qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s);
 
 // Tensor-core (tcgen05) GEMM for any batch 1..64; rows of each matrix are
 // p.row_end differences.
-size_t tc_smem_bytes(int Np);
+size_t tc_smem_bytes(bool int4, int Np);
 size_t tc_workspace_bytes(bool int4, int64_t B, int64_t K, int64_t n_out);
 qz_status launch_tc(bool int4, int B, const GemvParams &p, const int64_t *mat_rows,
                     void *workspace, size_t workspace_bytes, cudaStream_t s);
