@@ -287,52 +287,6 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
                    : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // let the next kernel on the stream get scheduled as SMs free up
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  // ---- stage x (gathered through perm for INT4) in shared memory, fp16 ----
-  // Eight consecutive inputs per step and thread: eight perm entries, eight
-  // independent gathers, one 16-byte shared store (8 inputs never straddle a
-  // staged chunk); INT8 inputs are read in order.
-  const int elems = staged * EPC;           // multiple of 8
-  const __half hzero = __ushort_as_half((unsigned short)0);
-  const int step8 = kThreads * 8;
-#pragma unroll 1
-  for (int b = 0; b < B; ++b) {
-    const __half *xb = p.x + b * p.ldx;
-#pragma unroll 1
-    for (int e0 = threadIdx.x * 8; e0 < elems; e0 += step8) {
-      uint32_t h[4];
-      if constexpr (INT4) {
-        int idx[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) idx[k] = e0 + k < p.kb ? __ldg(p.perm + p.n_out + e0 + k) : -1;
-        __half v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = idx[k] >= 0 ? xb[idx[k]] : hzero;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          h[k] = (uint32_t)__half_as_ushort(v[2 * k]) | ((uint32_t)__half_as_ushort(v[2 * k + 1]) << 16);
-      } else {
-        __half v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = e0 + k < p.kb ? xb[e0 + k] : hzero;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          h[k] = (uint32_t)__half_as_ushort(v[2 * k]) | ((uint32_t)__half_as_ushort(v[2 * k + 1]) << 16);
-      }
-      *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(xs) + b * bstride + (e0 / EPC) * CS +
-                                 (e0 % EPC) * 2) = make_uint4(h[0], h[1], h[2], h[3]);
-    }
-    if constexpr (INT4) {
-#pragma unroll 1
-      for (int e = threadIdx.x; e < p.ocpr * 8; e += kThreads)
-        xo[b * ostride / 2 + e] = e < p.n_out ? xb[__ldg(p.perm + e)] : hzero;
-    }
-  }
-  __syncthreads();
-
   // ---- each warp: row groups of R rows, streamed through its ring -----------
   Bounds bd;
 #pragma unroll
@@ -341,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
   const int rlo = (int)r0, rhi = (int)r1;
   const int first = rlo + warp * R;
   constexpr int stride = kWarps * R;
-  if (first >= rhi) return;  // no barrier follows
-  const int P = (rhi - first + stride - 1) / stride;  // row groups of this warp
+  const bool has_rows = first < rhi;  // warps without rows still join the barrier
+  const int P = has_rows ? (rhi - first + stride - 1) / stride : 0;  // row groups of this warp
   const int SPR = (Jw + kRPS - 1) / kRPS;             // stages per row group
   const int items = P * SPR;
   const uint32_t lane_off = (uint32_t)lane * CS;
@@ -395,8 +349,57 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
     }
   };
 
+  // The first stages are issued before the wait: weights are static, so
+  // under programmatic overlap they stream in during the previous kernel.
   if (items > 0) prow_setup(0);
   for (int it = 0; it < NS - 1 && pleft > 0; ++it) issue_next();
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // let the next kernel on the stream get scheduled as SMs free up
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // ---- stage x (gathered through perm for INT4) in shared memory, fp16 ----
+  // Eight consecutive inputs per step and thread: eight perm entries, eight
+  // independent gathers, one 16-byte shared store (8 inputs never straddle a
+  // staged chunk); INT8 inputs are read in order.
+  const int elems = staged * EPC;           // multiple of 8
+  const __half hzero = __ushort_as_half((unsigned short)0);
+  const int step8 = kThreads * 8;
+#pragma unroll 1
+  for (int b = 0; b < B; ++b) {
+    const __half *xb = p.x + b * p.ldx;
+#pragma unroll 1
+    for (int e0 = threadIdx.x * 8; e0 < elems; e0 += step8) {
+      uint32_t h[4];
+      if constexpr (INT4) {
+        int idx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) idx[k] = e0 + k < p.kb ? __ldg(p.perm + p.n_out + e0 + k) : -1;
+        __half v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = idx[k] >= 0 ? xb[idx[k]] : hzero;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          h[k] = (uint32_t)__half_as_ushort(v[2 * k]) | ((uint32_t)__half_as_ushort(v[2 * k + 1]) << 16);
+      } else {
+        __half v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = e0 + k < p.kb ? xb[e0 + k] : hzero;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          h[k] = (uint32_t)__half_as_ushort(v[2 * k]) | ((uint32_t)__half_as_ushort(v[2 * k + 1]) << 16);
+      }
+      *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(xs) + b * bstride + (e0 / EPC) * CS +
+                                 (e0 % EPC) * 2) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    if constexpr (INT4) {
+#pragma unroll 1
+      for (int e = threadIdx.x; e < p.ocpr * 8; e += kThreads)
+        xo[b * ostride / 2 + e] = e < p.n_out ? xb[__ldg(p.perm + e)] : hzero;
+    }
+  }
+  __syncthreads();
+  if (!has_rows) return;  // no barrier follows
 
   Acc4 acc[R][B];
 #pragma unroll
@@ -414,13 +417,17 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
     float srow[R];
     bool live[R];
 #pragma unroll
+    uint4 ov[R];  // first outlier chunk of each row, loaded now, used at the end
+#pragma unroll
     for (int rr = 0; rr < R; ++rr) {
       live[rr] = rb + rr < rhi;
       locate(bd, live[rr] ? rb + rr : rhi - 1, mrow[rr], irow[rr]);
       srow[rr] = INT4 ? __ldg(p.scale[mrow[rr]] + irow[rr]) : __ldg(p.scale[mrow[rr]]);
-      if (INT4 && p.ocpr && lane == 8 + rr)
-        prefetch_l2(p.w_out[mrow[rr]] + (int64_t)irow[rr] * p.ld_out[mrow[rr]],
-                    (uint32_t)p.ocpr * 16u);
+      ov[rr] = make_uint4(0, 0, 0, 0);
+      if (INT4 && lane < p.ocpr)
+        ov[rr] = ld_stream(reinterpret_cast<const uint4 *>(
+                               p.w_out[mrow[rr]] + (int64_t)irow[rr] * p.ld_out[mrow[rr]]) +
+                           lane);
     }
     for (int sj = 0; sj < SPR; ++sj) {
       if (ok && pleft > 0) {
@@ -471,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
                                                             (int64_t)irow[rr] * p.ld_out[mrow[rr]]);
 #pragma unroll 1
         for (int c = lane; c < p.ocpr; c += 32) {
-          const uint4 v = ld_stream(orow + c);
+          const uint4 v = c == lane ? ov[rr] : ld_stream(orow + c);
 #pragma unroll
           for (int b = 0; b < B; ++b) {
             const uint4 xv = *reinterpret_cast<const uint4 *>(
