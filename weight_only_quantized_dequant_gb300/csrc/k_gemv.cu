@@ -411,12 +411,11 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
   int cst = 0;            // consumer ring slot
   uint32_t cphase = 0;    // parity of the slot's current use
   for (int g = 0; g < P; ++g) {
-    // rows of this group: scales, matrix, and the outlier rows into L2
+    // rows of this group: matrix, row, scale, first outlier chunk
     const int rb = first + g * stride;
     int mrow[R], irow[R];
     float srow[R];
     bool live[R];
-#pragma unroll
     uint4 ov[R];  // first outlier chunk of each row, loaded now, used at the end
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
