@@ -71,6 +71,25 @@ def int8_dequant(q: np.ndarray, scale) -> np.ndarray:
     return np.asarray(q, np.float64) * np.float64(np.float32(scale))
 
 
+def int8_embed(q: np.ndarray, scale, tokens) -> np.ndarray:
+    """Rows of an INT8 vocabulary table, reconstructed to fp16.
+
+    "On-The-Fly Weight Synthesizer (OTF-LLM Engine)", key innovation 4 keeps
+    the vocabulary lookup table (embed_tokens) in INT8; the reconstruction is
+    the ELG Stream Layer one ("FP16 On-The-Fly GPU Reconstruction"): q * scale
+    as fp16.  Readings: the table is quantized like any other matrix (one fp32
+    scale per tensor, int8_quantize); a looked-up row is the exact product
+    q * scale (int8_dequant) rounded once to the nearest fp16, ties to even.
+    Here the row leaves the method as an fp16 activation, so the one rounding
+    is the output's own.  tokens: int array of row indices, each in [0, V).
+    """
+    q = np.asarray(q)
+    tokens = np.asarray(tokens, np.int64).reshape(-1)
+    assert q.ndim == 2 and np.all((tokens >= 0) & (tokens < q.shape[0]))
+    exact = int8_dequant(q[tokens], scale)          # exact in fp64 (7 x 24 bits)
+    return exact.astype(np.float16)                 # one round to nearest even
+
+
 # --------------------------------------------------------------------------
 # Outlier-aware INT4 (OTF-LLM, "Architecture & Key Innovations")
 # --------------------------------------------------------------------------

@@ -100,6 +100,79 @@ def test_int8_product_brute_force_exact():
             assert abs(Fraction(a[b, i]) - mag) <= mag * Fraction(1, 2 ** 50)
 
 
+# ------------------------------------------------------ INT8 embedding ----
+_F16_POS = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16)   # every finite value >= 0
+_F16_POS64 = _F16_POS.astype(np.float64)                             # exact
+
+
+def _nearest_fp16(v: Fraction) -> np.float16:
+    """Round an exact rational to fp16 by brute force: the two finite fp16
+    neighbours of |v| are compared with exact arithmetic; ties go to the
+    neighbour with the even bit pattern."""
+    a = abs(v)
+    k = int(np.searchsorted(_F16_POS64, float(a), side="left"))
+    cands = [c for c in (k - 1, k, k + 1) if 0 <= c < _F16_POS.size]
+    best = min(cands, key=lambda c: (abs(Fraction(float(_F16_POS64[c])) - a), c & 1))
+    h = _F16_POS[best]
+    return np.float16(-h) if v < 0 else h
+
+
+def test_embed_hand_ties_to_even():
+    # scale 1 + 2^-11 is an fp16 midpoint between 1 and 1 + 2^-10 -> 1 (even);
+    # 1 + 3*2^-11 lies between 1 + 2^-10 and 1 + 2^-9 -> 1 + 2^-9 (even).
+    q = np.array([[1, -1, 0], [2, 127, -127]], np.int8)
+    out = O.int8_embed(q, np.float32(1 + 2 ** -11), [0])
+    assert out.tolist() == [[1.0, -1.0, 0.0]]
+    out = O.int8_embed(q, np.float32(1 + 3 * 2 ** -11), [0, 0])
+    assert out.tolist() == [[1 + 2 ** -9, -(1 + 2 ** -9), 0.0]] * 2
+    # 2 * (1 + 2^-11) = 2 + 2^-10, midpoint between 2 and 2 + 2^-9 -> 2
+    out = O.int8_embed(q, np.float32(1 + 2 ** -11), [1])
+    assert out[0, 0] == 2.0
+    assert out.dtype == np.float16
+
+
+def test_embed_single_rounding_not_via_fp32():
+    """A product that an fp32 multiply would round onto an fp16 midpoint must
+    still round to the fp16 neighbour the exact value is nearer to."""
+    found = 0
+    for qv in range(3, 128, 2):
+        for mid in (1 + 2 ** -11, 1 + 3 * 2 ** -11, 1.5 + 2 ** -11):
+            s = np.float32(mid / qv)
+            for _ in range(4):
+                exact = qv * Fraction(float(s))
+                naive = np.float32(np.float32(qv) * s)
+                if float(naive) == mid and exact != Fraction(mid):
+                    want = _nearest_fp16(exact)
+                    got = O.int8_embed(np.array([[qv]], np.int8), s, [0])[0, 0]
+                    assert got == want and got.view(np.uint16) == want.view(np.uint16)
+                    found += np.float16(naive) != want   # the fp32 path would be wrong
+                s = np.nextafter(s, np.float32(1))
+    assert found >= 3
+
+
+def test_embed_brute_force_nearest_and_special_cases():
+    rng = np.random.default_rng(11)
+    W = f16(rng.standard_t(4, size=(40, 24)) * 0.02)
+    q, s = O.int8_quantize(W)
+    tokens = [5, 0, 39, 5]
+    out = O.int8_embed(q, s, tokens)
+    assert out.shape == (4, 24) and out.dtype == np.float16
+    S = Fraction(float(s))
+    for b, t in enumerate(tokens):
+        for j in range(24):
+            want = _nearest_fp16(int(q[t, j]) * S)
+            assert out[b, j].view(np.uint16) == want.view(np.uint16) or (want == 0 and out[b, j] == 0)
+    assert (out[0] == out[3]).all()
+    # the fp16 rows are within half an fp16 ulp of the reconstruction q * s
+    exact = O.int8_dequant(q[tokens], s)
+    assert (np.abs(out.astype(np.float64) - exact) <= O.fp16_ulp(exact) / 2).all()
+    # zero table: scale 0, rows 0
+    qz, sz = O.int8_quantize(np.zeros((3, 8), np.float16))
+    assert (O.int8_embed(qz, sz, [2, 1]) == 0).all()
+    with pytest.raises(AssertionError):
+        O.int8_embed(q, s, [40])
+
+
 # ------------------------------------------------------------- INT4 parts --
 def test_saliency_hand():
     # column sums of |W| over rows, in units of 2^-24; includes the smallest
