@@ -5,7 +5,7 @@ layer), replayed from a CUDA graph.  The stack (several GB) is far larger
 than the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--extra] [--no-cpu]
+                  [--impl ours|reference] [--extra] [--head] [--paged] [--no-cpu]
 
 Prints ONE JSON line.  Under torchrun (N > 1) every rank runs an independent
 replica (the method targets one GPU; no collectives) and rank 0 prints.
@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--paged", action="store_true",
                     help="also stream the 70B and Gemma stacks through the pager")
+    ap.add_argument("--head", action="store_true",
+                    help="also time the 3B vocabulary lookup + lm_head (tied INT8, untied INT4)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch without programmatic dependent launch")
     ap.add_argument("--batch", type=int, default=1,
@@ -452,6 +454,72 @@ def measure_paged(wl_name: str, steps: int, warmup: int, device, distinct: int =
     return out
 
 
+def measure_head(name: str, steps: int, warmup: int, device):
+    """The steps either side of the stack: INT8 vocabulary lookup of one
+    token plus the output projection over the whole vocabulary, tied (the
+    INT8 table) or untied (outlier-aware INT4).  Each variant is one captured
+    graph (lookup + lm_head GEMV) replayed `steps` times."""
+    import torch
+
+    from weight_only_quantized_dequant_gb300 import api
+    from weight_only_quantized_dequant_gb300 import synthetic as S
+
+    hd = S.HEADS[name]
+    V, H = hd.vocab, hd.hidden
+    W = S.weight(V, H, hd.seed_base, device=device)
+    table = api.quantize_int8(W)
+    del W
+    n_out = api.default_n_out(H)
+    W2 = S.weight(V, H, hd.seed_base + 1, device=device)
+    colsum = torch.zeros((H,), dtype=torch.int64, device=device)
+    api.saliency_accumulate(W2, colsum)
+    perm = api.select_outliers(colsum, S.x_profile(H, n_out, hd.seed_base + 2, device=device), n_out)
+    w4 = api.quantize_int4_outlier(W2, perm, n_out)
+    del W2
+    tok = S.tokens(1, V, hd.seed_base + 4, device=device)
+    h = S.activation(1, H, hd.seed_base + 3, device=device)[0]
+    emb = torch.empty((1, H), dtype=torch.float16, device=device)
+    logits = torch.empty((V,), dtype=torch.float16, device=device)
+    torch.cuda.synchronize(device)
+    s = torch.cuda.Stream(device=device)
+    io = 4 + 2 * H + 2 * H + 2 * V       # token, looked-up row, hidden state, logits
+    variants = {"tied_int8": (lambda st: api.gemv_int8(table, h, logits, stream=st),
+                              H + 4 + table.nbytes() + io),
+                "untied_int4o": (lambda st: api.gemv_int4_outlier(w4, h, logits, stream=st),
+                                 H + 4 + w4.nbytes() + 4 * H + io)}
+    out = {"vocab": V, "hidden": H}
+    for key, (head, nbytes) in variants.items():
+        def step(st):
+            api.embed_int8(table, tok, emb, stream=st)
+            head(st)
+        s.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(s):
+            step(s)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step(s)
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                g.replay()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(steps):
+                g.replay()
+            e1.record(s)
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / steps
+        out[key] = {"us_per_token": round(ms * 1e3, 3), "bytes": nbytes,
+                    "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        del g
+    assert api.device_error() == 0
+    del table, w4
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     a = parse()
     if a.impl == "reference":
@@ -496,6 +564,10 @@ def main():
             extra[f"{name}_b{b}"] = {k: e[k] for k in ("us_per_layer", "gbs", "ms_per_step",
                                                           "stack_gb")}
             extra[f"{name}_b{b}"]["dominant_gbs"] = e["dominant"]["gbs"]
+
+    if a.head and rank == 0:
+        extra["llama32_3b_head"] = measure_head("llama32_3b_head", max(10, a.steps), a.warmup,
+                                                device)
 
     if a.paged and rank == 0:
         for name in ("llama_70b_int4o", "gemma2_9b_int8"):

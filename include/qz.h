@@ -76,8 +76,10 @@ qz_status qz_set_overlap(int enable);
 /* The current host thread's overlap setting (0 or 1). */
 int qz_get_overlap(void);
 
-/* The library's device error word: 0, or 1 if a kernel gave up a bounded
- * wait (its output is then incomplete).  Synchronous (reads device memory);
+/* The library's device error word, a bit set: 1 if a kernel gave up a
+ * bounded wait (its output is then incomplete); 2 if qz_embed_int8 met a
+ * token outside its table (that row was written as zeros).  0 if neither
+ * happened since the last clear.  Synchronous (reads device memory);
  * clear = 1 resets it.  Not for use during stream capture. */
 qz_status qz_device_error(int *code, int clear);
 
@@ -144,6 +146,24 @@ size_t qz_gemm_workspace_bytes(int64_t B, int64_t K, int64_t n_out);
 qz_status qz_gemv_int8_grouped(const qz_int8_weight *ws, int n,
                                const qz_half *x, qz_half *const *ys,
                                qz_stream s);
+
+/* Rows of an INT8 vocabulary table (embed_tokens) as fp16 activations
+ * [OTF "Architecture & Key Innovations", key innovation 4: vocabulary
+ * lookup tables compressed to INT8; ELG "FP16 On-The-Fly GPU
+ * Reconstruction": q * scale as fp16]:
+ *   out[b][j] = fp16(q[tokens[b]][j] * scale), b < B, j < K,
+ * the exact product rounded once to the nearest fp16, ties to even.
+ * table: the quantized [V][K] table (V = table->N), as qz_quantize_int8
+ * makes it (one scale per tensor); any K.  tokens: device int32 [B], 4-byte
+ * aligned.  out: device fp16 [B][ldo], 16-byte aligned, ldo >= K, ldo a
+ * multiple of 8.  B >= 0 (B = 0 enqueues nothing).  A token outside [0, V)
+ * is not read: its row of out is written as zeros and bit 2 of the device
+ * error word (qz_device_error) is set.
+ * With tied word embeddings the same table is the output projection
+ * (lm_head): qz_gemv_int8(table, h, logits) gives
+ * logits[v] = scale * sum_j q[v][j] h[j]. */
+qz_status qz_embed_int8(const qz_int8_weight *table, const int32_t *tokens,
+                        int64_t B, qz_half *out, int64_t ldo, qz_stream s);
 
 /* ======================================================================
  * Outlier-aware INT4  [OTF "Architecture & Key Innovations": diagram and

@@ -131,6 +131,22 @@ def test_gemv_int8_validation(lib):
     assert lib.qz_gemm_int8(ctypes.byref(w), 2, P, 32, P + 1, 8, None, 0, None) == ALIGN
 
 
+def test_embed_int8_validation(lib):
+    w = _w8()                                     # V = 8 rows of K = 32
+    E = lib.qz_embed_int8
+    assert E(None, P, 1, P, 32, None) == INVAL
+    assert E(ctypes.byref(w), P, -1, P, 32, None) == INVAL
+    assert E(ctypes.byref(w), None, 0, None, 0, None) == OK       # B = 0: nothing to do
+    assert E(ctypes.byref(w), None, 1, P, 32, None) == INVAL
+    assert E(ctypes.byref(w), P + 2, 1, P, 32, None) == ALIGN     # tokens need 4-byte alignment
+    assert E(ctypes.byref(w), P, 2, P + 2, 32, None) == ALIGN     # out rows start on 16 bytes
+    assert E(ctypes.byref(w), P, 2, P, 36, None) == ALIGN         # ldo a multiple of 8
+    assert E(ctypes.byref(w), P, 2, P, 16, None) == INVAL         # ldo < K
+    assert E(ctypes.byref(_w8(ldq=40)), P, 1, P, 32, None) == ALIGN
+    bad = _lib.Int8Weight(P, None, 4, 32, 32)
+    assert E(ctypes.byref(bad), P, 1, P, 32, None) == INVAL        # no scale
+
+
 def test_grouped_int8_validation(lib):
     ws = (_lib.Int8Weight * 5)(*[_w8() for _ in range(5)])
     ys = (ctypes.c_void_p * 5)(*[P] * 5)

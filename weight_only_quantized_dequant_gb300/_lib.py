@@ -56,6 +56,7 @@ _SIGS = {
     "qz_gemm_workspace_bytes": (c_size_t, [c_int64, c_int64, c_int64]),
     "qz_gemv_int8_grouped": (_S, [POINTER(Int8Weight), c_int, c_void_p, POINTER(c_void_p),
                                   c_void_p]),
+    "qz_embed_int8": (_S, [POINTER(Int8Weight), c_void_p, c_int64, c_void_p, c_int64, c_void_p]),
     "qz_int4o_layout": (_S, [c_int64, c_int64, c_int64, POINTER(c_int64), POINTER(c_int64)]),
     "qz_saliency_accumulate": (_S, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     "qz_select_outliers": (_S, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),

@@ -155,6 +155,22 @@ def gemv_int8_grouped(ws, x: torch.Tensor, ys=None, stream=None):
     return ys
 
 
+def embed_int8(table: Int8Matrix, tokens: torch.Tensor, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """out [B, K] fp16 = rows tokens[b] of the INT8 table, each q * scale
+    rounded once to fp16.  tokens: int32 device tensor [B].  A token outside
+    [0, V) gives a zero row and sets bit 2 of device_error()."""
+    _need_cuda(tokens)
+    assert tokens.dtype == torch.int32 and tokens.dim() == 1 and tokens.is_contiguous()
+    B = tokens.shape[0]
+    if out is None:
+        buf = torch.empty((B, _round_up(table.K, 8)), dtype=torch.float16, device=tokens.device)
+        out = buf[:, :table.K]
+    _lib.call("qz_embed_int8", ctypes.byref(table.struct()), tokens.data_ptr(), B,
+              out.data_ptr(), out.stride(0) if B > 0 else _round_up(table.K, 8), _stream(stream))
+    return out
+
+
 # ------------------------------------------------------------------ INT4 ---
 def int4o_layout(N: int, K: int, n_out: int) -> tuple[int, int]:
     """(ld_out halves, ld_q4 bytes) of the packed INT4-outlier format."""

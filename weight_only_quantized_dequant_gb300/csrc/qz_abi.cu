@@ -206,10 +206,11 @@ int qz_get_overlap(void) { return g_overlap; }
 
 qz_status qz_device_error(int *code, int clear) {
   if (!code || (clear != 0 && clear != 1)) return QZ_ERR_INVALID_ARG;
-  int a = 0, b = 0;
+  int a = 0, b = 0, c = 0;
   QZ_TRY(read_device_error(&a, clear));
   QZ_TRY(read_gemv_error(&b, clear));
-  *code = a | b;
+  QZ_TRY(read_embed_error(&c, clear));
+  *code = a | b | c;
   return QZ_OK;
 }
 
@@ -241,6 +242,19 @@ qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X, int
   qz_half *ys[1] = {Y};
   return gemm_common(false, p, B, X, ldx, ys, ldy, 1, workspace, workspace_bytes,
                      (cudaStream_t)s);
+}
+
+qz_status qz_embed_int8(const qz_int8_weight *table, const int32_t *tokens, int64_t B,
+                        qz_half *out, int64_t ldo, qz_stream s) {
+  if (!table || B < 0) return QZ_ERR_INVALID_ARG;
+  QZ_TRY(check_mat(table->q, table->N, table->K, table->ldq, 1));
+  if (!table->scale) return QZ_ERR_INVALID_ARG;
+  if (B == 0) return QZ_OK;
+  if (!tokens) return QZ_ERR_INVALID_ARG;
+  if (((uintptr_t)tokens & 3u) != 0) return QZ_ERR_ALIGNMENT;
+  QZ_TRY(check_mat(out, B, table->K, ldo, 2));
+  return launch_embed_int8(table->q, table->ldq, table->scale, table->N, table->K, tokens, B,
+                           reinterpret_cast<__half *>(out), ldo, (cudaStream_t)s);
 }
 
 qz_status qz_gemv_int8_grouped(const qz_int8_weight *ws, int n, const qz_half *x,

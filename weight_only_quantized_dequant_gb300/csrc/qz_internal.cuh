@@ -62,6 +62,12 @@ qz_status launch_tc(bool int4, int B, const GemvParams &p, const int64_t *mat_ro
                     void *workspace, size_t workspace_bytes, cudaStream_t s);
 qz_status read_device_error(int *code, int clear);
 qz_status read_gemv_error(int *code, int clear);
+qz_status read_embed_error(int *code, int clear);
+
+// INT8 vocabulary-table lookup (rows of q reconstructed to fp16).
+qz_status launch_embed_int8(const int8_t *q, int64_t ldq, const float *scale, int64_t V, int64_t K,
+                            const int32_t *tokens, int64_t B, __half *out, int64_t ldo,
+                            cudaStream_t s);
 
 // ------------------------------------------------------------ quantizers ---
 qz_status launch_quantize_int8(const __half *W, int64_t N, int64_t K,

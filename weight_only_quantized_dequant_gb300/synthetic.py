@@ -14,10 +14,16 @@ tensor is synthetic with the shapes of the model families the pages name):
   (OTF-LLM validates on Llama-3.2-3B).
 * ``llama_7b_int4o`` - 7B Llama-style shapes, 32 layers, batch 1/4/16/64.
 * ``llama_70b_int4o`` - 70B shapes, 80 layers (NTransformer runs Llama 3.1 70B).
+* ``llama32_3b_head`` - the steps either side of the 3B stack: an INT8
+  vocabulary table of 128256 x 3072 (embed_tokens) and the output projection
+  (lm_head) of the same shape, tied (the INT8 table itself) or untied
+  (outlier-aware INT4); OTF-LLM key innovation 4.
 
 Weights are 0.02 * StudentT(4) in fp16, drawn as z0 / sqrt((z1^2+..+z4^2)/4)
 from five standard normals; activations x ~ N(0, 1) fp16; the activation
 profile is |N(0, 1)| with a seeded random 1% of channels multiplied by 20.
+Head seeds: table = base, untied lm_head = base + 1, its profile base + 2,
+hidden states base + 3, token ids base + 4 (uniform over the vocabulary).
 Seeds: matrix m of layer l uses base + 16*l + m (m = 0..6 for q,k,v,o,gate,
 up,down); the input of group g uses base + 16*l + 8 + g; the profile of
 permutation table p uses base + 16*l + 12 + p.
@@ -68,6 +74,24 @@ WORKLOADS = {
                                batches=(1, 4, 16, 64)),
     "llama_70b_int4o": Workload("llama_70b_int4o", "int4o", 8192, 8192, 1024, 28672, 80, 70000),
 }
+
+
+@dataclass(frozen=True)
+class Head:
+    """Vocabulary table and output projection of one model family."""
+    name: str
+    vocab: int
+    hidden: int
+    seed_base: int
+
+
+HEADS = {"llama32_3b_head": Head("llama32_3b_head", 128256, 3072, 3900)}
+
+
+def tokens(B: int, V: int, seed: int, device="cpu") -> torch.Tensor:
+    """int32 [B] token ids, uniform over [0, V)."""
+    g = _gen(seed, device)
+    return torch.randint(0, V, (B,), generator=g, device=device, dtype=torch.int64).to(torch.int32)
 
 
 def matrix_seed(wl: Workload, layer: int, m: str) -> int:
