@@ -147,6 +147,17 @@ qz_status qz_gemv_int8_grouped(const qz_int8_weight *ws, int n,
                                const qz_half *x, qz_half *const *ys,
                                qz_stream s);
 
+/* The batched form of qz_gemv_int8_grouped: n matrices (1 <= n <=
+ * QZ_MAX_GROUP) of equal K read the same inputs X [B][ldx] in one call, and
+ * Ys[m] [B][ldys[m]] receives matrix m's outputs.  Ys and ldys are host
+ * arrays of n entries.  Batch limits, the CUDA-core/tensor-core choice and
+ * the workspace are those of qz_gemm_int8 (one workspace serves the whole
+ * group: qz_gemm_workspace_bytes(B, K, 0)). */
+qz_status qz_gemm_int8_grouped(const qz_int8_weight *ws, int n, int64_t B,
+                               const qz_half *X, int64_t ldx, qz_half *const *Ys,
+                               const int64_t *ldys, void *workspace,
+                               size_t workspace_bytes, qz_stream s);
+
 /* Rows of an INT8 vocabulary table (embed_tokens) as fp16 activations
  * [OTF "Architecture & Key Innovations", key innovation 4: vocabulary
  * lookup tables compressed to INT8; ELG "FP16 On-The-Fly GPU
@@ -268,6 +279,17 @@ qz_status qz_gemm_int4_outlier_noalloc(const qz_int4o_weight *w, int64_t B,
  * n_out), one launch.  ws: host array; ys: host array of device pointers. */
 qz_status qz_gemv_int4_outlier_grouped(const qz_int4o_weight *ws, int n,
                                        const qz_half *x, qz_half *const *ys,
+                                       qz_stream s);
+
+/* The batched form of qz_gemv_int4_outlier_grouped: n matrices sharing K,
+ * n_out and perm read X [B][ldx]; Ys[m] [B][ldys[m]] receives matrix m's
+ * outputs (host arrays of n entries).  Otherwise as qz_gemm_int4_outlier;
+ * one workspace of qz_gemm_workspace_bytes(B, K, n_out) bytes serves the
+ * group. */
+qz_status qz_gemm_int4_outlier_grouped(const qz_int4o_weight *ws, int n, int64_t B,
+                                       const qz_half *X, int64_t ldx,
+                                       qz_half *const *Ys, const int64_t *ldys,
+                                       void *workspace, size_t workspace_bytes,
                                        qz_stream s);
 
 /* ======================================================================

@@ -66,9 +66,10 @@ def test_overlap_setting_is_per_thread_and_validated(lib):
 
 
 def test_workspace_bytes(lib):
-    # ceil(n_out/64) + ceil((K-n_out)/64) tiles of Np x 64 fp16, Np = B rounded to 16
-    assert lib.qz_gemm_workspace_bytes(64, 4096, 41) == (1 + 64) * 64 * 64 * 2
-    assert lib.qz_gemm_workspace_bytes(5, 100, 0) == 2 * 16 * 64 * 2
+    # ceil(n_out/128) + ceil((K-n_out)/128) tiles of Np x 128 fp16, Np = B rounded to 16
+    assert lib.qz_gemm_workspace_bytes(64, 4096, 41) == (1 + 32) * 64 * 128 * 2
+    assert lib.qz_gemm_workspace_bytes(5, 100, 0) == 1 * 16 * 128 * 2
+    assert lib.qz_gemm_workspace_bytes(5, 300, 0) == 3 * 16 * 128 * 2
     assert lib.qz_gemm_workspace_bytes(65, 100, 0) == 0
     assert lib.qz_gemm_workspace_bytes(1, 100, 101) == 0
 
@@ -154,6 +155,24 @@ def test_grouped_int8_validation(lib):
     assert lib.qz_gemv_int8_grouped(ws, 0, P, ys, None) == INVAL
     bad = (_lib.Int8Weight * 2)(_w8(K=32), _w8(K=48, ldq=48))
     assert lib.qz_gemv_int8_grouped(bad, 2, P, ys, None) == INVAL
+
+
+def test_grouped_gemm_validation(lib):
+    ws = (_lib.Int8Weight * 5)(*[_w8() for _ in range(5)])
+    ys = (ctypes.c_void_p * 5)(*[P] * 5)
+    ld = (ctypes.c_int64 * 5)(*[8] * 5)
+    G = lib.qz_gemm_int8_grouped
+    assert G(ws, 5, 3, P, 32, ys, ld, None, 0, None) == UNSUP
+    assert G(ws, 2, 65, P, 32, ys, ld, None, 0, None) == UNSUP
+    assert G(ws, 2, 0, P, 32, ys, ld, None, 0, None) == INVAL
+    assert G(ws, 2, 3, P, 32, ys, None, None, 0, None) == INVAL
+    assert G(ws, 2, 3, P, 16, ys, ld, None, 0, None) == INVAL        # ldx < K
+    bad_ld = (ctypes.c_int64 * 2)(8, 4)                                 # ldy < N
+    assert G(ws, 2, 3, P, 32, ys, bad_ld, None, 0, None) == INVAL
+    bad = (_lib.Int8Weight * 2)(_w8(K=32), _w8(K=48, ldq=48))
+    assert G(bad, 2, 3, P, 48, ys, ld, None, 0, None) == INVAL
+    w4 = (_lib.Int4oWeight * 2)(_w4(), _w4(perm=P + 16))
+    assert lib.qz_gemm_int4_outlier_grouped(w4, 2, 3, P, 64, ys, ld, None, 0, None) == INVAL
 
 
 def _w4(N=8, K=64, n_out=1, perm=P, w_out=P, q4=P, scale=P, ld_out=None, ld_q4=None):

@@ -222,6 +222,45 @@ def test_int4_grouped_matches_separate():
 
 
 @pytest.mark.parametrize("fmt", ["int8", "int4o"])
+@pytest.mark.parametrize("B", [3, 16, 64])
+def test_batched_grouped_matches_oracle(fmt, B):
+    """One grouped batched call over 3 matrices of different heights sharing
+    the input (and, for INT4, the permutation); outputs with padded strides
+    of their own; every output against the oracle."""
+    K, n_out = 1000, 10
+    Ns = [300, 129, 64]
+    Ws = [S.weight(n, K, 9500 + i, device=DEV) for i, n in enumerate(Ns)]
+    X = padded_rows(S.activation(B, K, 9510 + B, device=DEV))
+    Ys = [torch.full((B, n + 8 * (i + 1)), 3.0, dtype=torch.float16, device=DEV)[:, :n]
+          for i, n in enumerate(Ns)]
+    if fmt == "int8":
+        ws = [qz().quantize_int8(W) for W in Ws]
+        qz().gemm_int8_grouped(ws, X, Ys)
+    else:
+        prof = S.x_profile(K, n_out, 9520, device=DEV)
+        colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+        for W in Ws:
+            qz().saliency_accumulate(W, colsum)
+        perm = qz().select_outliers(colsum, prof, n_out)
+        ws = [qz().quantize_int4_outlier(W, perm, n_out) for W in Ws]
+        qz().gemm_int4_outlier_grouped(ws, X, Ys)
+    assert qz().device_error() == 0
+    Xn = X.cpu().numpy()
+    for i, (W, Y) in enumerate(zip(Ws, Ys)):
+        Wn = W.cpu().numpy()
+        if fmt == "int8":
+            q_ref, s_ref = O.int8_quantize(Wn)
+            y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, Xn)
+        else:
+            pn = perm.cpu().numpy()
+            wo, q4, s = O.int4o_quantize(Wn, pn, n_out)
+            y_ref, a_ref = O.int4o_product_ref(wo, q4, s, pn, n_out, K, Xn)
+        assert_close(Y, y_ref, a_ref, f"grouped {fmt} B={B} m={i}")
+        full = Y.as_strided((B, Y.stride(0)), (Y.stride(0), 1)).cpu()
+        assert (full[:, Ns[i]:] == 3.0).all()   # the padding of each row untouched
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4o"])
 @pytest.mark.parametrize("B", [5, 64])
 def test_tensor_core_without_workspace(fmt, B):
     """The tensor-core kernel also works without a workspace (it gathers the

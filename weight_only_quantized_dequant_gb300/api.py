@@ -301,6 +301,29 @@ def gemv_int4_outlier_grouped(ws, x: torch.Tensor, ys=None, stream=None):
     return ys
 
 
+def _grouped_gemm(fn: str, struct_t, ws, X: torch.Tensor, Ys, stream, workspace, n_out: int):
+    _need_cuda(X)
+    n, B = len(ws), X.shape[0]
+    Ys = [_vec_out(X, w.N, B) for w in ws] if Ys is None else Ys
+    arr = (struct_t * n)(*[w.struct() for w in ws])
+    yp = (ctypes.c_void_p * n)(*[y.data_ptr() for y in Ys])
+    ld = (ctypes.c_int64 * n)(*[y.stride(0) for y in Ys])
+    wp, wb = _workspace(X, ws[0].K, n_out, workspace)
+    _lib.call(fn, arr, n, B, X.data_ptr(), X.stride(0), yp, ld, wp, wb, _stream(stream))
+    return Ys
+
+
+def gemm_int8_grouped(ws, X: torch.Tensor, Ys=None, stream=None, workspace=None):
+    """Ys[m] [B, N_m] for X [B, K] and n matrices sharing K, in one call."""
+    return _grouped_gemm("qz_gemm_int8_grouped", Int8Weight, ws, X, Ys, stream, workspace, 0)
+
+
+def gemm_int4_outlier_grouped(ws, X: torch.Tensor, Ys=None, stream=None, workspace=None):
+    """Ys[m] [B, N_m] for X [B, K] and n matrices sharing K, n_out and perm."""
+    return _grouped_gemm("qz_gemm_int4_outlier_grouped", Int4oWeight, ws, X, Ys, stream,
+                         workspace, ws[0].n_out)
+
+
 # ----------------------------------------------------------------- Pager ---
 class Pager:
     """Double-buffered host->device layer streaming (qz_pager_*).

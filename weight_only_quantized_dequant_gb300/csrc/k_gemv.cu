@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
         const float bg = (acc[rr][b][0] + acc[rr][b][2]) + (acc[rr][b][1] + acc[rr][b][3]) * 0.0625f;
         // y = s_i * background + outliers, combined per lane, one reduction
         const float yl = warp_sum(fmaf(srow[rr], bg, outl[rr][b][0] + outl[rr][b][1]));
-        if (lane == 0 && live[rr]) p.y[mrow[rr]][b * p.ldy + irow[rr]] = __float2half_rn(yl);
+        if (lane == 0 && live[rr]) p.y[mrow[rr]][b * p.ldy[mrow[rr]] + irow[rr]] = __float2half_rn(yl);
         acc[rr][b][0] = acc[rr][b][1] = acc[rr][b][2] = acc[rr][b][3] = 0.f;
       }
     }

@@ -18,6 +18,9 @@
 //    per-row scale multiplies the background only: y = D_out + s_i * D_bg.
 //  * A 4-stage mbarrier ring decouples producers and the MMA thread; every
 //    wait is bounded in time and reports a timeout through a device flag.
+#include <cuda.h>
+
+#include <cstring>
 #include <mutex>
 
 #include "qz_internal.cuh"
@@ -31,29 +34,37 @@ __device__ int g_device_error = 0;
 namespace {
 
 constexpr int kM = 128;         // weight rows per tile (MMA M)
-constexpr int kKT = 64;         // K elements per pipeline stage
-constexpr int kStages = 4;
-constexpr int kProducers = 128;  // 4 warps, one weight row each
-constexpr int kThreadsTc = kProducers + 32;  // + the MMA warp
-constexpr int kABytes = kM * kKT * 2;         // 16 KiB per stage
+constexpr int kKT = 128;        // K elements per pipeline stage
+constexpr int kStages = 3;
+constexpr int kProducers = 256;  // 8 warps, two threads per weight row
+constexpr int kMmaWarp = kProducers / 32;     // warp 8 issues the MMAs
+constexpr int kLoadWarp = kMmaWarp + 1;       // warp 9 fills the activation ring
+constexpr int kThreadsTc = kProducers + 64;
+constexpr int kMaxBStages = 8;                // activation ring depth (smem permitting)
+constexpr size_t kBRingBytes = 80 * 1024;     // shared memory given to that ring
+constexpr int kABytes = kM * kKT * 2;         // 32 KiB per stage
 constexpr uint32_t kLBO = 128;   // bytes between core matrices along K
-constexpr uint32_t kSBO = 1024;  // bytes between 8-row groups (kKT/8 * 128)
+constexpr uint32_t kSBO = 2048;  // bytes between 8-row groups (kKT/8 * 128)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
-// Raw-code prefetch ring (cp.async, per producer thread = per weight row):
-// K tiles of packed codes in flight ahead of the fp16 A stages.
+// Raw-code ring: K tiles of packed codes (kM rows x ROWB bytes, one 2D
+// tensor copy each) in flight ahead of the fp16 A stages.
 template <bool INT4>
 struct RawRing {
-  static constexpr int DEPTH = INT4 ? 4 : 2;        // K tiles in flight
+  static constexpr int DEPTH = INT4 ? 6 : 3;        // K tiles in flight
   static constexpr int ROWB = INT4 ? kKT / 2 : kKT;  // packed bytes per row per K tile
+  static constexpr int HB = ROWB / 2;                // bytes of one producer thread
   static constexpr int BYTES = DEPTH * kM * ROWB;
 };
+constexpr int kMaxRaw = 6;
 
 struct TcParams {
+  CUtensorMap codes_map[QZ_MAX_GROUP];  // 2D: [rows][ld_codes bytes], box kM x ROWB
   GemvParams g;
   int B;                // batch rows
   int Np;               // MMA N: B rounded up to 16
   int S;                // CTAs per tile (cluster size): each does 1/S of the K tiles
   const uint8_t *ws;    // gathered activations, one canonical B tile per K tile (or null)
+  int nbs;              // stages of the activation ring
   int ko;               // K tiles of the outlier block
   int kbt;              // K tiles of the background block
   int n_tiles[QZ_MAX_GROUP];
@@ -187,11 +198,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   uint8_t *base = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int bBytes = tp.Np * kKT * 2;
+  const int NB = tp.nbs;
   uint8_t *a_st = base;                              // kStages * kABytes
-  uint8_t *b_st = a_st + kStages * kABytes;          // kStages * bBytes
-  uint8_t *raw = b_st + kStages * bBytes;            // RawRing<INT4>::BYTES
+  uint8_t *b_st = a_st + kStages * kABytes;          // NB * bBytes
+  uint8_t *raw = b_st + NB * bBytes;                 // RawRing<INT4>::BYTES
   uint64_t *bars = reinterpret_cast<uint64_t *>(raw + RawRing<INT4>::BYTES);
-  uint64_t *full = bars, *empty = bars + kStages, *done = bars + 2 * kStages;
+  uint64_t *full = bars, *empty = bars + kStages;
+  uint64_t *bfull = bars + 2 * kStages, *bempty = bfull + kMaxBStages;
+  uint64_t *rfull = bempty + kMaxBStages, *rempty = rfull + kMaxRaw;
+  uint64_t *done = rempty + kMaxRaw;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -213,8 +228,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&full[s]), kProducers + (tp.ws ? 1 : 0));
+      mbar_init(smem_u32(&full[s]), kProducers);
       mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int s = 0; s < kMaxBStages; ++s) {
+      mbar_init(smem_u32(&bfull[s]), 1);
+      mbar_init(smem_u32(&bempty[s]), 1);
+    }
+    for (int s = 0; s < kMaxRaw; ++s) {
+      mbar_init(smem_u32(&rfull[s]), 1);
+      mbar_init(smem_u32(&rempty[s]), kProducers);
     }
     mbar_init(smem_u32(done), 1);
     *abort_flag = 0;
@@ -233,37 +256,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   const uint32_t tmem = *tmem_slot;
   const uint32_t d_out = tmem, d_bg = tmem + (uint32_t)tp.Np;
 
-  if (warp < 4) {
+  if (warp < kProducers / 32) {
     // ------------------------------------------------------ producers ----
-    const int r = tid;  // weight row of this thread inside the tile
+    // Two threads per weight row: thread (r, h) converts k slots
+    // [64 h, 64 h + 64) of row r in every stage.
+    const int r = tid >> 1, h = tid & 1;
     const int64_t grow = row0 + r;
     const bool live = grow < nrows;
-    // Background (INT4) or all (INT8) K tiles stream their packed codes
-    // through a per-thread cp.async ring DEPTH tiles ahead; each thread reads
-    // back only its own row's bytes, so cp.async.wait_group orders it.
-    constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
+    // Background (INT4) or all (INT8) K tiles arrive as packed codes in the
+    // raw ring (filled by the loader warp); each thread converts its bytes.
+    constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB, HB = RawRing<INT4>::HB;
     const int bgb = kt_begin > tp.ko ? kt_begin : tp.ko;  // first code tile
-    const int nbg = kt_end > bgb ? kt_end - bgb : 0;
-    const uint8_t *crow = p.codes[m] + (live ? grow : 0) * p.ld_codes[m];
-    const uint32_t raw_me = smem_u32(raw) + (uint32_t)r * RB;
-    auto raw_issue = [&](int i) {  // i-th code tile of this CTA
-      if (i < nbg) {
-        const int kt = bgb + i;
-        const int64_t b0 = INT4 ? (int64_t)(kt - tp.ko) * (kKT / 2) : (int64_t)kt * kKT;
-        const uint32_t dst = raw_me + (uint32_t)(i % DR) * (kM * RB);
-#pragma unroll
-        for (int h = 0; h < RB / 16; ++h) {
-          const bool ok = live && b0 + 16 * h < p.ld_codes[m];
-          const uint8_t *src = ok ? crow + b0 + 16 * h : p.codes[m];
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + 16 * h),
-                       "l"(src), "r"(ok ? 16 : 0)
-                       : "memory");
-        }
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    for (int i = 0; i < DR - 1; ++i) raw_issue(i);
-    // inputs (and the gathered B tiles) may come from earlier kernels
+    const uint32_t raw_me = smem_u32(raw) + (uint32_t)r * RB + (uint32_t)h * HB;
+    // inputs may come from earlier kernels (outlier weights do not)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int kt = kt_begin; kt < kt_end; ++kt) {
       const int q = kt - kt_begin;  // position in this CTA's ring sequence
@@ -271,11 +276,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       if (q >= kStages && !mbar_wait(smem_u32(&empty[s]), ((q / kStages) - 1) & 1, abort_flag))
         break;
       uint8_t *A = a_st + s * kABytes;
-      uint8_t *Bt = b_st + s * bBytes;
       const bool outl = kt < tp.ko;
-      // --- A: one row of 64 k slots = 8 core-matrix rows of 16 bytes
+      const int c0 = h * (kKT / 2);  // first k slot of this thread
+      // --- A: 64 k slots of row r = 8 core-matrix rows of 16 bytes
       if (INT4 && outl) {
-        const int t0 = kt * kKT;
+        const int t0 = kt * kKT + c0;
         const uint4 *src = reinterpret_cast<const uint4 *>(p.w_out[m] + grow * p.ld_out[m]);
 #pragma unroll
         for (int kg = 0; kg < 8; ++kg) {
@@ -288,27 +293,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
             if (valid < 8) {
               uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int h = 0; h < 8; ++h)
-                if (h >= valid) w[h >> 1] &= (h & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+              for (int e = 0; e < 8; ++e)
+                if (e >= valid) w[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
               v = make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
-          *reinterpret_cast<uint4 *>(A + core_off(r, kg * 8)) = v;
+          *reinterpret_cast<uint4 *>(A + core_off(r, c0 + kg * 8)) = v;
         }
       } else if (INT4) {
         const int i = kt - bgb;
-        raw_issue(i + DR - 1);
-        asm volatile("cp.async.wait_group %0;" ::"n"(DR - 1) : "memory");
+        if (!mbar_wait(smem_u32(&rfull[i % DR]), (i / DR) & 1, abort_flag)) break;
         const uint32_t rsrc = raw_me + (uint32_t)(i % DR) * (kM * RB);
-        uint4 q[2];
+        uint4 qv[2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int c = 0; c < 2; ++c)
           asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(q[h].x), "=r"(q[h].y), "=r"(q[h].z), "=r"(q[h].w)
-                       : "r"(rsrc + 16 * h));
-        const uint32_t words[8] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w};
+                       : "=r"(qv[c].x), "=r"(qv[c].y), "=r"(qv[c].z), "=r"(qv[c].w)
+                       : "r"(rsrc + 16 * c));
+        mbar_arrive(smem_u32(&rempty[i % DR]));  // the codes are in registers
+        const uint32_t words[8] = {qv[0].x, qv[0].y, qv[0].z, qv[0].w,
+                                   qv[1].x, qv[1].y, qv[1].z, qv[1].w};
         const uint32_t bias = 0x64086408u;   // 1032 in both halves after the XOR
-        const uint32_t k1032 = 0x64086408u;
 #pragma unroll
         for (int kg = 0; kg < 8; ++kg) {
           const uint32_t w = words[kg];
@@ -318,25 +323,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
           uint32_t h3 = ((w >> 12) & 0x000F000Fu) ^ bias;  // 3 and 7
           // 1024 + (q+8) - 1032 = q, exact in fp16; elements past kb hold
           // zero nibbles (q = 0) from the row padding, and zero rows past N
-          h0 = hsub2_u32(h0, k1032);
-          h1 = hsub2_u32(h1, k1032);
-          h2 = hsub2_u32(h2, k1032);
-          h3 = hsub2_u32(h3, k1032);
+          h0 = hsub2_u32(h0, bias);
+          h1 = hsub2_u32(h1, bias);
+          h2 = hsub2_u32(h2, bias);
+          h3 = hsub2_u32(h3, bias);
           if (!live) h0 = h1 = h2 = h3 = 0;
           // slot order 0,4,1,5,2,6,3,7
-          *reinterpret_cast<uint4 *>(A + core_off(r, kg * 8)) = make_uint4(h0, h1, h2, h3);
+          *reinterpret_cast<uint4 *>(A + core_off(r, c0 + kg * 8)) = make_uint4(h0, h1, h2, h3);
         }
       } else {
         const int i = kt - bgb;
-        raw_issue(i + DR - 1);
-        asm volatile("cp.async.wait_group %0;" ::"n"(DR - 1) : "memory");
+        if (!mbar_wait(smem_u32(&rfull[i % DR]), (i / DR) & 1, abort_flag)) break;
         const uint32_t rsrc = raw_me + (uint32_t)(i % DR) * (kM * RB);
+        uint4 vv[4];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint4 v;
+        for (int c = 0; c < 4; ++c)
           asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                       : "r"(rsrc + 16 * h));
+                       : "=r"(vv[c].x), "=r"(vv[c].y), "=r"(vv[c].z), "=r"(vv[c].w)
+                       : "r"(rsrc + 16 * c));
+        mbar_arrive(smem_u32(&rempty[i % DR]));  // the codes are in registers
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = vv[c];
           const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
                                  v.w ^ 0x80808080u};
           uint32_t o[8];
@@ -350,15 +358,83 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
             for (int k = 0; k < 8; ++k) o[k] = 0;
           }
-          *reinterpret_cast<uint4 *>(A + core_off(r, 16 * h)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4 *>(A + core_off(r, 16 * h + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+          *reinterpret_cast<uint4 *>(A + core_off(r, c0 + 16 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4 *>(A + core_off(r, c0 + 16 * c + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
-      // --- B: Np x 64 activations.  With a workspace the tile was gathered
-      // once per call by tc_xprep_kernel and arrives by one bulk copy.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(smem_u32(&full[s]));
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      // ---------------------------------------------------- MMA issuer ---
+      const uint32_t idesc = idesc_f16(kM, tp.Np);
+      for (int kt = kt_begin; kt < kt_end; ++kt) {
+        const int q = kt - kt_begin;
+        const int s = q % kStages, sb = q % NB;
+        if (!mbar_wait(smem_u32(&full[s]), (q / kStages) & 1, abort_flag)) break;
+        if (!mbar_wait(smem_u32(&bfull[sb]), (q / NB) & 1, abort_flag)) break;
+        fence_after();
+        const bool outl = kt < tp.ko;
+        const uint32_t d = outl ? d_out : d_bg;
+        const bool first = outl ? kt == kt_begin : kt == (kt_begin > tp.ko ? kt_begin : tp.ko);
+        const uint32_t a0 = smem_u32(a_st + s * kABytes), b0 = smem_u32(b_st + sb * bBytes);
+#pragma unroll
+        for (int k16 = 0; k16 < kKT / 16; ++k16)
+          mma_f16(d, sdesc(a0 + k16 * 2 * kLBO), sdesc(b0 + k16 * 2 * kLBO), idesc,
+                  (first && k16 == 0) ? 0u : 1u);
+        mma_commit(smem_u32(&empty[s]));
+        mma_commit(smem_u32(&bempty[sb]));
+      }
+      mma_commit(smem_u32(done));  // arrives once every issued MMA has completed
+    }
+  } else if (warp == kLoadWarp) {
+    // ------------------------------------------------ activation loader ---
+    // Np x kKT activations per K tile, NB tiles ahead of the MMAs.  With a
+    // workspace the tile was gathered once per call by tc_xprep_kernel and
+    // arrives by one bulk copy; without one this warp gathers it.
+    constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
+    const int bgb = kt_begin > tp.ko ? kt_begin : tp.ko;  // first code tile
+    const uint64_t cmap = reinterpret_cast<uint64_t>(&tp.codes_map[m]);
+    // the codes are static: the first DR tiles are requested before the wait
+    auto raw_issue = [&](int kt) {
+      const int i = kt - bgb;
+      const uint32_t bar = smem_u32(&rfull[i % DR]);
+      if (i >= DR) {
+        if (!mbar_wait(smem_u32(&rempty[i % DR]), ((i / DR) - 1) & 1, abort_flag)) return false;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      const int x = INT4 ? (kt - tp.ko) * RB : kt * RB;
+      asm volatile(
+          "{\n\t.reg .b64 t;\n\t"
+          "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
+          "r"((uint32_t)(kM * RB))
+          : "memory");
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+          "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(raw) + (uint32_t)(i % DR) * (kM * RB)),
+          "l"(cmap), "r"(x), "r"((int)row0), "r"(bar)
+          : "memory");
+      return true;
+    };
+    int kr = bgb;  // next code tile to request
+    if (lane == 0)
+      for (; kr < kt_end && kr < bgb + DR; ++kr) raw_issue(kr);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int kt = kt_begin; kt < kt_end; ++kt) {
+      const int q = kt - kt_begin;
+      const int sb = q % NB;
+      // keep the code ring DR tiles ahead of this K tile
+      if (lane == 0)
+        for (; kr < kt_end && kr < kt + DR; ++kr)
+          if (!raw_issue(kr)) break;
+      if (*(volatile int *)abort_flag) break;
+      if (q >= NB && !mbar_wait(smem_u32(&bempty[sb]), ((q / NB) - 1) & 1, abort_flag)) break;
+      uint8_t *Bt = b_st + sb * bBytes;
+      const uint32_t bar = smem_u32(&bfull[sb]);
       if (tp.ws) {
-        if (tid == 0) {
-          const uint32_t bar = smem_u32(&full[s]);
+        if (lane == 0) {
           asm volatile(
               "{\n\t.reg .b64 t;\n\t"
               "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
@@ -370,48 +446,31 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
               "l"(tp.ws + (size_t)kt * bBytes), "r"((uint32_t)bBytes), "r"(bar)
               : "memory");
         }
-      } else
-      for (int idx = tid; idx < tp.Np * kKT; idx += kProducers) {
-        const int c = idx % kKT, n = idx / kKT;
-        __half v = __float2half_rn(0.0f);
-        if (n < tp.B) {
-          const __half *xb = p.x + (int64_t)n * p.ldx;
-          if (INT4 && outl) {
-            const int t = kt * kKT + c;
-            if (t < p.n_out) v = xb[__ldg(p.perm + t)];
-          } else if (INT4) {
-            const int e = (kt - tp.ko) * kKT + slot_elem(c);
-            if (e < p.kb) v = xb[__ldg(p.perm + p.n_out + e)];
-          } else {
-            const int e = kt * kKT + c;
-            if (e < p.K) v = xb[e];
+      } else {
+        const bool outl = kt < tp.ko;
+        for (int idx = lane; idx < tp.Np * kKT; idx += 32) {
+          const int c = idx % kKT, n = idx / kKT;
+          __half v = __float2half_rn(0.0f);
+          if (n < tp.B) {
+            const __half *xb = p.x + (int64_t)n * p.ldx;
+            if (INT4 && outl) {
+              const int t = kt * kKT + c;
+              if (t < p.n_out) v = xb[__ldg(p.perm + t)];
+            } else if (INT4) {
+              const int e = (kt - tp.ko) * kKT + slot_elem(c);
+              if (e < p.kb) v = xb[__ldg(p.perm + p.n_out + e)];
+            } else {
+              const int e = kt * kKT + c;
+              if (e < p.K) v = xb[e];
+            }
           }
+          *reinterpret_cast<__half *>(Bt + core_off(n, c)) = v;
         }
-        *reinterpret_cast<__half *>(Bt + core_off(n, c)) = v;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(smem_u32(&full[s]));
     }
-  } else if (lane == 0) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // ------------------------------------------------------ MMA issuer ---
-    const uint32_t idesc = idesc_f16(kM, tp.Np);
-    for (int kt = kt_begin; kt < kt_end; ++kt) {
-      const int q = kt - kt_begin;
-      const int s = q % kStages;
-      if (!mbar_wait(smem_u32(&full[s]), (q / kStages) & 1, abort_flag)) break;
-      fence_after();
-      const bool outl = kt < tp.ko;
-      const uint32_t d = outl ? d_out : d_bg;
-      const bool first = outl ? kt == kt_begin : kt == (kt_begin > tp.ko ? kt_begin : tp.ko);
-      const uint32_t a0 = smem_u32(a_st + s * kABytes), b0 = smem_u32(b_st + s * bBytes);
-#pragma unroll
-      for (int k16 = 0; k16 < kKT / 16; ++k16)
-        mma_f16(d, sdesc(a0 + k16 * 2 * kLBO), sdesc(b0 + k16 * 2 * kLBO), idesc,
-                (first && k16 == 0) ? 0u : 1u);
-      mma_commit(smem_u32(&empty[s]));
-    }
-    mma_commit(smem_u32(done));  // arrives once every issued MMA has completed
   }
 
   // ---------------------------------------------------------- epilogue ----
@@ -437,7 +496,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         const float y = fmaf(s_i, bg, o);  // partial of this CTA's K tiles
         if (S == 1) {
           if (ok && grow < nrows && n < tp.B)
-            p.y[m][(int64_t)n * p.ldy + grow] = __float2half_rn(y);
+            p.y[m][(int64_t)n * p.ldy[m] + grow] = __float2half_rn(y);
         } else {
           part[n * kM + r] = ok ? y : 0.0f;
         }
@@ -465,7 +524,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         acc += v;
       }
       const int64_t grow = row0 + r;
-      if (grow < nrows && n < tp.B) p.y[m][(int64_t)n * p.ldy + grow] = __float2half_rn(acc);
+      if (grow < nrows && n < tp.B) p.y[m][(int64_t)n * p.ldy[m] + grow] = __float2half_rn(acc);
     }
     // keep every CTA's shared memory alive until all remote reads are done
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -492,23 +551,38 @@ __global__ void __launch_bounds__(256) tc_xprep_kernel(const __grid_constant__ T
   const int bBytes = tp.Np * kKT * 2;
   uint8_t *tile = ws + (size_t)kt * bBytes;
   const bool outl = kt < tp.ko;
-  for (int idx = threadIdx.x; idx < tp.Np * kKT; idx += 256) {
-    const int c = idx % kKT, n = idx / kKT;
-    __half v = __ushort_as_half((unsigned short)0);
-    if (n < tp.B) {
-      const __half *xb = p.x + (int64_t)n * p.ldx;
-      if (INT4 && outl) {
-        const int t = kt * kKT + c;
-        if (t < p.n_out) v = xb[__ldg(p.perm + t)];
-      } else if (INT4) {
-        const int e = (kt - tp.ko) * kKT + slot_elem(c);
-        if (e < p.kb) v = xb[__ldg(p.perm + p.n_out + e)];
-      } else {
-        const int e = kt * kKT + c;
-        if (e < p.K) v = xb[e];
+  // Eight elements per thread and step, all eight loads issued before the
+  // one 16-byte store: the compiler cannot prove that the workspace does not
+  // alias the inputs, so loads and stores mixed in one loop stay in order.
+  const int total = tp.Np * kKT;
+  for (int base = threadIdx.x * 8; base < total; base += 256 * 8) {
+    __half v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int idx = base + k;             // 8 consecutive k slots of one row n
+      const int c = idx % kKT, n = idx / kKT;
+      v[k] = __ushort_as_half((unsigned short)0);
+      if (n < tp.B) {
+        const __half *xb = p.x + (int64_t)n * p.ldx;
+        if (INT4 && outl) {
+          const int t = kt * kKT + c;
+          if (t < p.n_out) v[k] = xb[__ldg(p.perm + t)];
+        } else if (INT4) {
+          const int e = (kt - tp.ko) * kKT + slot_elem(c);
+          if (e < p.kb) v[k] = xb[__ldg(p.perm + p.n_out + e)];
+        } else {
+          const int e = kt * kKT + c;
+          if (e < p.K) v[k] = xb[e];
+        }
       }
     }
-    *reinterpret_cast<__half *>(tile + core_off(n, c)) = v;
+    // slots c .. c+7 (c a multiple of 8) are one 16-byte core-matrix row
+    const int c = base % kKT, n = base / kKT;
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      h[k] = (uint32_t)__half_as_ushort(v[2 * k]) | ((uint32_t)__half_as_ushort(v[2 * k + 1]) << 16);
+    *reinterpret_cast<uint4 *>(tile + core_off(n, c)) = make_uint4(h[0], h[1], h[2], h[3]);
   }
 }
 
@@ -521,10 +595,60 @@ size_t tc_workspace_bytes(bool int4, int64_t B, int64_t K, int64_t n_out) {
   return (size_t)(tiles * Np * kKT * 2);
 }
 
-size_t tc_smem_bytes(bool int4, int Np) {
-  return 1024 + (size_t)kStages * (kABytes + Np * kKT * 2) +
-         (int4 ? RawRing<true>::BYTES : RawRing<false>::BYTES) + (2 * kStages + 1) * 8 + 16;
+// Stages of the activation ring for a batch of Np (MMA N) columns.
+static int tc_b_stages(int Np) {
+  const size_t per = (size_t)Np * kKT * 2;
+  const size_t n = kBRingBytes / per;
+  return (int)(n < (size_t)kMaxBStages ? n : (size_t)kMaxBStages);
 }
+
+size_t tc_smem_bytes(bool int4, int Np) {
+  return 1024 + (size_t)kStages * kABytes + (size_t)tc_b_stages(Np) * Np * kKT * 2 +
+         (int4 ? RawRing<true>::BYTES : RawRing<false>::BYTES) +
+         (2 * kStages + 2 * kMaxBStages + 2 * kMaxRaw + 1) * 8 + 16;
+}
+
+namespace {
+
+// cuTensorMapEncodeTiled, found once through the runtime's driver entry point
+// (the library does not link the driver API).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// The packed codes of one matrix as a 2D byte tensor [rows][ld bytes], read
+// in boxes of kM rows x row_bytes bytes (rows past the end read as zeros).
+qz_status codes_map(CUtensorMap *map, const uint8_t *codes, int64_t ld, int64_t rows,
+                    int row_bytes) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return QZ_ERR_CUDA;
+  const cuuint64_t dim[2] = {(cuuint64_t)ld, (cuuint64_t)rows};
+  const cuuint64_t stride[1] = {(cuuint64_t)ld};
+  const cuuint32_t box[2] = {(cuuint32_t)row_bytes, (cuuint32_t)kM};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dim,
+                        stride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? QZ_OK : QZ_ERR_INVALID_ARG;
+}
+
+}  // namespace
 
 qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_rows,
                     void *workspace, size_t workspace_bytes, cudaStream_t s) {
@@ -532,9 +656,11 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   qz_status st = device_info(&di);
   if (st != QZ_OK) return st;
   TcParams tp;
+  memset(&tp, 0, sizeof(tp));
   tp.g = g;
   tp.B = B;
   tp.Np = (B + 15) / 16 * 16;
+  tp.nbs = tc_b_stages(tp.Np);
   tp.ko = int4 ? (g.n_out + kKT - 1) / kKT : 0;
   tp.kbt = int4 ? (g.kb + kKT - 1) / kKT : (g.K + kKT - 1) / kKT;
   tp.S = 1;
@@ -544,6 +670,12 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
     if ((uintptr_t)workspace & 15u) return QZ_ERR_ALIGNMENT;
     tp.ws = reinterpret_cast<const uint8_t *>(workspace);
   }
+  for (int m = 0; m < g.n_mats; ++m)
+    if (tp.kbt > 0) {
+      st = codes_map(&tp.codes_map[m], g.codes[m], g.ld_codes[m], mat_rows[m],
+                     int4 ? RawRing<true>::ROWB : RawRing<false>::ROWB);
+      if (st != QZ_OK) return st;
+    }
   int tiles = 0;
   for (int m = 0; m < QZ_MAX_GROUP; ++m) {
     tp.mat_rows[m] = m < g.n_mats ? mat_rows[m] : 0;
@@ -554,9 +686,9 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   const size_t smem = tc_smem_bytes(int4, tp.Np);
   if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
   // Split K over a cluster of S CTAs per tile so that small matrices still
-  // fill the GPU.  A CTA costs a fixed start/epilogue of about 8 K tiles plus
+  // fill the GPU.  A CTA costs a fixed start/epilogue of about 4 K tiles plus
   // its share of the K tiles; pick S in {1,2,4,8} minimising
-  // waves * (8 + tiles_of_K / S), keeping at least two K tiles per CTA.
+  // waves * (4 + tiles_of_K / S), keeping at least two K tiles per CTA.
   {
     const int per_sm_smem = (int)(233472 / (smem + 1024));
     const int per_sm_tmem = 512 / (tp.Np <= 16 ? 32 : (tp.Np <= 32 ? 64 : 128));
@@ -567,7 +699,7 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
     for (int S = 1; S <= 8; S *= 2) {
       if (S > 1 && kt_total < 2 * S) break;
       const long ctas = (long)tiles * S;
-      const double t = (double)((ctas + slots - 1) / slots) * (8.0 + (double)kt_total / S);
+      const double t = (double)((ctas + slots - 1) / slots) * (4.0 + (double)kt_total / S);
       if (t < best - 1e-9) {
         best = t;
         tp.S = S;

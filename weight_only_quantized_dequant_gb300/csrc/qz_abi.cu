@@ -152,12 +152,12 @@ void fill_int4o(GemvParams &p, const qz_int4o_weight *ws, int n) {
 }
 
 qz_status gemm_common(bool int4, GemvParams &p, int64_t B, const qz_half *X, int64_t ldx,
-                      qz_half *const *Ys, int64_t ldy, int n, void *ws, size_t ws_bytes,
+                      qz_half *const *Ys, const int64_t *ldys, int n, void *ws, size_t ws_bytes,
                       cudaStream_t s) {
   p.x = reinterpret_cast<const __half *>(X);
   p.overlap = overlap_enabled();
   p.ldx = B > 1 ? ldx : 0;
-  p.ldy = B > 1 ? ldy : 0;
+  for (int m = 0; m < QZ_MAX_GROUP; ++m) p.ldy[m] = (B > 1 && m < n) ? ldys[m] : 0;
   for (int m = 0; m < n; ++m) p.y[m] = reinterpret_cast<__half *>(Ys[m]);
   DeviceInfo di;
   QZ_TRY(device_info(&di));
@@ -240,7 +240,7 @@ qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X, int
   GemvParams p;
   fill_int8(p, w, 1);
   qz_half *ys[1] = {Y};
-  return gemm_common(false, p, B, X, ldx, ys, ldy, 1, workspace, workspace_bytes,
+  return gemm_common(false, p, B, X, ldx, ys, &ldy, 1, workspace, workspace_bytes,
                      (cudaStream_t)s);
 }
 
@@ -269,7 +269,24 @@ qz_status qz_gemv_int8_grouped(const qz_int8_weight *ws, int n, const qz_half *x
   QZ_TRY(check_vec(x, 1, ws[0].K, 0));
   GemvParams p;
   fill_int8(p, ws, n);
-  return gemm_common(false, p, 1, x, 0, ys, 0, n, nullptr, 0, (cudaStream_t)s);
+  return gemm_common(false, p, 1, x, 0, ys, nullptr, n, nullptr, 0, (cudaStream_t)s);
+}
+
+qz_status qz_gemm_int8_grouped(const qz_int8_weight *ws, int n, int64_t B, const qz_half *X,
+                               int64_t ldx, qz_half *const *Ys, const int64_t *ldys,
+                               void *workspace, size_t workspace_bytes, qz_stream s) {
+  if (!ws || !Ys || !ldys || n < 1 || B < 1) return QZ_ERR_INVALID_ARG;
+  if (n > QZ_MAX_GROUP || B > QZ_MAX_BATCH) return QZ_ERR_UNSUPPORTED;
+  for (int m = 0; m < n; ++m) {
+    QZ_TRY(check_int8_weight(&ws[m]));
+    if (ws[m].K != ws[0].K) return QZ_ERR_INVALID_ARG;
+    QZ_TRY(check_vec(Ys[m], B, ws[m].N, ldys[m]));
+  }
+  QZ_TRY(check_vec(X, B, ws[0].K, ldx));
+  GemvParams p;
+  fill_int8(p, ws, n);
+  return gemm_common(false, p, B, X, ldx, Ys, ldys, n, workspace, workspace_bytes,
+                     (cudaStream_t)s);
 }
 
 size_t qz_gemm_workspace_bytes(int64_t B, int64_t K, int64_t n_out) {
@@ -350,7 +367,26 @@ qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B, const qz_hal
   GemvParams p;
   fill_int4o(p, w, 1);
   qz_half *ys[1] = {Y};
-  return gemm_common(true, p, B, X, ldx, ys, ldy, 1, workspace, workspace_bytes,
+  return gemm_common(true, p, B, X, ldx, ys, &ldy, 1, workspace, workspace_bytes,
+                     (cudaStream_t)s);
+}
+
+qz_status qz_gemm_int4_outlier_grouped(const qz_int4o_weight *ws, int n, int64_t B,
+                                       const qz_half *X, int64_t ldx, qz_half *const *Ys,
+                                       const int64_t *ldys, void *workspace,
+                                       size_t workspace_bytes, qz_stream s) {
+  if (!ws || !Ys || !ldys || n < 1 || B < 1) return QZ_ERR_INVALID_ARG;
+  if (n > QZ_MAX_GROUP || B > QZ_MAX_BATCH) return QZ_ERR_UNSUPPORTED;
+  for (int m = 0; m < n; ++m) {
+    QZ_TRY(check_int4o_weight(&ws[m]));
+    if (ws[m].K != ws[0].K || ws[m].n_out != ws[0].n_out || ws[m].perm != ws[0].perm)
+      return QZ_ERR_INVALID_ARG;
+    QZ_TRY(check_vec(Ys[m], B, ws[m].N, ldys[m]));
+  }
+  QZ_TRY(check_vec(X, B, ws[0].K, ldx));
+  GemvParams p;
+  fill_int4o(p, ws, n);
+  return gemm_common(true, p, B, X, ldx, Ys, ldys, n, workspace, workspace_bytes,
                      (cudaStream_t)s);
 }
 
@@ -367,7 +403,7 @@ qz_status qz_gemv_int4_outlier_grouped(const qz_int4o_weight *ws, int n, const q
   QZ_TRY(check_vec(x, 1, ws[0].K, 0));
   GemvParams p;
   fill_int4o(p, ws, n);
-  return gemm_common(true, p, 1, x, 0, ys, 0, n, nullptr, 0, (cudaStream_t)s);
+  return gemm_common(true, p, 1, x, 0, ys, nullptr, n, nullptr, 0, (cudaStream_t)s);
 }
 
 }  // extern "C"

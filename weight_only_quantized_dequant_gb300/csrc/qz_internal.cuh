@@ -42,7 +42,7 @@ struct GemvParams {
   int64_t ld_out[QZ_MAX_GROUP];        // halves between rows
   const float *scale[QZ_MAX_GROUP];    // INT8: [1]; INT4: [N]
   __half *y[QZ_MAX_GROUP];             // [B][ldy]
-  int64_t ldy;
+  int64_t ldy[QZ_MAX_GROUP];          // row stride of each y
   int overlap;  // programmatic dependent launch + weight prefetch before the wait
 };
 

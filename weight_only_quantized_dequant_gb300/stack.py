@@ -88,10 +88,10 @@ class LayerStack:
 
     # ------------------------------------------------------------- run ----
     def launches_per_step(self) -> int:
-        per_group = 1 if self.batch == 1 else None
-        if per_group is None:  # batched calls run one launch per matrix
-            return self.n_layers * len(S.MATS)
-        return self.n_layers * len(S.GROUPS)
+        """Kernel launches of one step: one per group; on the tensor-core path
+        (batch > 4) each group adds the launch that gathers its inputs."""
+        per_group = 1 if self.batch <= 4 else 2
+        return self.n_layers * len(S.GROUPS) * per_group
 
     def run_group(self, l: int, g: int, stream=None):
         names = S.GROUPS[g]
@@ -106,10 +106,12 @@ class LayerStack:
             else:
                 fn = api.gemv_int8_grouped if int8 else api.gemv_int4_outlier_grouped
                 fn(mats, x[0], outs, stream=stream)
-        else:
+        elif len(mats) == 1:
             fn = api.gemm_int8 if int8 else api.gemm_int4_outlier
-            for w, y in zip(mats, ys):
-                fn(w, x, y, stream=stream, workspace=self.workspace)
+            fn(mats[0], x, ys[0], stream=stream, workspace=self.workspace)
+        else:
+            fn = api.gemm_int8_grouped if int8 else api.gemm_int4_outlier_grouped
+            fn(mats, x, ys, stream=stream, workspace=self.workspace)
 
     def run_step(self, stream=None):
         for l in range(self.n_layers):
