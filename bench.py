@@ -5,7 +5,8 @@ layer), replayed from a CUDA graph.  The stack (several GB) is far larger
 than the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--extra] [--head] [--paged] [--no-cpu]
+                  [--impl ours|reference] [--extra] [--head] [--paged] [--tiered]
+                  [--no-cpu]
 
 Prints ONE JSON line.  Under torchrun (N > 1) every rank runs an independent
 replica (the method targets one GPU; no collectives) and rank 0 prints.
@@ -43,6 +44,9 @@ def parse():
                     help="also stream the 70B and Gemma stacks through the pager")
     ap.add_argument("--head", action="store_true",
                     help="also time the 3B vocabulary lookup + lm_head (tied INT8, untied INT4)")
+    ap.add_argument("--tiered", action="store_true",
+                    help="also time the 70B stack with layers 40.. in pinned host memory "
+                         "(read in place, or paged), and all 80 read in place")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch without programmatic dependent launch")
     ap.add_argument("--batch", type=int, default=1,
@@ -520,6 +524,40 @@ def measure_head(name: str, steps: int, warmup: int, device):
     return out
 
 
+def measure_tiered(wl_name: str, resident: int, mode: str, steps: int, warmup: int, device,
+                   distinct: int = 4):
+    """First `resident` layers in HBM, the rest in pinned host memory, read in
+    place (zero_copy) or streamed through the pager (paged)."""
+    import torch
+
+    from weight_only_quantized_dequant_gb300 import api
+    from weight_only_quantized_dequant_gb300 import stack as ST
+    from weight_only_quantized_dequant_gb300 import synthetic as S
+
+    ts = ST.TieredStack(S.WORKLOADS[wl_name], resident, mode, distinct=distinct, device=device)
+    cs = ts.stream
+    for _ in range(warmup):
+        ts.run_step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    for _ in range(steps):
+        ts.run_step()
+    e1.record(cs)
+    torch.cuda.synchronize(device)
+    assert api.device_error() == 0
+    ms = e0.elapsed_time(e1) / steps
+    tier_b = ts.n_layers - ts.resident
+    out = {"workload": wl_name, "mode": mode, "layers": ts.n_layers, "resident": ts.resident,
+           "ms_per_step": round(ms, 3), "us_per_layer": round(ms * 1e3 / ts.n_layers, 2),
+           "gbs": round(ts.bytes_per_step() / (ms * 1e-3) / 1e9, 1),
+           "host_layer_bytes": ts.weight_bytes_per_layer}
+    ts.close()
+    del ts
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     a = parse()
     if a.impl == "reference":
@@ -568,6 +606,13 @@ def main():
     if a.head and rank == 0:
         extra["llama32_3b_head"] = measure_head("llama32_3b_head", max(10, a.steps), a.warmup,
                                                 device)
+
+    if a.tiered and rank == 0:
+        wl70 = "llama_70b_int4o"
+        for res, mode in ((0, "zero_copy"), (40, "zero_copy"), (40, "paged")):
+            extra[f"{wl70}_tiered_{res}_{mode}"] = measure_tiered(wl70, res, mode,
+                                                                  max(2, a.steps // 10), 1, device)
+        extra["link_probe_gbs"] = round(h2d_probe_gbs(device), 1)
 
     if a.paged and rank == 0:
         for name in ("llama_70b_int4o", "gemma2_9b_int8"):

@@ -70,6 +70,9 @@ class Int8Matrix:
     def struct(self) -> Int8Weight:
         return Int8Weight(self.q.data_ptr(), self.scale.data_ptr(), self.N, self.K, self.ldq)
 
+    def tensors(self):
+        return (self.q, self.scale)
+
     def nbytes(self) -> int:
         """Algorithmic bytes: N*K codes + one fp32 scale."""
         return self.N * self.K + 4
@@ -210,6 +213,9 @@ class Int4oMatrix:
                            self.q4.data_ptr() if self.ld_q4 else None,
                            self.scale.data_ptr())
 
+    def tensors(self):
+        return (self.perm, self.w_out, self.q4, self.scale)
+
     def nbytes(self) -> int:
         """Algorithmic bytes: packed codes + fp16 outliers + fp32 row scales."""
         kb = self.K - self.n_out
@@ -322,6 +328,25 @@ def gemm_int4_outlier_grouped(ws, X: torch.Tensor, Ys=None, stream=None, workspa
     """Ys[m] [B, N_m] for X [B, K] and n matrices sharing K, n_out and perm."""
     return _grouped_gemm("qz_gemm_int4_outlier_grouped", Int4oWeight, ws, X, Ys, stream,
                          workspace, ws[0].n_out)
+
+
+def gemv_mapped(ws, x: torch.Tensor, ys=None, stream=None):
+    """Batch-1 grouped product with the weights read in place (zero-copy):
+    the matrices' tensors may be pinned host tensors (or device tensors).
+    ws: Int8Matrix or Int4oMatrix list sharing K (INT4: and the permutation)."""
+    _need_cuda(x)
+    n = len(ws)
+    ys = [_vec_out(x, w.N) for w in ws] if ys is None else ys
+    for w in ws:
+        for t in w.tensors():
+            if t.numel() and not (t.is_cuda or t.is_pinned()):
+                raise ValueError("zero-copy weights must be device or pinned host tensors")
+    int8 = isinstance(ws[0], Int8Matrix)
+    arr = ((Int8Weight if int8 else Int4oWeight) * n)(*[w.struct() for w in ws])
+    yp = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    fn = "qz_gemv_int8_grouped_mapped" if int8 else "qz_gemv_int4_outlier_grouped_mapped"
+    _lib.call(fn, arr, n, x.data_ptr(), yp, _stream(stream))
+    return ys
 
 
 # ----------------------------------------------------------------- Pager ---

@@ -38,8 +38,9 @@ constexpr int kKT = 128;        // K elements per pipeline stage
 constexpr int kStages = 3;
 constexpr int kProducers = 256;  // 8 warps, two threads per weight row
 constexpr int kMmaWarp = kProducers / 32;     // warp 8 issues the MMAs
-constexpr int kLoadWarp = kMmaWarp + 1;       // warp 9 fills the activation ring
-constexpr int kThreadsTc = kProducers + 64;
+constexpr int kCodeWarp = kMmaWarp + 1;       // warp 9 fills the code ring
+constexpr int kLoadWarp = kMmaWarp + 2;       // warp 10 fills the activation ring
+constexpr int kThreadsTc = kProducers + 96;
 constexpr int kMaxBStages = 8;                // activation ring depth (smem permitting)
 constexpr size_t kBRingBytes = 80 * 1024;     // shared memory given to that ring
 constexpr int kABytes = kM * kKT * 2;         // 32 KiB per stage
@@ -389,47 +390,45 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       }
       mma_commit(smem_u32(done));  // arrives once every issued MMA has completed
     }
+  } else if (warp == kCodeWarp) {
+    // ------------------------------------------------------ code loader ---
+    // Packed codes of the background (INT4) or all (INT8) K tiles, one 2D
+    // tensor copy of kM rows x ROWB bytes per tile, DR tiles ahead of the
+    // converters.  The codes are static: the first DR tiles are requested
+    // before the wait for the previous kernel.
+    if (lane == 0) {
+      constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
+      const int bgb = kt_begin > tp.ko ? kt_begin : tp.ko;  // first code tile
+      const uint64_t cmap = reinterpret_cast<uint64_t>(&tp.codes_map[m]);
+      for (int kt = bgb; kt < kt_end; ++kt) {
+        const int i = kt - bgb;
+        const uint32_t bar = smem_u32(&rfull[i % DR]);
+        if (i >= DR) {
+          if (!mbar_wait(smem_u32(&rempty[i % DR]), ((i / DR) - 1) & 1, abort_flag)) break;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        const int x = INT4 ? (kt - tp.ko) * RB : kt * RB;
+        asm volatile(
+            "{\n\t.reg .b64 t;\n\t"
+            "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
+            "r"((uint32_t)(kM * RB))
+            : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+            "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(raw) + (uint32_t)(i % DR) * (kM * RB)),
+            "l"(cmap), "r"(x), "r"((int)row0), "r"(bar)
+            : "memory");
+      }
+    }
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------ activation loader ---
     // Np x kKT activations per K tile, NB tiles ahead of the MMAs.  With a
     // workspace the tile was gathered once per call by tc_xprep_kernel and
     // arrives by one bulk copy; without one this warp gathers it.
-    constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
-    const int bgb = kt_begin > tp.ko ? kt_begin : tp.ko;  // first code tile
-    const uint64_t cmap = reinterpret_cast<uint64_t>(&tp.codes_map[m]);
-    // the codes are static: the first DR tiles are requested before the wait
-    auto raw_issue = [&](int kt) {
-      const int i = kt - bgb;
-      const uint32_t bar = smem_u32(&rfull[i % DR]);
-      if (i >= DR) {
-        if (!mbar_wait(smem_u32(&rempty[i % DR]), ((i / DR) - 1) & 1, abort_flag)) return false;
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
-      const int x = INT4 ? (kt - tp.ko) * RB : kt * RB;
-      asm volatile(
-          "{\n\t.reg .b64 t;\n\t"
-          "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
-          "r"((uint32_t)(kM * RB))
-          : "memory");
-      asm volatile(
-          "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
-          "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(raw) + (uint32_t)(i % DR) * (kM * RB)),
-          "l"(cmap), "r"(x), "r"((int)row0), "r"(bar)
-          : "memory");
-      return true;
-    };
-    int kr = bgb;  // next code tile to request
-    if (lane == 0)
-      for (; kr < kt_end && kr < bgb + DR; ++kr) raw_issue(kr);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int kt = kt_begin; kt < kt_end; ++kt) {
       const int q = kt - kt_begin;
       const int sb = q % NB;
-      // keep the code ring DR tiles ahead of this K tile
-      if (lane == 0)
-        for (; kr < kt_end && kr < kt + DR; ++kr)
-          if (!raw_issue(kr)) break;
-      if (*(volatile int *)abort_flag) break;
       if (q >= NB && !mbar_wait(smem_u32(&bempty[sb]), ((q / NB) - 1) & 1, abort_flag)) break;
       uint8_t *Bt = b_st + sb * bBytes;
       const uint32_t bar = smem_u32(&bfull[sb]);
