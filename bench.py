@@ -45,8 +45,8 @@ def parse():
     ap.add_argument("--head", action="store_true",
                     help="also time the 3B vocabulary lookup + lm_head (tied INT8, untied INT4)")
     ap.add_argument("--tiered", action="store_true",
-                    help="also time the 70B stack with layers 40.. in pinned host memory "
-                         "(read in place, or paged), and all 80 read in place")
+                    help="also time the 70B stack with its first 40 (60) layers in HBM and "
+                         "the rest streamed from pinned host memory")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch without programmatic dependent launch")
     ap.add_argument("--batch", type=int, default=1,
@@ -524,17 +524,17 @@ def measure_head(name: str, steps: int, warmup: int, device):
     return out
 
 
-def measure_tiered(wl_name: str, resident: int, mode: str, steps: int, warmup: int, device,
+def measure_tiered(wl_name: str, resident: int, steps: int, warmup: int, device,
                    distinct: int = 4):
-    """First `resident` layers in HBM, the rest in pinned host memory, read in
-    place (zero_copy) or streamed through the pager (paged)."""
+    """First `resident` layers in HBM, the rest streamed from pinned host
+    memory through the pager."""
     import torch
 
     from weight_only_quantized_dequant_gb300 import api
     from weight_only_quantized_dequant_gb300 import stack as ST
     from weight_only_quantized_dequant_gb300 import synthetic as S
 
-    ts = ST.TieredStack(S.WORKLOADS[wl_name], resident, mode, distinct=distinct, device=device)
+    ts = ST.TieredStack(S.WORKLOADS[wl_name], resident, distinct=distinct, device=device)
     cs = ts.stream
     for _ in range(warmup):
         ts.run_step()
@@ -548,7 +548,7 @@ def measure_tiered(wl_name: str, resident: int, mode: str, steps: int, warmup: i
     assert api.device_error() == 0
     ms = e0.elapsed_time(e1) / steps
     tier_b = ts.n_layers - ts.resident
-    out = {"workload": wl_name, "mode": mode, "layers": ts.n_layers, "resident": ts.resident,
+    out = {"workload": wl_name, "layers": ts.n_layers, "resident": ts.resident,
            "ms_per_step": round(ms, 3), "us_per_layer": round(ms * 1e3 / ts.n_layers, 2),
            "gbs": round(ts.bytes_per_step() / (ms * 1e-3) / 1e9, 1),
            "host_layer_bytes": ts.weight_bytes_per_layer}
@@ -609,9 +609,9 @@ def main():
 
     if a.tiered and rank == 0:
         wl70 = "llama_70b_int4o"
-        for res, mode in ((0, "zero_copy"), (40, "zero_copy"), (40, "paged")):
-            extra[f"{wl70}_tiered_{res}_{mode}"] = measure_tiered(wl70, res, mode,
-                                                                  max(2, a.steps // 10), 1, device)
+        for res in (40, 60):
+            extra[f"{wl70}_tiered_{res}"] = measure_tiered(wl70, res, max(2, a.steps // 10), 1,
+                                                           device)
         extra["link_probe_gbs"] = round(h2d_probe_gbs(device), 1)
 
     if a.paged and rank == 0:

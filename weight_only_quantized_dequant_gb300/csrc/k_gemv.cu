@@ -46,44 +46,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   return r;
 }
 
-// Weight loads.  Device-resident weights stream through the non-coherent
-// path with 256-byte L2 promotion; weights in mapped host memory (zero-copy)
-// are read with plain global loads.
-template <bool ZC>
-__device__ __forceinline__ uint4 ld_w4(const uint4 *p) {
-  if constexpr (ZC) {
-    uint4 r;
-    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-  } else {
-    return ld_stream(p);
-  }
-}
-
-template <bool ZC>
-__device__ __forceinline__ float ld_wf(const float *p) {
-  if constexpr (ZC) {
-    float v;
-    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
-    return v;
-  } else {
-    return __ldg(p);
-  }
-}
-
-template <bool ZC>
-__device__ __forceinline__ int ld_wi(const int32_t *p) {
-  if constexpr (ZC) {
-    int v;
-    asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-  } else {
-    return __ldg(p);
-  }
-}
-
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -278,10 +240,7 @@ __device__ __forceinline__ void locate(const Bounds &bd, int r, int &m, int &i) 
   i = r - lo;
 }
 
-// ZC: the weights (codes, outliers, scales, permutation) may live in mapped
-// host memory; codes are then read by every lane with plain loads, one stage
-// of rounds at a time, instead of through the bulk-copy ring.
-template <bool INT4, int B, bool ZC = false>
+template <bool INT4, int B>
 __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
     gemv_kernel(const __grid_constant__ GemvParams p) {
   constexpr int R = Ring<B>::R, NS = Ring<B>::NS, kRPS = Ring<B>::RPS;
@@ -297,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
   __half *xs = reinterpret_cast<__half *>(smem_raw);
   __half *xo = reinterpret_cast<__half *>(smem_raw + B * bstride);
   uint8_t *ring = smem_raw + (((size_t)B * bstride + (size_t)B * ostride + 127) & ~(size_t)127);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (ZC ? 0 : (size_t)kWarps * NS * R * kStageRow));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)kWarps * NS * R * kStageRow);
 
   const int64_t r0 = p.total_rows * blockIdx.x / gridDim.x;
   const int64_t r1 = p.total_rows * (blockIdx.x + 1) / gridDim.x;
@@ -307,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
   // programmatic overlap this CTA may start while the previous kernel on the
   // stream is still running; the weights are static by the caller's promise,
   // and x (which that kernel may produce) is only read after the wait.
-  if (!ZC && threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
     int64_t budget = kPrefetchBytes;
     int64_t r = r0;
     for (int m = 0; m < p.n_mats && budget > 0 && r < r1; ++m) {
@@ -392,10 +351,8 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
 
   // The first stages are issued before the wait: weights are static, so
   // under programmatic overlap they stream in during the previous kernel.
-  if constexpr (!ZC) {
-    if (items > 0) prow_setup(0);
-    for (int it = 0; it < NS - 1 && pleft > 0; ++it) issue_next();
-  }
+  if (items > 0) prow_setup(0);
+  for (int it = 0; it < NS - 1 && pleft > 0; ++it) issue_next();
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // let the next kernel on the stream get scheduled as SMs free up
@@ -417,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
       if constexpr (INT4) {
         int idx[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) idx[k] = e0 + k < p.kb ? ld_wi<ZC>(p.perm + p.n_out + e0 + k) : -1;
+        for (int k = 0; k < 8; ++k) idx[k] = e0 + k < p.kb ? __ldg(p.perm + p.n_out + e0 + k) : -1;
         __half v[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) v[k] = idx[k] >= 0 ? xb[idx[k]] : hzero;
@@ -438,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
     if constexpr (INT4) {
 #pragma unroll 1
       for (int e = threadIdx.x; e < p.ocpr * 8; e += kThreads)
-        xo[b * ostride / 2 + e] = e < p.n_out ? xb[ld_wi<ZC>(p.perm + e)] : hzero;
+        xo[b * ostride / 2 + e] = e < p.n_out ? xb[__ldg(p.perm + e)] : hzero;
     }
   }
   __syncthreads();
@@ -464,38 +421,14 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
     for (int rr = 0; rr < R; ++rr) {
       live[rr] = rb + rr < rhi;
       locate(bd, live[rr] ? rb + rr : rhi - 1, mrow[rr], irow[rr]);
-      srow[rr] = INT4 ? ld_wf<ZC>(p.scale[mrow[rr]] + irow[rr]) : ld_wf<ZC>(p.scale[mrow[rr]]);
+      srow[rr] = INT4 ? __ldg(p.scale[mrow[rr]] + irow[rr]) : __ldg(p.scale[mrow[rr]]);
       ov[rr] = make_uint4(0, 0, 0, 0);
       if (INT4 && lane < p.ocpr)
-        ov[rr] = ld_w4<ZC>(reinterpret_cast<const uint4 *>(
+        ov[rr] = ld_stream(reinterpret_cast<const uint4 *>(
                                p.w_out[mrow[rr]] + (int64_t)irow[rr] * p.ld_out[mrow[rr]]) +
                            lane);
     }
     for (int sj = 0; sj < SPR; ++sj) {
-      if constexpr (ZC) {
-        // every lane loads its chunk of each round straight from memory
-        uint4 v[kRPS][R];
-#pragma unroll
-        for (int u = 0; u < kRPS; ++u) {
-          const int c = (sj * kRPS + u) * 32 + lane;  // chunk of the row
-#pragma unroll
-          for (int rr = 0; rr < R; ++rr)
-            v[u][rr] = c < cpr ? ld_w4<true>(reinterpret_cast<const uint4 *>(
-                                     p.codes[mrow[rr]] + (int64_t)irow[rr] * p.ld_codes[mrow[rr]]) +
-                                 c)
-                               : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < kRPS; ++u) {
-          const int j = sj * kRPS + u;
-          if (j < Jw) {  // warp-uniform
-            const uint32_t o = lane_off + (uint32_t)j * kRound;
-            if constexpr (INT4) int4_chunk<B, R>(v[u], xs, o, bstride, acc);
-            else int8_chunk<B, R>(v[u], xs, o, bstride, acc);
-          }
-        }
-        continue;
-      }
       if (ok && pleft > 0) {
         // the slot being refilled was read by every lane before the last
         // __syncwarp; order those reads before the async-proxy write
@@ -544,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
                                                             (int64_t)irow[rr] * p.ld_out[mrow[rr]]);
 #pragma unroll 1
         for (int c = lane; c < p.ocpr; c += 32) {
-          const uint4 v = c == lane ? ov[rr] : ld_w4<ZC>(orow + c);
+          const uint4 v = c == lane ? ov[rr] : ld_stream(orow + c);
 #pragma unroll
           for (int b = 0; b < B; ++b) {
             const uint4 xv = *reinterpret_cast<const uint4 *>(
@@ -571,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
   }
   // A warp that gave up a wait still has copies in flight into its ring;
   // give them a bounded time to land before the CTA's shared memory goes.
-  if (!ZC && !ok && lane == 0) {
+  if (!ok && lane == 0) {
     for (int st = 0; st < NS; ++st) {
       const unsigned long long t0 = gtimer();
       while (!mbar_try(bar_w + st * 8, 0) && !mbar_try(bar_w + st * 8, 1) &&
@@ -581,14 +514,14 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
   }
 }
 
-template <bool INT4, int B, bool ZC = false>
+template <bool INT4, int B>
 qz_status launch_t(const GemvParams &p, cudaStream_t s) {
   constexpr int R = Ring<B>::R;
-  auto kern = gemv_kernel<INT4, B, ZC>;
+  auto kern = gemv_kernel<INT4, B>;
   DeviceInfo di;
   qz_status st = device_info(&di);
   if (st != QZ_OK) return st;
-  const size_t smem = gemv_smem_bytes(INT4, B, p, ZC);
+  const size_t smem = gemv_smem_bytes(INT4, B, p);
   if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -619,12 +552,12 @@ qz_status launch_t(const GemvParams &p, cudaStream_t s) {
 
 }  // namespace
 
-size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p, bool zc) {
+size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p) {
   const size_t cs = int4 ? 80 : 48;  // padded staged fp16 bytes per chunk
   const size_t rounds = p.cpr > 0 ? (size_t)(p.cpr + 31) / 32 : 1;
   const size_t staged = (rounds * 32 * cs + (int4 ? (size_t)p.ocpr * 16 : 0)) * (size_t)B;
   const size_t R = B == 1 ? 2 : 1, NS = 2, RPS = B == 1 ? 4 : 2;
-  const size_t ring = zc ? 0 : (size_t)kWarps * NS * R * RPS * kRoundBytes;
+  const size_t ring = (size_t)kWarps * NS * R * RPS * kRoundBytes;
   return ((staged + 127) & ~(size_t)127) + ring + (size_t)kWarps * NS * 8;
 }
 
@@ -639,10 +572,6 @@ qz_status read_gemv_error(int *code, int clear) {
   }
   *code = v;
   return QZ_OK;
-}
-
-qz_status launch_gemv_mapped(bool int4, const GemvParams &p, cudaStream_t s) {
-  return int4 ? launch_t<true, 1, true>(p, s) : launch_t<false, 1, true>(p, s);
 }
 
 qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s) {

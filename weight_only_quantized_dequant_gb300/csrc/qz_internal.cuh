@@ -50,11 +50,9 @@ struct GemvParams {
 int overlap_enabled();
 
 // Shared-memory bytes the CUDA-core kernel needs for batch B.
-size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p, bool zc = false);
+size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p);
 // Enqueue the CUDA-core GEMV for batch 1 <= B <= 4.
 qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s);
-// Batch 1 with weights read in place, also from mapped host memory.
-qz_status launch_gemv_mapped(bool int4, const GemvParams &p, cudaStream_t s);
 
 // Tensor-core (tcgen05) GEMM for any batch 1..64; rows of each matrix are
 // p.row_end differences.

@@ -280,43 +280,31 @@ class PagedStack:
 # ------------------------------------------------------------ tiering ---
 class TieredStack:
     """Tier A + tier B on one GPU ("NTransformer" summary, 3-Tier Adaptive
-    Caching: VRAM-resident layers, pinned-RAM layers): the first `resident`
-    layers live in device memory; the others stay in pinned host memory and
-    are either read in place by the zero-copy GEMV (mode "zero_copy"; the ELG
-    page's pinned pool reached by zero-copy DMA) or streamed through the pager
-    into two device slots (mode "paged").
-
-    Host layers: `distinct` packed blobs reused cyclically, as in PagedStack.
+    Caching: VRAM-resident layers, then layers streamed from pinned RAM by
+    host-to-device DMA): the first `resident` layers live in device memory,
+    the others stay in pinned host memory and stream through the pager into
+    two device slots.  Host layers: `distinct` packed blobs reused cyclically,
+    as in PagedStack.  Both tiers run on the pager's compute stream.
     """
 
-    def __init__(self, wl: S.Workload, resident: int, mode: str = "zero_copy",
-                 n_layers: int | None = None, distinct: int = 4, device="cuda"):
-        assert mode in ("zero_copy", "paged")
-        self.wl, self.mode = wl, mode
+    def __init__(self, wl: S.Workload, resident: int, n_layers: int | None = None,
+                 distinct: int = 4, device="cuda"):
+        self.wl = wl
         self.n_layers = wl.layers if n_layers is None else n_layers
         self.resident = max(0, min(resident, self.n_layers))
         self.device = torch.device(device)
         self.host = PagedStack(wl, n_layers=max(1, self.n_layers - self.resident),
                                distinct=distinct, device=device)
         self.dev = LayerStack(wl, layers=self.resident, device=device) if self.resident else None
-        self._host_views = [self.host._mats_in(b) for b in self.host.blobs]
         self.weight_bytes_per_layer = self.host.weight_bytes_per_layer
         self.io_bytes_per_layer = self.host.io_bytes_per_layer
 
     def bytes_per_step(self) -> int:
         return self.n_layers * (self.weight_bytes_per_layer + self.io_bytes_per_layer)
 
-    def _run_host_layer(self, j: int, stream):
-        """Layer j of tier B (0-based within the tier), read in place."""
-        mats = self._host_views[j % self.host.distinct]
-        xs, ys = self.host.x[j % self.host.distinct], self.host.y[j % self.host.distinct]
-        for g, names in enumerate(S.GROUPS):
-            api.gemv_mapped([mats[m] for m in names], xs[g][0], [y[0] for y in ys[g]],
-                            stream=stream)
-
     @property
     def stream(self):
-        """The stream a step runs on (the pager's compute stream when paged)."""
+        """The stream a step runs on (the pager's compute stream)."""
         return self.host.compute_stream
 
     def run_step(self):
@@ -324,10 +312,7 @@ class TieredStack:
         for l in range(self.resident):
             for g in range(len(S.GROUPS)):
                 self.dev.run_group(l, g, s)
-        if self.mode == "zero_copy":
-            for j in range(self.n_layers - self.resident):
-                self._run_host_layer(j, s)
-        elif self.n_layers > self.resident:
+        if self.n_layers > self.resident:
             self.host.run_step()
 
     def close(self):
