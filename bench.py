@@ -435,6 +435,7 @@ def measure_paged(wl_name: str, steps: int, warmup: int, device, distinct: int =
     from weight_only_quantized_dequant_gb300 import synthetic as S
 
     ps = ST.PagedStack(S.WORKLOADS[wl_name], distinct=distinct, device=device)
+    torch.cuda.synchronize(device)
     cs = ps.compute_stream
     for _ in range(warmup):
         ps.run_step()
@@ -535,6 +536,7 @@ def measure_tiered(wl_name: str, resident: int, steps: int, warmup: int, device,
     from weight_only_quantized_dequant_gb300 import synthetic as S
 
     ts = ST.TieredStack(S.WORKLOADS[wl_name], resident, distinct=distinct, device=device)
+    torch.cuda.synchronize(device)
     cs = ts.stream
     for _ in range(warmup):
         ts.run_step()

@@ -35,7 +35,9 @@ namespace {
 
 constexpr int kM = 128;         // weight rows per tile (MMA M)
 constexpr int kKT = 128;        // K elements per pipeline stage
-constexpr int kStages = 3;
+constexpr int kStages = 5;      // A stages in tensor memory (64 columns each)
+constexpr uint32_t kTmemCols = 512;    // accumulators in columns [0, 128), A above
+constexpr uint32_t kAColBase = 128;
 constexpr int kProducers = 256;  // 8 warps, two threads per weight row
 constexpr int kMmaWarp = kProducers / 32;     // warp 8 issues the MMAs
 constexpr int kCodeWarp = kMmaWarp + 1;       // warp 9 fills the code ring
@@ -43,7 +45,6 @@ constexpr int kLoadWarp = kMmaWarp + 2;       // warp 10 fills the activation ri
 constexpr int kThreadsTc = kProducers + 96;
 constexpr int kMaxBStages = 8;                // activation ring depth (smem permitting)
 constexpr size_t kBRingBytes = 80 * 1024;     // shared memory given to that ring
-constexpr int kABytes = kM * kKT * 2;         // 32 KiB per stage
 constexpr uint32_t kLBO = 128;   // bytes between core matrices along K
 constexpr uint32_t kSBO = 2048;  // bytes between 8-row groups (kKT/8 * 128)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
@@ -51,12 +52,12 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 // tensor copy each) in flight ahead of the fp16 A stages.
 template <bool INT4>
 struct RawRing {
-  static constexpr int DEPTH = INT4 ? 6 : 3;        // K tiles in flight
+  static constexpr int DEPTH = INT4 ? 8 : 4;        // K tiles in flight
   static constexpr int ROWB = INT4 ? kKT / 2 : kKT;  // packed bytes per row per K tile
   static constexpr int HB = ROWB / 2;                // bytes of one producer thread
   static constexpr int BYTES = DEPTH * kM * ROWB;
 };
-constexpr int kMaxRaw = 6;
+constexpr int kMaxRaw = 8;
 
 struct TcParams {
   CUtensorMap codes_map[QZ_MAX_GROUP];  // 2D: [rows][ld_codes bytes], box kM x ROWB
@@ -137,13 +138,28 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
+// D (TMEM) += A (TMEM: lane = row, 2 fp16 of K per column) * B (shared).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -200,8 +216,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int bBytes = tp.Np * kKT * 2;
   const int NB = tp.nbs;
-  uint8_t *a_st = base;                              // kStages * kABytes
-  uint8_t *b_st = a_st + kStages * kABytes;          // NB * bBytes
+  uint8_t *b_st = base;                              // NB * bBytes
   uint8_t *raw = b_st + NB * bBytes;                 // RawRing<INT4>::BYTES
   uint64_t *bars = reinterpret_cast<uint64_t *>(raw + RawRing<INT4>::BYTES);
   uint64_t *full = bars, *empty = bars + kStages;
@@ -225,7 +240,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   const int kt_begin = ktiles * rank / S, kt_end = ktiles * (rank + 1) / S;
   const bool has_out = kt_begin < (kt_end < tp.ko ? kt_end : tp.ko);
   const bool has_bg = (kt_begin > tp.ko ? kt_begin : tp.ko) < kt_end;
-  const uint32_t ncols = tp.Np <= 16 ? 32 : (tp.Np <= 32 ? 64 : 128);
+  const uint32_t ncols = kTmemCols;  // one CTA per SM (the host pads shared memory)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -255,17 +270,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
+  // TMEM columns: outlier accumulator [0, Np), background accumulator
+  // [Np, 2 Np), A stages from kAColBase.
   const uint32_t d_out = tmem, d_bg = tmem + (uint32_t)tp.Np;
 
   if (warp < kProducers / 32) {
     // ------------------------------------------------------ producers ----
-    // Two threads per weight row: thread (r, h) converts k slots
-    // [64 h, 64 h + 64) of row r in every stage.
-    const int r = tid >> 1, h = tid & 1;
+    // Warp w converts k slots [64 h, 64 h + 64) of the rows of TMEM lane
+    // quarter w % 4 (h = w / 4): thread = one row, its 64 fp16 codes go to
+    // 32 columns of its own TMEM lane with one tcgen05.st.
+    const int h = warp >> 2, r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int64_t grow = row0 + r;
     const bool live = grow < nrows;
     // Background (INT4) or all (INT8) K tiles arrive as packed codes in the
-    // raw ring (filled by the loader warp); each thread converts its bytes.
+    // raw ring (filled by the code loader warp); each thread converts its bytes.
     constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB, HB = RawRing<INT4>::HB;
     const int bgb = kt_begin > tp.ko ? kt_begin : tp.ko;  // first code tile
     const uint32_t raw_me = smem_u32(raw) + (uint32_t)r * RB + (uint32_t)h * HB;
@@ -274,14 +293,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     for (int kt = kt_begin; kt < kt_end; ++kt) {
       const int q = kt - kt_begin;  // position in this CTA's ring sequence
       const int s = q % kStages;
-      if (q >= kStages && !mbar_wait(smem_u32(&empty[s]), ((q / kStages) - 1) & 1, abort_flag))
-        break;
-      uint8_t *A = a_st + s * kABytes;
+      if (q >= kStages) {
+        if (!mbar_wait(smem_u32(&empty[s]), ((q / kStages) - 1) & 1, abort_flag)) break;
+        fence_after();  // the MMAs that read this A stage are complete
+      }
       const bool outl = kt < tp.ko;
-      const int c0 = h * (kKT / 2);  // first k slot of this thread
-      // --- A: 64 k slots of row r = 8 core-matrix rows of 16 bytes
+      uint32_t o[32];  // fp16 pairs of k slots 2j, 2j+1 of this thread's 64
       if (INT4 && outl) {
-        const int t0 = kt * kKT + c0;
+        const int t0 = kt * kKT + h * (kKT / 2);
         const uint4 *src = reinterpret_cast<const uint4 *>(p.w_out[m] + grow * p.ld_out[m]);
 #pragma unroll
         for (int kg = 0; kg < 8; ++kg) {
@@ -299,7 +318,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
               v = make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
-          *reinterpret_cast<uint4 *>(A + core_off(r, c0 + kg * 8)) = v;
+          o[4 * kg] = v.x;
+          o[4 * kg + 1] = v.y;
+          o[4 * kg + 2] = v.z;
+          o[4 * kg + 3] = v.w;
         }
       } else if (INT4) {
         const int i = kt - bgb;
@@ -318,19 +340,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
         for (int kg = 0; kg < 8; ++kg) {
           const uint32_t w = words[kg];
-          uint32_t h0 = ((w >> 0) & 0x000F000Fu) ^ bias;   // elements 0 and 4
-          uint32_t h1 = ((w >> 4) & 0x000F000Fu) ^ bias;   // 1 and 5
-          uint32_t h2 = ((w >> 8) & 0x000F000Fu) ^ bias;   // 2 and 6
-          uint32_t h3 = ((w >> 12) & 0x000F000Fu) ^ bias;  // 3 and 7
           // 1024 + (q+8) - 1032 = q, exact in fp16; elements past kb hold
-          // zero nibbles (q = 0) from the row padding, and zero rows past N
-          h0 = hsub2_u32(h0, bias);
-          h1 = hsub2_u32(h1, bias);
-          h2 = hsub2_u32(h2, bias);
-          h3 = hsub2_u32(h3, bias);
-          if (!live) h0 = h1 = h2 = h3 = 0;
-          // slot order 0,4,1,5,2,6,3,7
-          *reinterpret_cast<uint4 *>(A + core_off(r, c0 + kg * 8)) = make_uint4(h0, h1, h2, h3);
+          // zero nibbles (q = 0) from the row padding, rows past N zeros;
+          // slot order 0,4,1,5,2,6,3,7 (pairs (e0,e4), (e1,e5), ...)
+          o[4 * kg] = hsub2_u32(((w >> 0) & 0x000F000Fu) ^ bias, bias);
+          o[4 * kg + 1] = hsub2_u32(((w >> 4) & 0x000F000Fu) ^ bias, bias);
+          o[4 * kg + 2] = hsub2_u32(((w >> 8) & 0x000F000Fu) ^ bias, bias);
+          o[4 * kg + 3] = hsub2_u32(((w >> 12) & 0x000F000Fu) ^ bias, bias);
         }
       } else {
         const int i = kt - bgb;
@@ -345,25 +361,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         mbar_arrive(smem_u32(&rempty[i % DR]));  // the codes are in registers
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint4 v = vv[c];
-          const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
-                                 v.w ^ 0x80808080u};
-          uint32_t o[8];
+          const uint32_t w[4] = {vv[c].x ^ 0x80808080u, vv[c].y ^ 0x80808080u,
+                                 vv[c].z ^ 0x80808080u, vv[c].w ^ 0x80808080u};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             // 0x64 above each offset-binary byte: 1024 + (q + 128); minus 1152
-            o[2 * k] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4140), 0x64806480u);
-            o[2 * k + 1] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4342), 0x64806480u);
+            o[8 * c + 2 * k] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4140), 0x64806480u);
+            o[8 * c + 2 * k + 1] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4342), 0x64806480u);
           }
-          if (!live) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) o[k] = 0;
-          }
-          *reinterpret_cast<uint4 *>(A + core_off(r, c0 + 16 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4 *>(A + core_off(r, c0 + 16 * c + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (!live) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0;
+      }
+      tmem_st32(tmem + lane_base + kAColBase + (uint32_t)s * (kKT / 2) + (uint32_t)h * 32, o);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      fence_before();
       mbar_arrive(smem_u32(&full[s]));
     }
   } else if (warp == kMmaWarp) {
@@ -378,13 +392,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         if (!mbar_wait(smem_u32(&bfull[sb]), (q / NB) & 1, abort_flag)) break;
         fence_after();
         const bool outl = kt < tp.ko;
+        const uint32_t a0 = tmem + kAColBase + (uint32_t)s * (kKT / 2);
+        const uint32_t b0 = smem_u32(b_st + sb * bBytes);
         const uint32_t d = outl ? d_out : d_bg;
         const bool first = outl ? kt == kt_begin : kt == (kt_begin > tp.ko ? kt_begin : tp.ko);
-        const uint32_t a0 = smem_u32(a_st + s * kABytes), b0 = smem_u32(b_st + sb * bBytes);
 #pragma unroll
         for (int k16 = 0; k16 < kKT / 16; ++k16)
-          mma_f16(d, sdesc(a0 + k16 * 2 * kLBO), sdesc(b0 + k16 * 2 * kLBO), idesc,
-                  (first && k16 == 0) ? 0u : 1u);
+          mma_f16_ta(d, a0 + 8 * k16, sdesc(b0 + k16 * 2 * kLBO), idesc,
+                     (first && k16 == 0) ? 0u : 1u);
         mma_commit(smem_u32(&empty[s]));
         mma_commit(smem_u32(&bempty[sb]));
       }
@@ -474,7 +489,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 
   // ---------------------------------------------------------- epilogue ----
   // Each thread of warps 0-3 owns one row of the tile (its TMEM lane).
-  float *part = reinterpret_cast<float *>(a_st);  // S > 1: partials [Np][kM]
+  // S > 1: partials [Np][kM] in the activation ring (idle once every MMA is done)
+  float *part = reinterpret_cast<float *>(b_st);
   if (warp < 4) {
     const bool ok = mbar_wait(smem_u32(done), 0, abort_flag);
     fence_after();
@@ -602,9 +618,13 @@ static int tc_b_stages(int Np) {
 }
 
 size_t tc_smem_bytes(bool int4, int Np) {
-  return 1024 + (size_t)kStages * kABytes + (size_t)tc_b_stages(Np) * Np * kKT * 2 +
-         (int4 ? RawRing<true>::BYTES : RawRing<false>::BYTES) +
-         (2 * kStages + 2 * kMaxBStages + 2 * kMaxRaw + 1) * 8 + 16;
+  const size_t need = 1024 + (size_t)tc_b_stages(Np) * Np * kKT * 2 +
+                      (int4 ? RawRing<true>::BYTES : RawRing<false>::BYTES) +
+                      (2 * kStages + 2 * kMaxBStages + 2 * kMaxRaw + 1) * 8 + 16;
+  // more than half of an SM's shared memory, so that one CTA (which holds
+  // all 512 TMEM columns) runs per SM
+  const size_t one_per_sm = 120 * 1024;
+  return need > one_per_sm ? need : one_per_sm;
 }
 
 namespace {

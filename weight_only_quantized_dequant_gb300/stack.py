@@ -23,6 +23,22 @@ class Layer:
     perms: dict = field(default_factory=dict)
 
 
+def make_io(wl: S.Workload, layers: int, batch: int, device):
+    """Seeded inputs and output buffers of every group of `layers` layers:
+    x[layer][group] = [B, K] fp16, y[layer][group] = list of [B, N] fp16."""
+    xs_all, ys_all = [], []
+    for l in range(layers):
+        xs, ys = [], []
+        for g, names in enumerate(S.GROUPS):
+            K = wl.shape(names[0])[1]
+            xs.append(S.activation(batch, K, S.input_seed(wl, l, g), device=device))
+            ys.append([torch.empty((batch, wl.shape(m)[0]), dtype=torch.float16, device=device)
+                       for m in names])
+        xs_all.append(xs)
+        ys_all.append(ys)
+    return xs_all, ys_all
+
+
 class LayerStack:
     def __init__(self, wl: S.Workload, layers: int | None = None, batch: int = 1,
                  device="cuda", keep_fp16: bool = False):
@@ -73,18 +89,7 @@ class LayerStack:
         return layer
 
     def _alloc_io(self):
-        B, dev = self.batch, self.device
-        self.x = []   # [layer][group] -> [B, K] fp16
-        self.y = []   # [layer][group] -> list of [B, N] fp16
-        for l in range(self.n_layers):
-            xs, ys = [], []
-            for g, names in enumerate(S.GROUPS):
-                K = self.wl.shape(names[0])[1]
-                xs.append(S.activation(B, K, S.input_seed(self.wl, l, g), device=dev))
-                ys.append([torch.empty((B, self.wl.shape(m)[0]), dtype=torch.float16, device=dev)
-                           for m in names])
-            self.x.append(xs)
-            self.y.append(ys)
+        self.x, self.y = make_io(self.wl, self.n_layers, self.batch, self.device)
 
     # ------------------------------------------------------------- run ----
     def launches_per_step(self) -> int:
@@ -172,6 +177,68 @@ def _align16(n: int) -> int:
     return (n + 15) // 16 * 16
 
 
+def _pad_bytes(wl: S.Workload, m: str) -> int:
+    """Padding bytes of matrix m in its packed parts (not algorithmic bytes)."""
+    N, K = wl.shape(m)
+    if wl.fmt == "int8":
+        return N * (_align16(K) - K)
+    n_out = api.default_n_out(K)
+    ld_out, ld_q4 = api.int4o_layout(N, K, n_out)
+    return N * (2 * (ld_out - n_out) + ld_q4 - (K - n_out + 1) // 2)
+
+
+def _io_bytes(wl: S.Workload, batch: int) -> int:
+    """Input and output vectors of one layer (+ the permutation tables for INT4)."""
+    b = 0
+    for names in S.GROUPS:
+        K = wl.shape(names[0])[1]
+        b += 2 * batch * K + sum(2 * batch * wl.shape(m)[0] for m in names)
+        if wl.fmt == "int4o":
+            b += 4 * K
+    return b
+
+
+def blob_layout(wl: S.Workload):
+    """Layout of one packed layer in a contiguous blob (host pool, device
+    slot, pool file): a list of (key, part, offset, nbytes, dtype, shape),
+    16-byte aligned parts, and the blob size.  INT8: q and scale of every
+    matrix; INT4: the permutation of every input space, then w_out, q4 and
+    scale of every matrix."""
+    layout, off = [], 0
+
+    def add(key, part, dtype, shape):
+        nonlocal off
+        nb = int(torch.empty((), dtype=dtype).element_size())
+        for d in shape:
+            nb *= d
+        layout.append((key, part, off, nb, dtype, tuple(shape)))
+        off = _align16(off + nb)
+
+    if wl.fmt == "int8":
+        for m in S.MATS:
+            N, K = wl.shape(m)
+            add(m, "q", torch.int8, (N, _align16(K)))
+            add(m, "scale", torch.float32, (1,))
+    else:
+        for table, members in S.PERM_TABLES.items():
+            add(table, "perm", torch.int32, (wl.shape(members[0])[1],))
+        for m in S.MATS:
+            N, K = wl.shape(m)
+            ld_out, ld_q4 = api.int4o_layout(N, K, api.default_n_out(K))
+            add(m, "w_out", torch.float16, (N, ld_out))
+            add(m, "q4", torch.uint8, (N, ld_q4))
+            add(m, "scale", torch.float32, (N,))
+    return layout, _align16(off)
+
+
+def pack_layer(layer: "Layer", layout, blob: torch.Tensor) -> None:
+    """Copy a quantized layer's tensors into a host blob at their offsets."""
+    for key, part, o, nb, dt, shape in layout:
+        t = layer.perms[key] if part == "perm" else getattr(layer.mats[key], part)
+        assert t.dtype == dt and tuple(t.shape) == shape, (key, part, t.shape, shape)
+        blob[o:o + nb] = t.reshape(-1).view(torch.uint8).cpu()
+
+
 class PagedStack:
     """A stack whose packed layers live in pinned host memory and stream
     through the pager into two device slots ("Open Origin - ELG Stream
@@ -182,54 +249,41 @@ class PagedStack:
     """
 
     def __init__(self, wl: S.Workload, n_layers: int | None = None, distinct: int = 4,
-                 device="cuda"):
+                 device="cuda", blobs: list | None = None):
+        """blobs: packed host layers to stream instead of building them (for
+        example from a pool file, checkpoint.load_pool); pinned uint8 tensors
+        in the layout of blob_layout(wl)."""
         self.wl = wl
         self.n_layers = wl.layers if n_layers is None else n_layers
-        self.distinct = min(distinct, self.n_layers)
         self.device = torch.device(device)
-        src = LayerStack(wl, layers=self.distinct, device=device)
-        self.x, self.y = src.x, src.y
         # one blob layout shared by every layer (same shapes)
-        self.layout = []  # (kind, name, offset, nbytes, dtype, shape)
-        off = 0
-        lay0 = src.layers[0]
-        if wl.fmt == "int8":
-            for m in S.MATS:
-                w = lay0.mats[m]
-                for part, t in (("q", w.q), ("scale", w.scale)):
-                    self.layout.append((m, part, off, t.numel() * t.element_size(), t.dtype,
-                                        tuple(t.shape)))
-                    off = _align16(off + t.numel() * t.element_size())
+        self.layout, self.blob_bytes = blob_layout(wl)
+        if blobs is None:
+            self.distinct = min(distinct, self.n_layers)
+            src = LayerStack(wl, layers=self.distinct, device=device)
+            self.blobs = []
+            for l in range(self.distinct):
+                blob = torch.zeros((self.blob_bytes,), dtype=torch.uint8).pin_memory()
+                pack_layer(src.layers[l], self.layout, blob)
+                self.blobs.append(blob)
+            del src
         else:
-            for table in S.PERM_TABLES:
-                t = lay0.perms[table]
-                self.layout.append((table, "perm", off, t.numel() * 4, t.dtype, tuple(t.shape)))
-                off = _align16(off + t.numel() * 4)
-            for m in S.MATS:
-                w = lay0.mats[m]
-                for part, t in (("w_out", w.w_out), ("q4", w.q4), ("scale", w.scale)):
-                    nb = t.numel() * t.element_size()
-                    self.layout.append((m, part, off, nb, t.dtype, tuple(t.shape)))
-                    off = _align16(off + nb)
-        self.blob_bytes = _align16(off)
-        self.blobs = []
-        for l in range(self.distinct):
-            blob = torch.zeros((self.blob_bytes,), dtype=torch.uint8).pin_memory()
-            lay = src.layers[l]
-            for key, part, o, nb, dt, shape in self.layout:
-                if part == "perm":
-                    t = lay.perms[key]
-                else:
-                    t = getattr(lay.mats[key], part)
-                blob[o:o + nb] = t.reshape(-1).view(torch.uint8).cpu()
-            self.blobs.append(blob)
-        self.weight_bytes_per_layer = src.weight_bytes_per_layer()
-        self.io_bytes_per_layer = src.io_bytes_per_layer()
-        del src
+            assert all(b.numel() == self.blob_bytes and b.is_pinned() for b in blobs)
+            self.distinct = min(len(blobs), self.n_layers)
+            self.blobs = list(blobs[:self.distinct])
+        self.x, self.y = make_io(wl, self.distinct, 1, self.device)
+        self.weight_bytes_per_layer = sum(
+            nb for key, part, o, nb, dt, shape in self.layout if part != "perm") - sum(
+            _pad_bytes(wl, m) for m in S.MATS)
+        self.io_bytes_per_layer = _io_bytes(wl, 1)
         self.slots = [torch.empty((self.blob_bytes,), dtype=torch.uint8, device=self.device)
                       for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(device=self.device)
         self.compute_stream = torch.cuda.Stream(device=self.device)
+        # the inputs were generated on the current stream: order both streams after it
+        cur = torch.cuda.current_stream(self.device)
+        self.copy_stream.wait_stream(cur)
+        self.compute_stream.wait_stream(cur)
         hosts = [self.blobs[l % self.distinct] for l in range(self.n_layers)]
         self.pager = api.Pager(hosts, self.slots, self.copy_stream, self.compute_stream)
         self._views = [self._mats_in(slot) for slot in self.slots]
@@ -296,6 +350,9 @@ class TieredStack:
         self.host = PagedStack(wl, n_layers=max(1, self.n_layers - self.resident),
                                distinct=distinct, device=device)
         self.dev = LayerStack(wl, layers=self.resident, device=device) if self.resident else None
+        # the resident layers were quantized on the current stream; the step
+        # runs on the pager's compute stream, which must not start before them
+        self.host.compute_stream.wait_stream(torch.cuda.current_stream(self.device))
         self.weight_bytes_per_layer = self.host.weight_bytes_per_layer
         self.io_bytes_per_layer = self.host.io_bytes_per_layer
 
