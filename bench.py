@@ -5,7 +5,7 @@ layer), replayed from a CUDA graph.  The stack (several GB) is far larger
 than the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--extra] [--head] [--paged] [--tiered]
+                  [--impl ours|reference] [--extra] [--head] [--paged] [--tiered] [--stream-quant]
                   [--no-cpu]
 
 Prints ONE JSON line.  Under torchrun (N > 1) every rank runs an independent
@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--tiered", action="store_true",
                     help="also time the 70B stack with its first 40 (60) layers in HBM and "
                          "the rest streamed from pinned host memory")
+    ap.add_argument("--stream-quant", action="store_true",
+                    help="also time the streaming quantizer (checkpoint file -> pool file)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch without programmatic dependent launch")
     ap.add_argument("--batch", type=int, default=1,
@@ -560,6 +562,46 @@ def measure_tiered(wl_name: str, resident: int, steps: int, warmup: int, device,
     return out
 
 
+def measure_stream_quant(wl_name: str, layers: int, device) -> dict:
+    """Offline side: a synthetic checkpoint of `layers` layers written to a
+    temporary directory, quantized layer by layer into a pool file (timed, with
+    the host memory it held), then the pool read back into pinned memory."""
+    import resource
+    import shutil
+
+    import torch
+
+    from weight_only_quantized_dequant_gb300 import checkpoint as C
+    from weight_only_quantized_dequant_gb300 import synthetic as S
+
+    wl = S.WORKLOADS[wl_name]
+    tmp = tempfile.mkdtemp(prefix="qz_ckpt_")
+    try:
+        ck, pool = os.path.join(tmp, "w.safetensors"), os.path.join(tmp, "w.qz")
+        t = time.perf_counter()
+        size = C.write_synthetic_checkpoint(ck, wl, layers, device=device)
+        t_write = time.perf_counter() - t
+        rss0 = resource.getrusage(resource.RUSAGE_SELF).ru_maxrss
+        torch.cuda.synchronize(device)
+        t = time.perf_counter()
+        st = C.quantize_stream(ck, wl, layers, pool, device=device)
+        t_q = time.perf_counter() - t
+        rss1 = resource.getrusage(resource.RUSAGE_SELF).ru_maxrss
+        t = time.perf_counter()
+        hdr, blobs = C.load_pool(pool)
+        t_load = time.perf_counter() - t
+        return {"workload": wl_name, "layers": layers, "checkpoint_gb": round(size / 1e9, 3),
+                "write_s": round(t_write, 2), "quantize_s": round(t_q, 2),
+                "quantize_gbs": round(st["checkpoint_bytes"] / t_q / 1e9, 2),
+                "host_buffers_mb": round(st["host_buffer_bytes"] / 2**20, 1),
+                "peak_rss_growth_mb": round(max(0, rss1 - rss0) / 1024, 1),
+                "pool_gb": round(st["pool_bytes"] / 1e9, 3),
+                "pool_load_gbs": round(st["pool_bytes"] / t_load / 1e9, 2),
+                "note": "checkpoint freshly written: its pages are likely in the page cache"}
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+
+
 def main():
     a = parse()
     if a.impl == "reference":
@@ -615,6 +657,10 @@ def main():
             extra[f"{wl70}_tiered_{res}"] = measure_tiered(wl70, res, max(2, a.steps // 10), 1,
                                                            device)
         extra["link_probe_gbs"] = round(h2d_probe_gbs(device), 1)
+
+    if a.stream_quant and rank == 0:
+        extra["stream_quant_llama32_3b"] = measure_stream_quant("llama32_3b_int4o", 4, device)
+        extra["stream_quant_gemma2_9b"] = measure_stream_quant("gemma2_9b_int8", 2, device)
 
     if a.paged and rank == 0:
         for name in ("llama_70b_int4o", "gemma2_9b_int8"):
