@@ -49,6 +49,8 @@ def parse():
                          "the rest streamed from pinned host memory")
     ap.add_argument("--stream-quant", action="store_true",
                     help="also time the streaming quantizer (checkpoint file -> pool file)")
+    ap.add_argument("--fused", action="store_true",
+                    help="one sequence launch per layer (the four products) instead of four")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch without programmatic dependent launch")
     ap.add_argument("--batch", type=int, default=1,
@@ -257,7 +259,7 @@ def copy_probe_gbs(device) -> float:
 
 
 def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
-            clocks=False, device=None, layers=None, overlap=True):
+            clocks=False, device=None, layers=None, overlap=True, fused=False):
     """Build the stack, capture one step, time it.  Returns a dict."""
     import torch
 
@@ -266,7 +268,7 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
 
     wl = S.WORKLOADS[wl_name]
     t_build = time.perf_counter()
-    st = ST.LayerStack(wl, layers=layers, batch=batch, device=device)
+    st = ST.LayerStack(wl, layers=layers, batch=batch, device=device, fused=fused)
     torch.cuda.synchronize()
     t_build = time.perf_counter() - t_build
 
@@ -306,6 +308,13 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
 
     def step(stream, events):
         for l in range(st.n_layers):
+            if st.fused:  # one launch per layer: that launch is the timed kernel
+                if events:
+                    ev[l][0].record(stream)
+                st.run_layer_fused(l, stream)
+                if events:
+                    ev[l][1].record(stream)
+                continue
             for g in range(len(S.GROUPS)):
                 if events and g == DOMINANT_GROUP:
                     ev[l][0].record(stream)
@@ -391,6 +400,9 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
     dom_bytes += 2 * batch * K_dom + sum(2 * batch * wl.shape(m)[0] for m in dom_names)
     if wl.fmt == "int4o":
         dom_bytes += 4 * K_dom
+    if st.fused:
+        dom_names = ("layer",)
+        dom_bytes = st.weight_bytes_per_layer() + st.io_bytes_per_layer()
     out = {
         "workload": wl_name, "batch": batch, "layers": st.n_layers,
         "bytes_per_step": st.bytes_per_step(),
@@ -629,7 +641,7 @@ def main():
         dist_ctx.barrier()
 
     r = measure(a.workload, a.batch, a.steps, a.warmup, dist_ctx, clocks=(rank == 0), device=device,
-                layers=a.layers, overlap=not a.no_overlap)
+                layers=a.layers, overlap=not a.no_overlap, fused=a.fused)
     ms_all = r["ms_per_step"]
     e2e_all = r["e2e_ms"]
     if dist_ctx is not None:
@@ -687,7 +699,8 @@ def main():
         "config": {"workload": a.workload,
                    "format": "int8 per-tensor" if "int8" in a.workload else "int4 outlier-aware",
                    "batch": a.batch,
-                   "layers": r["layers"], "launches_per_layer": 4, "graph": True,
+                   "layers": r["layers"], "launches_per_layer": 1 if a.fused else 4,
+                   "graph": True,
                    "overlap": not a.no_overlap,
                    "l2": f"inputs larger than L2 ({r['stack_gb']:.2f} GB stack > 129 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -699,7 +712,8 @@ def main():
                      "traffic": profiled_traffic(
                          f"gemv_{a.workload}_gateup.md",
                          "weight_only_quantized_dequant_gb300/csrc/k_gemv.cu"),
-                     "kernel": f"gemv ({dom['group']} grouped launch)",
+                     "kernel": ("gemv sequence (one layer per launch)" if a.fused
+                                else f"gemv ({dom['group']} grouped launch)"),
                      "bytes_per_launch": dom["bytes_per_launch"],
                      "avg_launch_us": round(dom["avg_ms"] * 1e3, 3),
                      "peak_kind": peak_src},

@@ -87,6 +87,8 @@ qz_status qz_device_error(int *code, int clear);
 #define QZ_MAX_BATCH 64
 /* Largest number of matrices in one grouped launch. */
 #define QZ_MAX_GROUP 4
+/* Largest number of products in one sequence call (qz_gemv_*_sequence). */
+#define QZ_MAX_SEQ 4
 
 /* ======================================================================
  * INT8, one scale per tensor  [ELG "Technical Architecture > INT8
@@ -291,6 +293,35 @@ qz_status qz_gemm_int4_outlier_grouped(const qz_int4o_weight *ws, int n, int64_t
                                        qz_half *const *Ys, const int64_t *ldys,
                                        void *workspace, size_t workspace_bytes,
                                        qz_stream s);
+
+/* ======================================================================
+ * Dependent products in one launch  [no counterpart on the pages: a decoder
+ * layer's four products (q,k,v; o; gate,up; down) run back to back, each
+ * reading the previous one's result through the layer glue, so one launch
+ * per layer replaces four]
+ *
+ * n batch-1 grouped products (1 <= n <= QZ_MAX_SEQ) run in order in one
+ * launch: product k multiplies the next counts[k] matrices of ws (equal K;
+ * for INT4 also equal n_out and perm, as in the grouped calls) with x[k] and
+ * stores them to the next counts[k] entries of ys.  Product k reads x[k] only
+ * after every output of products 0..k-1 has been stored, so x[k] may be one
+ * of those outputs.  Results equal the separate grouped calls bit for bit.
+ *   ws, ys: host arrays of sum(counts) entries; counts, x: host arrays of n.
+ *   sync: device uint32, 4-byte aligned, 0 before the first call; every call
+ *   that completes leaves it 0.  Calls that can be in flight at the same time
+ *   (for example consecutive calls under qz_set_overlap) need different
+ *   words; after a device error (qz_device_error) it must be zeroed again.
+ * The launch holds one CTA on every SM and its CTAs wait on one another
+ * (bounded in time, reported through qz_device_error), so it must not share
+ * the GPU with work that keeps SMs busy indefinitely.
+ * ====================================================================== */
+qz_status qz_gemv_int8_sequence(const qz_int8_weight *ws, const int *counts, int n,
+                                const qz_half *const *x, qz_half *const *ys,
+                                uint32_t *sync, qz_stream s);
+qz_status qz_gemv_int4_outlier_sequence(const qz_int4o_weight *ws, const int *counts,
+                                        int n, const qz_half *const *x,
+                                        qz_half *const *ys, uint32_t *sync,
+                                        qz_stream s);
 
 /* ======================================================================
  * Layer pager  [ELG "Key Features" 2 (prefetch, transfer, reconstruct,

@@ -175,6 +175,27 @@ def test_grouped_gemm_validation(lib):
     assert lib.qz_gemm_int4_outlier_grouped(w4, 2, 3, P, 64, ys, ld, None, 0, None) == INVAL
 
 
+def test_sequence_validation(lib):
+    ws = (_lib.Int8Weight * 6)(*[_w8() for _ in range(6)])
+    ys = (ctypes.c_void_p * 6)(*[P] * 6)
+    xs = (ctypes.c_void_p * 5)(*[P] * 5)
+    F = lib.qz_gemv_int8_sequence
+    one = (ctypes.c_int * 5)(1, 1, 1, 1, 1)
+    assert F(ws, one, 5, xs, ys, P, None) == UNSUP              # more than QZ_MAX_SEQ
+    assert F(ws, one, 0, xs, ys, P, None) == INVAL
+    assert F(ws, one, 2, xs, ys, None, None) == INVAL           # no barrier word
+    assert F(ws, one, 2, xs, ys, P + 2, None) == ALIGN          # barrier word 4-byte aligned
+    zero = (ctypes.c_int * 2)(1, 0)
+    assert F(ws, zero, 2, xs, ys, P, None) == INVAL             # empty product
+    five = (ctypes.c_int * 1)(5)
+    assert F(ws, five, 1, xs, ys, P, None) == UNSUP              # more than QZ_MAX_GROUP
+    bad = (_lib.Int8Weight * 2)(_w8(K=32), _w8(K=48, ldq=48))
+    two = (ctypes.c_int * 1)(2)
+    assert F(bad, two, 1, xs, ys, P, None) == INVAL              # K differs inside a product
+    w4 = (_lib.Int4oWeight * 2)(_w4(), _w4(perm=P + 16))
+    assert lib.qz_gemv_int4_outlier_sequence(w4, two, 1, xs, ys, P, None) == INVAL
+
+
 def _w4(N=8, K=64, n_out=1, perm=P, w_out=P, q4=P, scale=P, ld_out=None, ld_q4=None):
     lo, lq = O.int4o_layout(K, min(n_out, K))
     return _lib.Int4oWeight(N, K, n_out, lo if ld_out is None else ld_out,

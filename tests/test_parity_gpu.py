@@ -411,3 +411,79 @@ def test_pager_streams_layers_and_reports_injected_failure():
     assert ei.value.name == "QZ_ERR_IO"
     pager.close()
     torch.cuda.synchronize()
+
+
+# ----------------------------------------------------- sequence launches ----
+@pytest.mark.parametrize("fmt", ["int8", "int4o"])
+def test_sequence_chain_matches_separate_calls(fmt):
+    """Three dependent products in one launch, each reading the previous
+    one's output: same bits as the grouped calls made one after the other;
+    the first product against the oracle; the barrier word left at zero and
+    reusable."""
+    K0, N0, N1, N2 = 3072, 1536, 1024, 700
+    shapes = [(N0, K0), (N1, N0), (N2, N1), (N2 + 64, N1)]
+    Ws = [S.weight(n, k, 9900 + i, device=DEV) for i, (n, k) in enumerate(shapes)]
+    x0 = S.activation(1, K0, 9910, device=DEV)[0]
+    if fmt == "int8":
+        ws = [qz().quantize_int8(W) for W in Ws]
+        grouped = qz().gemv_int8_grouped
+    else:
+        ws = []
+        perms = {}
+        for i, W in enumerate(Ws):
+            K = W.shape[1]
+            n_out = O.default_n_out(K)
+            key = (K, i >= 2)              # products 2 and 3 share one permutation
+            if key not in perms:
+                colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+                for j in ([2, 3] if i >= 2 else [i]):
+                    qz().saliency_accumulate(Ws[j], colsum)
+                perms[key] = qz().select_outliers(colsum, S.x_profile(K, n_out, 9920 + i,
+                                                                      device=DEV), n_out)
+            ws.append(qz().quantize_int4_outlier(W, perms[key], n_out))
+        grouped = qz().gemv_int4_outlier_grouped
+    # chain: y0 = W0 x0; y1 = W1 y0; (y2, y3) = (W2, W3) y1
+    y0 = torch.empty((N0,), dtype=torch.float16, device=DEV)
+    y1 = torch.empty((N1,), dtype=torch.float16, device=DEV)
+    y2 = torch.empty((N2,), dtype=torch.float16, device=DEV)
+    y3 = torch.empty((N2 + 64,), dtype=torch.float16, device=DEV)
+    sync = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    for _ in range(2):                      # the second call reuses the barrier word
+        qz().gemv_sequence([[ws[0]], [ws[1]], [ws[2], ws[3]]], [x0, y0, y1],
+                           [[y0], [y1], [y2, y3]], sync=sync)
+        assert qz().device_error() == 0
+        assert int(sync.item()) == 0
+    r0 = grouped([ws[0]], x0)[0]
+    r1 = grouped([ws[1]], r0)[0]
+    r2, r3 = grouped([ws[2], ws[3]], r1)
+    for a, b in ((y0, r0), (y1, r1), (y2, r2), (y3, r3)):
+        assert torch.equal(a, b)
+    Wn = Ws[0].cpu().numpy()
+    if fmt == "int8":
+        q_ref, s_ref = O.int8_quantize(Wn)
+        y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, x0.cpu().numpy()[None])
+    else:
+        pn = ws[0].perm.cpu().numpy()
+        wo, q4, s = O.int4o_quantize(Wn, pn, ws[0].n_out)
+        y_ref, a_ref = O.int4o_product_ref(wo, q4, s, pn, ws[0].n_out, K0, x0.cpu().numpy()[None])
+    assert_close(y0, y_ref[0], a_ref[0], f"sequence {fmt} product 0")
+
+
+def test_fused_stack_graph_matches_per_group_launches():
+    """A decode step of two Gemma layers captured as one sequence launch per
+    layer (with programmatic overlap) gives the bits of the four-launch step."""
+    from weight_only_quantized_dequant_gb300 import stack as ST
+    wl = S.WORKLOADS["gemma2_9b_int8"]
+    a = ST.LayerStack(wl, layers=2)
+    b = ST.LayerStack(wl, layers=2, fused=True)
+    a.run_step()
+    g = b.capture(overlap=True)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert qz().device_error() == 0
+    assert not b.sync.any()
+    for l in range(2):
+        for ya, yb in zip(a.y[l], b.y[l]):
+            for u, v in zip(ya, yb):
+                assert torch.equal(u, v)

@@ -77,6 +77,11 @@ _SIGS = {
     "qz_gemm_int4_outlier_grouped": (_S, [POINTER(Int4oWeight), c_int, c_int64, c_void_p,
                                           c_int64, POINTER(c_void_p), POINTER(c_int64),
                                           c_void_p, c_size_t, c_void_p]),
+    "qz_gemv_int8_sequence": (_S, [POINTER(Int8Weight), POINTER(c_int), c_int, POINTER(c_void_p),
+                                   POINTER(c_void_p), c_void_p, c_void_p]),
+    "qz_gemv_int4_outlier_sequence": (_S, [POINTER(Int4oWeight), POINTER(c_int), c_int,
+                                           POINTER(c_void_p), POINTER(c_void_p), c_void_p,
+                                           c_void_p]),
     "qz_pager_create": (_S, [POINTER(c_void_p), POINTER(c_size_t), c_int, c_void_p, c_void_p,
                              c_size_t, c_void_p, c_void_p, POINTER(c_void_p)]),
     "qz_pager_acquire": (_S, [c_void_p, c_int, POINTER(c_void_p)]),

@@ -330,6 +330,27 @@ def gemm_int4_outlier_grouped(ws, X: torch.Tensor, Ys=None, stream=None, workspa
                          workspace, ws[0].n_out)
 
 
+def gemv_sequence(groups, xs, ys=None, sync: torch.Tensor | None = None, stream=None):
+    """Dependent batch-1 grouped products in one launch: product k multiplies
+    the matrices groups[k] with xs[k] into ys[k]; xs[k] may be an output of an
+    earlier product.  sync: a zeroed device int32 word (left zero); concurrent
+    calls need different words.  Returns ys (list of lists)."""
+    _need_cuda(*xs)
+    n = len(groups)
+    ys = [[_vec_out(xs[k], w.N) for w in g] for k, g in enumerate(groups)] if ys is None else ys
+    flat = [w for g in groups for w in g]
+    int8 = isinstance(flat[0], Int8Matrix)
+    arr = ((Int8Weight if int8 else Int4oWeight) * len(flat))(*[w.struct() for w in flat])
+    counts = (ctypes.c_int * n)(*[len(g) for g in groups])
+    xp = (ctypes.c_void_p * n)(*[x.data_ptr() for x in xs])
+    yp = (ctypes.c_void_p * len(flat))(*[y.data_ptr() for yy in ys for y in yy])
+    if sync is None:
+        sync = torch.zeros((1,), dtype=torch.int32, device=xs[0].device)
+    fn = "qz_gemv_int8_sequence" if int8 else "qz_gemv_int4_outlier_sequence"
+    _lib.call(fn, arr, counts, n, xp, yp, sync.data_ptr(), _stream(stream))
+    return ys
+
+
 # ----------------------------------------------------------------- Pager ---
 class Pager:
     """Double-buffered host->device layer streaming (qz_pager_*).

@@ -514,6 +514,322 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Sequence kernel: up to kMaxSeq dependent batch-1 products in one launch.
+// Product k reads its x only after every CTA has stored its rows of products
+// 0..k-1 (a grid-wide barrier on a counter in caller memory), so x of k may be
+// the y of an earlier product.  The weight ring is not drained at the
+// barriers: the producers run into the next product's rows (weights are
+// static), and thread 0 pulls the next product's first rows into L2 while the
+// current one is computed.  Same per-row arithmetic as gemv_kernel<INT4, 1>.
+// The grid must be co-resident (one CTA per SM; every wait is bounded).
+// ---------------------------------------------------------------------------
+template <bool INT4>
+__global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_constant__ SeqParams sp) {
+  constexpr int B = 1;
+  constexpr int R = Ring<1>::R, NS = Ring<1>::NS, kRPS = Ring<1>::RPS;
+  constexpr uint32_t kStageRow = Ring<1>::STAGE_ROW;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  constexpr int EPC = INT4 ? 32 : 16;      // fp16 inputs per code chunk
+  constexpr uint32_t CS = EPC * 2 + 16;    // staged bytes per chunk (padded by 16)
+  constexpr uint32_t kRound = 32u * CS;    // staged bytes per round of 32 chunks
+  constexpr int stride = kWarps * R;
+  __half *xs = reinterpret_cast<__half *>(smem_raw);
+  uint8_t *ring = smem_raw + sp.xs_bytes;                       // 128-aligned by the host
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)kWarps * NS * R * kStageRow);
+  int *abort_flag = reinterpret_cast<int *>(bars + kWarps * NS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = (int)gridDim.x;
+
+  // This warp's share of product k: rows [rlo, rhi) of the CTA, groups of R
+  // rows starting at `first`, P groups of SPR stages.
+  struct Work {
+    int rlo, rhi, first, P, SPR, Jw;
+  };
+  auto plan = [&](int k) {
+    const GemvParams &p = sp.t[k];
+    Work w;
+    w.rlo = (int)(p.total_rows * blockIdx.x / G);
+    w.rhi = (int)(p.total_rows * (blockIdx.x + 1) / G);
+    w.first = w.rlo + warp * R;
+    w.P = w.first < w.rhi ? (w.rhi - w.first + stride - 1) / stride : 0;
+    w.Jw = (p.cpr + 31) >> 5;
+    w.SPR = (w.Jw + kRPS - 1) / kRPS;
+    return w;
+  };
+  auto prefetch_rows = [&](int k) {  // the first 64 KiB of this CTA's rows of product k
+    const GemvParams &p = sp.t[k];
+    const int64_t r0 = p.total_rows * blockIdx.x / G, r1 = p.total_rows * (blockIdx.x + 1) / G;
+    int64_t budget = kPrefetchBytes, r = r0;
+    for (int m = 0; m < p.n_mats && budget > 0 && r < r1; ++m) {
+      const int64_t m_lo = m ? p.row_end[m - 1] : 0, m_hi = p.row_end[m];
+      if (r >= m_hi) continue;
+      const int64_t e = r1 < m_hi ? r1 : m_hi;
+      int64_t bytes = (e - r) * p.ld_codes[m];
+      if (bytes > budget) bytes = budget;
+      bytes &= ~(int64_t)15;
+      if (bytes > 0) prefetch_l2(p.codes[m] + (r - m_lo) * p.ld_codes[m], (uint32_t)bytes);
+      budget -= bytes;
+      r = e;
+    }
+  };
+  if (threadIdx.x == 0) {
+    prefetch_rows(0);
+    *abort_flag = 0;
+  }
+  if (lane == 0) {
+    for (int st = 0; st < NS; ++st)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[warp * NS + st]))
+                   : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const uint32_t ring_w = smem_u32(ring) + (uint32_t)warp * NS * R * kStageRow;
+  const uint32_t bar_w = smem_u32(&bars[warp * NS]);
+
+  // Producer state, across products: product pk, row group pg, stage psj,
+  // ring slot pst, stages left in product pk.
+  int pk = 0, pg = 0, psj = 0, pst = 0, pleft = 0;
+  Work pw = plan(0);
+  Bounds pbd;
+  const uint8_t *pptr[R];
+  auto prow_setup = [&]() {
+    const GemvParams &p = sp.t[pk];
+    const int rb = pw.first + pg * stride;
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+      const int rc = rb + rr < pw.rhi ? rb + rr : pw.rhi - 1;  // past the end: alias a valid row
+      int m, i;
+      locate(pbd, rc, m, i);
+      pptr[rr] = p.codes[m] + (int64_t)i * p.ld_codes[m];
+    }
+  };
+  auto enter = [&](int k) {  // producer moves to the first product >= k with stages for it
+    for (pk = k; pk < sp.n; ++pk) {
+      pw = plan(pk);
+      if (pw.P > 0) break;
+    }
+    pg = psj = 0;
+    pleft = pk < sp.n ? pw.P * pw.SPR : 0;
+    if (pleft > 0) {
+#pragma unroll
+      for (int t = 0; t < QZ_MAX_GROUP; ++t) pbd.end[t] = (int)sp.t[pk].row_end[t];
+      pbd.n = sp.t[pk].n_mats;
+      prow_setup();
+    }
+  };
+  auto issue_next = [&]() {
+    if (lane == 0) {
+      const int cpr = sp.t[pk].cpr;
+      const int j0 = psj * kRPS;
+      const int span = cpr - 32 * j0 < 32 * kRPS ? cpr - 32 * j0 : 32 * kRPS;  // chunks
+      const uint32_t bytes = (uint32_t)span * 16u;
+      const uint32_t bar = bar_w + pst * 8;
+      asm volatile(
+          "{\n\t.reg .b64 t;\n\t"
+          "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
+          "r"(bytes * R)
+          : "memory");
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) {
+        if (bytes == 0) break;  // no codes: the arrival alone completes the stage
+        const uint32_t dst = ring_w + (uint32_t)(pst * R + rr) * kStageRow;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+                "r"(dst),
+            "l"(pptr[rr] + j0 * kRoundBytes), "r"(bytes), "r"(bar)
+            : "memory");
+      }
+    }
+    pst = pst + 1 == NS ? 0 : pst + 1;
+    if (--pleft == 0) {
+      enter(pk + 1);
+    } else if (++psj == pw.SPR) {
+      psj = 0;
+      ++pg;
+      prow_setup();
+    }
+  };
+  auto any_left = [&]() { return pk < sp.n && pleft > 0; };
+
+  enter(0);
+  for (int it = 0; it < NS - 1 && any_left(); ++it) issue_next();
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  const __half hzero = __ushort_as_half((unsigned short)0);
+  Acc4 acc[R][B];
+#pragma unroll
+  for (int rr = 0; rr < R; ++rr) acc[rr][0][0] = acc[rr][0][1] = acc[rr][0][2] = acc[rr][0][3] = 0.f;
+  bool ok = true;
+  int cst = 0;            // consumer ring slot
+  uint32_t cphase = 0;    // parity of the slot's current use
+
+  for (int k = 0; k < sp.n; ++k) {
+    const GemvParams &p = sp.t[k];
+    const Work w = plan(k);
+    const int cpr = p.cpr;
+    const int staged = (w.Jw > 0 ? w.Jw : 1) * 32;
+    const uint32_t bstride = (uint32_t)staged * CS;
+    __half *xo = reinterpret_cast<__half *>(smem_raw + bstride);
+    // ---- wait until every CTA has stored its rows of products < k ----------
+    if (k > 0) {
+      __syncthreads();  // this CTA's stores of product k-1 precede the arrival
+      if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(sp.sync, 1u);
+        const unsigned target = (unsigned)(k * G);
+        const unsigned long long t0 = gtimer();
+        unsigned v = 0;
+        for (;;) {
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(sp.sync) : "memory");
+          if (v >= target) break;
+          if (gtimer() - t0 > kWaitNs) {
+            atomicExch(&g_gemv_error, 1);
+            *(volatile int *)abort_flag = 1;
+            break;
+          }
+        }
+        if (k + 1 < sp.n) prefetch_rows(k + 1);
+      }
+      __syncthreads();
+      if (*(volatile int *)abort_flag) ok = false;
+    } else if (threadIdx.x == 0 && sp.n > 1) {
+      prefetch_rows(1);
+    }
+    // ---- stage x of product k (L1 bypassed: it may be an earlier product's y)
+    const int elems = staged * EPC;
+    const __half *xb = p.x;
+    if (ok) {
+#pragma unroll 1
+      for (int e0 = threadIdx.x * 8; e0 < elems; e0 += kThreads * 8) {
+        uint32_t h[4];
+        __half v[8];
+        if constexpr (INT4) {
+          int idx[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) idx[q] = e0 + q < p.kb ? __ldg(p.perm + p.n_out + e0 + q) : -1;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = idx[q] >= 0 ? __ldcg(xb + idx[q]) : hzero;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = e0 + q < p.kb ? __ldcg(xb + e0 + q) : hzero;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          h[q] = (uint32_t)__half_as_ushort(v[2 * q]) | ((uint32_t)__half_as_ushort(v[2 * q + 1]) << 16);
+        *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(xs) + (e0 / EPC) * CS + (e0 % EPC) * 2) =
+            make_uint4(h[0], h[1], h[2], h[3]);
+      }
+      if constexpr (INT4) {
+#pragma unroll 1
+        for (int e = threadIdx.x; e < p.ocpr * 8; e += kThreads)
+          xo[e] = e < p.n_out ? __ldcg(xb + __ldg(p.perm + e)) : hzero;
+      }
+    }
+    __syncthreads();
+
+    Bounds bd;
+#pragma unroll
+    for (int t = 0; t < QZ_MAX_GROUP; ++t) bd.end[t] = (int)p.row_end[t];
+    bd.n = p.n_mats;
+    const uint32_t lane_off = (uint32_t)lane * CS;
+    for (int g = 0; g < w.P; ++g) {
+      const int rb = w.first + g * stride;
+      int mrow[R], irow[R];
+      float srow[R];
+      bool live[R];
+      uint4 ov[R];
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) {
+        live[rr] = rb + rr < w.rhi;
+        locate(bd, live[rr] ? rb + rr : w.rhi - 1, mrow[rr], irow[rr]);
+        srow[rr] = INT4 ? __ldg(p.scale[mrow[rr]] + irow[rr]) : __ldg(p.scale[mrow[rr]]);
+        ov[rr] = make_uint4(0, 0, 0, 0);
+        if (INT4 && lane < p.ocpr)
+          ov[rr] = ld_stream(reinterpret_cast<const uint4 *>(
+                                 p.w_out[mrow[rr]] + (int64_t)irow[rr] * p.ld_out[mrow[rr]]) +
+                             lane);
+      }
+      for (int sj = 0; sj < w.SPR; ++sj) {
+        if (ok && any_left()) {
+          if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue_next();
+        }
+        if (ok) ok = mbar_wait(bar_w + cst * 8, cphase);
+        if (ok) {
+          const uint32_t sbase = ring_w + (uint32_t)cst * R * kStageRow + lane * 16;
+#pragma unroll
+          for (int u = 0; u < kRPS; ++u) {
+            const int j = sj * kRPS + u;
+            if (j < w.Jw) {  // warp-uniform
+              uint4 v[R];
+#pragma unroll
+              for (int rr = 0; rr < R; ++rr) {
+                const uint32_t a = sbase + (uint32_t)rr * kStageRow + u * kRoundBytes;
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(v[rr].x), "=r"(v[rr].y), "=r"(v[rr].z), "=r"(v[rr].w)
+                             : "r"(a));
+              }
+              const uint32_t o = lane_off + (uint32_t)j * kRound;
+              if constexpr (INT4) int4_chunk<B, R>(v, xs, o, bstride, acc);
+              else int8_chunk<B, R>(v, xs, o, bstride, acc);
+            }
+          }
+        }
+        __syncwarp();
+        if (++cst == NS) {
+          cst = 0;
+          cphase ^= 1u;
+        }
+      }
+      float outl[R][2];
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) outl[rr][0] = outl[rr][1] = 0.0f;
+      if constexpr (INT4) {
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+          const uint4 *orow = reinterpret_cast<const uint4 *>(p.w_out[mrow[rr]] +
+                                                              (int64_t)irow[rr] * p.ld_out[mrow[rr]]);
+#pragma unroll 1
+          for (int c = lane; c < p.ocpr; c += 32) {
+            const uint4 v = c == lane ? ov[rr] : ld_stream(orow + c);
+            const uint4 xv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(xo) + c * 16);
+            fhfma2(outl[rr][0], outl[rr][1], v.x, xv.x);
+            fhfma2(outl[rr][0], outl[rr][1], v.y, xv.y);
+            fhfma2(outl[rr][0], outl[rr][1], v.z, xv.z);
+            fhfma2(outl[rr][0], outl[rr][1], v.w, xv.w);
+          }
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) {
+        const float bg = (acc[rr][0][0] + acc[rr][0][2]) + (acc[rr][0][1] + acc[rr][0][3]) * 0.0625f;
+        const float yl = warp_sum(fmaf(srow[rr], bg, outl[rr][0] + outl[rr][1]));
+        if (lane == 0 && live[rr] && ok) p.y[mrow[rr]][irow[rr]] = __float2half_rn(yl);
+        acc[rr][0][0] = acc[rr][0][1] = acc[rr][0][2] = acc[rr][0][3] = 0.f;
+      }
+    }
+  }
+  // ---- the last CTA past the final product resets the counter ---------------
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(sp.sync, 1u);
+    if (old == (unsigned)(sp.n * G - 1)) atomicExch(sp.sync, 0u);
+  }
+  // A warp that gave up a wait still has copies in flight into its ring;
+  // give them a bounded time to land before the CTA's shared memory goes.
+  if (!ok && lane == 0) {
+    for (int st = 0; st < NS; ++st) {
+      const unsigned long long t0 = gtimer();
+      while (!mbar_try(bar_w + st * 8, 0) && !mbar_try(bar_w + st * 8, 1) &&
+             gtimer() - t0 < kWaitNs) {
+      }
+    }
+  }
+}
+
 template <bool INT4, int B>
 qz_status launch_t(const GemvParams &p, cudaStream_t s) {
   constexpr int R = Ring<B>::R;
@@ -559,6 +875,48 @@ size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p) {
   const size_t R = B == 1 ? 2 : 1, NS = 2, RPS = B == 1 ? 4 : 2;
   const size_t ring = (size_t)kWarps * NS * R * RPS * kRoundBytes;
   return ((staged + 127) & ~(size_t)127) + ring + (size_t)kWarps * NS * 8;
+}
+
+size_t gemv_seq_smem_bytes(bool int4, const SeqParams &sp, uint32_t *xs_bytes) {
+  const size_t cs = int4 ? 80 : 48;
+  size_t xsb = 0;
+  for (int k = 0; k < sp.n; ++k) {
+    const size_t rounds = sp.t[k].cpr > 0 ? (size_t)(sp.t[k].cpr + 31) / 32 : 1;
+    const size_t need = rounds * 32 * cs + (int4 ? (size_t)sp.t[k].ocpr * 16 : 0);
+    if (need > xsb) xsb = need;
+  }
+  xsb = (xsb + 127) & ~(size_t)127;
+  if (xs_bytes) *xs_bytes = (uint32_t)xsb;
+  const size_t ring = (size_t)kWarps * Ring<1>::NS * Ring<1>::R * Ring<1>::RPS * kRoundBytes;
+  return xsb + ring + (size_t)kWarps * Ring<1>::NS * 8 + 16;
+}
+
+qz_status launch_gemv_seq(bool int4, SeqParams &sp, cudaStream_t s) {
+  DeviceInfo di;
+  qz_status st = device_info(&di);
+  if (st != QZ_OK) return st;
+  const size_t smem = gemv_seq_smem_bytes(int4, sp, &sp.xs_bytes);
+  if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
+  auto kern = int4 ? gemv_seq_kernel<true> : gemv_seq_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (occ < 1) return QZ_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)di.sms);  // one CTA per SM: all resident for the barriers
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = sp.t[0].overlap ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, sp);
+  if (e != cudaSuccess) return cuda_status(e);
+  return launch_status();
 }
 
 qz_status read_gemv_error(int *code, int clear) {

@@ -2,6 +2,8 @@
 // Validation never touches the GPU, so an invalid call enqueues nothing.
 #include <mutex>
 
+#include <cstring>
+
 #include "qz_internal.cuh"
 
 namespace qz {
@@ -172,6 +174,38 @@ qz_status gemm_common(bool int4, GemvParams &p, int64_t B, const qz_half *X, int
   return launch_tc(int4, (int)B, p, rows, ws, ws_bytes, s);
 }
 
+template <typename W, typename Fill, typename Check>
+qz_status sequence_common(bool int4, const W *ws, const int *counts, int n,
+                          const qz_half *const *x, qz_half *const *ys, uint32_t *sync,
+                          cudaStream_t s, Fill fill, Check check) {
+  if (!ws || !counts || !x || !ys || !sync || n < 1) return QZ_ERR_INVALID_ARG;
+  if (n > QZ_MAX_SEQ) return QZ_ERR_UNSUPPORTED;
+  if (((uintptr_t)sync & 3u) != 0) return QZ_ERR_ALIGNMENT;
+  SeqParams sp;
+  memset(&sp, 0, sizeof(sp));
+  int off = 0;
+  for (int k = 0; k < n; ++k) {
+    const int c = counts[k];
+    if (c < 1) return QZ_ERR_INVALID_ARG;
+    if (c > QZ_MAX_GROUP) return QZ_ERR_UNSUPPORTED;
+    for (int m = 0; m < c; ++m) {
+      QZ_TRY(check(ws[off + m], ws[off]));
+      QZ_TRY(check_vec(ys[off + m], 1, ws[off + m].N, 0));
+    }
+    QZ_TRY(check_vec(x[k], 1, ws[off].K, 0));
+    GemvParams &p = sp.t[k];
+    fill(p, ws + off, c);
+    p.x = reinterpret_cast<const __half *>(x[k]);
+    p.ldx = 0;
+    p.overlap = overlap_enabled();
+    for (int m = 0; m < QZ_MAX_GROUP; ++m) p.ldy[m] = 0;
+    for (int m = 0; m < c; ++m) p.y[m] = reinterpret_cast<__half *>(ys[off + m]);
+    off += c;
+  }
+  sp.n = n;
+  sp.sync = reinterpret_cast<unsigned int *>(sync);
+  return launch_gemv_seq(int4, sp, s);
+}
 }  // namespace
 }  // namespace qz
 
@@ -404,6 +438,32 @@ qz_status qz_gemv_int4_outlier_grouped(const qz_int4o_weight *ws, int n, const q
   GemvParams p;
   fill_int4o(p, ws, n);
   return gemm_common(true, p, 1, x, 0, ys, nullptr, n, nullptr, 0, (cudaStream_t)s);
+}
+
+
+qz_status qz_gemv_int8_sequence(const qz_int8_weight *ws, const int *counts, int n,
+                                const qz_half *const *x, qz_half *const *ys, uint32_t *sync,
+                                qz_stream s) {
+  return sequence_common(
+      false, ws, counts, n, x, ys, sync, (cudaStream_t)s,
+      [](GemvParams &p, const qz_int8_weight *w, int c) { fill_int8(p, w, c); },
+      [](const qz_int8_weight &w, const qz_int8_weight &w0) -> qz_status {
+        QZ_TRY(check_int8_weight(&w));
+        return w.K == w0.K ? QZ_OK : QZ_ERR_INVALID_ARG;
+      });
+}
+
+qz_status qz_gemv_int4_outlier_sequence(const qz_int4o_weight *ws, const int *counts, int n,
+                                        const qz_half *const *x, qz_half *const *ys,
+                                        uint32_t *sync, qz_stream s) {
+  return sequence_common(
+      true, ws, counts, n, x, ys, sync, (cudaStream_t)s,
+      [](GemvParams &p, const qz_int4o_weight *w, int c) { fill_int4o(p, w, c); },
+      [](const qz_int4o_weight &w, const qz_int4o_weight &w0) -> qz_status {
+        QZ_TRY(check_int4o_weight(&w));
+        return (w.K == w0.K && w.n_out == w0.n_out && w.perm == w0.perm) ? QZ_OK
+                                                                          : QZ_ERR_INVALID_ARG;
+      });
 }
 
 }  // extern "C"

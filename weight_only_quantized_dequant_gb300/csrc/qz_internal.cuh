@@ -46,6 +46,16 @@ struct GemvParams {
   int overlap;  // programmatic dependent launch + weight prefetch before the wait
 };
 
+// Up to QZ_MAX_SEQ dependent batch-1 products in one launch (grid barrier
+// between products on the counter *sync, which starts and ends at 0).
+struct SeqParams {
+  GemvParams t[QZ_MAX_SEQ];
+  int n;
+  unsigned int *sync;
+  uint32_t xs_bytes;  // shared bytes reserved for the staged input (set by the launcher)
+};
+qz_status launch_gemv_seq(bool int4, SeqParams &sp, cudaStream_t s);
+
 // Per-host-thread launch option set by qz_set_overlap().
 int overlap_enabled();
 

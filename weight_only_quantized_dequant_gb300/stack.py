@@ -41,8 +41,11 @@ def make_io(wl: S.Workload, layers: int, batch: int, device):
 
 class LayerStack:
     def __init__(self, wl: S.Workload, layers: int | None = None, batch: int = 1,
-                 device="cuda", keep_fp16: bool = False):
+                 device="cuda", keep_fp16: bool = False, fused: bool = False):
+        """fused: at batch 1, run each layer's four products as one sequence
+        launch (api.gemv_sequence) instead of four launches."""
         self.wl = wl
+        self.fused = fused and batch == 1
         self.n_layers = wl.layers if layers is None else layers
         self.batch = batch
         self.device = torch.device(device)
@@ -52,6 +55,8 @@ class LayerStack:
         for l in range(self.n_layers):
             self.layers.append(self._build_layer(l, keep_fp16))
         self._alloc_io()
+        # barrier words of the sequence launches (consecutive layers alternate)
+        self.sync = torch.zeros((2,), dtype=torch.int32, device=self.device)
         self.workspace = None
         if batch > 1:  # one workspace for every batched call of the step
             nb = max(api.gemm_workspace_bytes(batch, K, api.default_n_out(K) if wl.fmt == "int4o" else 0)
@@ -93,8 +98,11 @@ class LayerStack:
 
     # ------------------------------------------------------------- run ----
     def launches_per_step(self) -> int:
-        """Kernel launches of one step: one per group; on the tensor-core path
-        (batch > 4) each group adds the launch that gathers its inputs."""
+        """Kernel launches of one step: one per group (one per layer when
+        fused); on the tensor-core path (batch > 4) each group adds the launch
+        that gathers its inputs."""
+        if self.fused:
+            return self.n_layers
         per_group = 1 if self.batch <= 4 else 2
         return self.n_layers * len(S.GROUPS) * per_group
 
@@ -118,8 +126,19 @@ class LayerStack:
             fn = api.gemm_int8_grouped if int8 else api.gemm_int4_outlier_grouped
             fn(mats, x, ys, stream=stream, workspace=self.workspace)
 
+    def run_layer_fused(self, l: int, stream=None):
+        """The layer's four products as one dependent sequence launch."""
+        mats = self.layers[l].mats
+        groups = [[mats[m] for m in names] for names in S.GROUPS]
+        xs = [x[0] for x in self.x[l]]
+        ys = [[y[0] for y in yy] for yy in self.y[l]]
+        api.gemv_sequence(groups, xs, ys, sync=self.sync[l % 2:l % 2 + 1], stream=stream)
+
     def run_step(self, stream=None):
         for l in range(self.n_layers):
+            if self.fused:
+                self.run_layer_fused(l, stream)
+                continue
             for g in range(len(S.GROUPS)):
                 self.run_group(l, g, stream)
 
