@@ -134,12 +134,18 @@ qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X,
 
 /* Device workspace the batched calls use on the tensor-core path: the
  * permuted inputs are gathered once per call into tensor-core tiles there,
- * then streamed into the GEMM by bulk copies.  B inputs of K channels with
- * n_out outlier channels (0 for INT8); 0 for invalid sizes.  Host only.
- * The workspace argument of qz_gemm_* may be NULL (the tensor-core kernel then
- * gathers its inputs itself, much more slowly); if given it must be 16-byte
- * aligned and at least this many bytes, caller-owned, and not used by other
- * work while the call runs.  The CUDA-core path ignores it. */
+ * then streamed into the GEMM by bulk copies; behind them lie the fp32
+ * partial sums of output tiles whose K range is cut between SMs (at most two
+ * per SM) and their arrival counters, so that every SM gets the same share
+ * of the call's work.  B inputs of K channels with n_out outlier channels (0
+ * for INT8); 0 for invalid sizes.  Host only; the size does not depend on N
+ * or the device.  The workspace argument of qz_gemm_* may be NULL (the
+ * tensor-core kernel then gathers its inputs itself and gives each SM whole
+ * 128-row tiles only, much more slowly); if given it must be 16-byte aligned
+ * and at least this many bytes, caller-owned, and not used by other work
+ * while the call runs.  The CUDA-core path ignores it.  Results with and
+ * without a workspace agree within the products' rounding bound, not bit for
+ * bit (the fp32 partial sums are added in a different order). */
 size_t qz_gemm_workspace_bytes(int64_t B, int64_t K, int64_t n_out);
 
 /* n matrices (1 <= n <= QZ_MAX_GROUP) that read the same input x, in one
@@ -266,13 +272,13 @@ qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B,
  * device array of QZ_NOALLOC_SCRATCH_BYTES, which every GPU that loads the
  * library holds until the process exits; it allocates nothing itself.
  * Limit: qz_gemm_workspace_bytes(B, K, n_out) must not exceed
- * QZ_NOALLOC_SCRATCH_BYTES (e.g. B = 64 up to K ~ 32k), else
+ * QZ_NOALLOC_SCRATCH_BYTES (e.g. B = 64 up to K ~ 48k), else
  * QZ_ERR_UNSUPPORTED.  All calls share the array (it keeps the last call's
  * contents, every call rewrites what it reads): calls that overlap on the
  * GPU, on any stream, race.  The first call on a device looks the array's
  * device address up (cudaGetSymbolAddress) and should come before any stream
  * capture.  Same arguments and result as qz_gemm_int4_outlier otherwise. */
-#define QZ_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define QZ_NOALLOC_SCRATCH_BYTES (16u << 20)
 qz_status qz_gemm_int4_outlier_noalloc(const qz_int4o_weight *w, int64_t B,
                                        const qz_half *X, int64_t ldx,
                                        qz_half *Y, int64_t ldy, qz_stream s);

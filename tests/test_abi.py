@@ -66,10 +66,15 @@ def test_overlap_setting_is_per_thread_and_validated(lib):
 
 
 def test_workspace_bytes(lib):
-    # ceil(n_out/128) + ceil((K-n_out)/128) tiles of Np x 128 fp16, Np = B rounded to 16
-    assert lib.qz_gemm_workspace_bytes(64, 4096, 41) == (1 + 32) * 64 * 128 * 2
-    assert lib.qz_gemm_workspace_bytes(5, 100, 0) == 1 * 16 * 128 * 2
-    assert lib.qz_gemm_workspace_bytes(5, 300, 0) == 3 * 16 * 128 * 2
+    # ceil(n_out/128) + ceil((K-n_out)/128) tiles of Np x 128 fp16 (Np = B
+    # rounded up to 16), then fp32 partials of two 128-row tiles for each of
+    # at most 160 CTAs, then 160 x 4 arrival counters
+    def extra(Np):
+        return 2 * 160 * Np * 128 * 4 + 160 * 4 * 4
+    assert lib.qz_gemm_workspace_bytes(64, 4096, 41) == (1 + 32) * 64 * 128 * 2 + extra(64)
+    assert lib.qz_gemm_workspace_bytes(5, 100, 0) == 1 * 16 * 128 * 2 + extra(16)
+    assert lib.qz_gemm_workspace_bytes(5, 300, 0) == 3 * 16 * 128 * 2 + extra(16)
+    assert lib.qz_gemm_workspace_bytes(33, 300, 0) == 3 * 48 * 128 * 2 + extra(48)
     assert lib.qz_gemm_workspace_bytes(65, 100, 0) == 0
     assert lib.qz_gemm_workspace_bytes(1, 100, 101) == 0
 

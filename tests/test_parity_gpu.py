@@ -264,20 +264,59 @@ def test_batched_grouped_matches_oracle(fmt, B):
 @pytest.mark.parametrize("B", [5, 64])
 def test_tensor_core_without_workspace(fmt, B):
     """The tensor-core kernel also works without a workspace (it gathers the
-    permuted inputs itself) and gives the same bits as with one."""
+    permuted inputs itself and gives each CTA whole tiles).  Both forms are
+    checked against the oracle and each repeats its own bits; they differ
+    from each other only in the order in which fp32 partial sums are added."""
     N, K = 300, 3072
     X = S.activation(B, K, 9100 + B, device=DEV)
     if fmt == "int8":
-        w = qz().quantize_int8(S.weight(N, K, 9101, device=DEV))
-        a = qz().gemm_int8(w, X, workspace=False)
-        b = qz().gemm_int8(w, X)
+        W = S.weight(N, K, 9101, device=DEV)
+        w = qz().quantize_int8(W)
+        run = lambda ws: qz().gemm_int8(w, X, workspace=ws)
+        q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+        y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, X.cpu().numpy())
     else:
         W, prof, perm = _int4_inputs(N, K, 31, 9102)
         w = qz().quantize_int4_outlier(W, perm, 31)
-        a = qz().gemm_int4_outlier(w, X, workspace=False)
-        b = qz().gemm_int4_outlier(w, X)
+        run = lambda ws: qz().gemm_int4_outlier(w, X, workspace=ws)
+        pn = perm.cpu().numpy()
+        wo, q4, s = O.int4o_quantize(W.cpu().numpy(), pn, 31)
+        y_ref, a_ref = O.int4o_product_ref(wo, q4, s, pn, 31, K, X.cpu().numpy())
+    for ws in (False, None):
+        a = run(ws)
+        b = run(ws)
+        assert qz().device_error() == 0
+        assert torch.equal(a, b), f"workspace={ws} not repeatable"
+        assert_close(a, y_ref, a_ref, f"{fmt} B={B} workspace={ws}")
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4o"])
+def test_tensor_core_one_tile_cut_between_many_ctas(fmt):
+    """One ragged 128-row tile at K = 28672: its K tiles are cut between
+    dozens of CTAs and the last to arrive adds all their partials.  Two
+    calls on one workspace give the same bits (the counters restart)."""
+    N, K, B, n_out = 100, 28672, 16, 287
+    X = S.activation(B, K, 9150, device=DEV)
+    if fmt == "int8":
+        W = S.weight(N, K, 9151, device=DEV)
+        w = qz().quantize_int8(W)
+        ws = torch.empty((qz().gemm_workspace_bytes(B, K, 0),), dtype=torch.uint8, device=DEV)
+        run = lambda: qz().gemm_int8(w, X, workspace=ws)
+        q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+        y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, X.cpu().numpy())
+    else:
+        W, prof, perm = _int4_inputs(N, K, n_out, 9152)
+        w = qz().quantize_int4_outlier(W, perm, n_out)
+        ws = torch.empty((qz().gemm_workspace_bytes(B, K, n_out),), dtype=torch.uint8, device=DEV)
+        run = lambda: qz().gemm_int4_outlier(w, X, workspace=ws)
+        pn = perm.cpu().numpy()
+        wo, q4, s = O.int4o_quantize(W.cpu().numpy(), pn, n_out)
+        y_ref, a_ref = O.int4o_product_ref(wo, q4, s, pn, n_out, K, X.cpu().numpy())
+    a = run()
+    b = run()
     assert qz().device_error() == 0
     assert torch.equal(a, b)
+    assert_close(a, y_ref, a_ref, f"{fmt} one tile cut")
 
 
 def test_tensor_core_7b_batch64_full_matrix():

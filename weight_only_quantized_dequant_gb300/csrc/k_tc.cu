@@ -5,19 +5,25 @@
 // Engine)", Architecture & Key Innovations: outlier product + background
 // product), now a dense contraction Y[b][i] = sum_k A[i][k] * X[b][k]:
 //
-//  * A (weights) is the MMA's M side: a CTA owns a tile of 128 output rows.
-//    Producer warps turn packed codes into exact fp16 integers in registers
-//    (INT4: one LOP3 on the 0x6400 exponent per nibble pair; INT8: one PRMT
-//    per byte pair) and store them in the canonical K-major no-swizzle layout
-//    (8x16-byte core matrices).  No fp16 weight tensor exists in HBM.
+//  * A (weights) is the MMA's M side, in tiles of 128 output rows.  Producer
+//    warps turn packed codes into exact fp16 integers in registers (INT4: one
+//    LOP3 on the 0x6400 exponent per nibble pair; INT8: one PRMT per byte
+//    pair) and store them into tensor memory, where the MMA reads A.  No fp16
+//    weight tensor exists in HBM.
 //  * B (activations, N = batch rounded up to 16) is gathered through the
-//    permutation straight into the same layout, in the k order the nibble
-//    conversion produces.
+//    permutation once per call into the canonical K-major layout, in the k
+//    order the nibble conversion produces, and streamed into shared memory.
 //  * One thread issues tcgen05.mma (kind::f16, fp32 accumulate) into two
 //    TMEM accumulators: outlier channels and INT4 background, so that the
 //    per-row scale multiplies the background only: y = D_out + s_i * D_bg.
-//  * A 4-stage mbarrier ring decouples producers and the MMA thread; every
-//    wait is bounded in time and reports a timeout through a device flag.
+//  * Persistent stream-K schedule: the (tile, K tile) work units of all
+//    matrices of the call are cut into one contiguous range per CTA, one CTA
+//    per SM, so every SM gets the same number of MMAs whatever the tile
+//    count.  A tile cut between CTAs is finished by the last of its CTAs to
+//    arrive, which adds the fp32 partials in CTA order (deterministic).
+//  * The accumulators are double-buffered, so the epilogue warps drain one
+//    tile while the MMAs of the next run.  Every wait is bounded in time and
+//    reports a timeout through a device flag.
 #include <cuda.h>
 
 #include <cstring>
@@ -34,17 +40,20 @@ __device__ int g_device_error = 0;
 namespace {
 
 constexpr int kM = 128;         // weight rows per tile (MMA M)
-constexpr int kKT = 128;        // K elements per pipeline stage
-constexpr int kStages = 5;      // A stages in tensor memory (64 columns each)
-constexpr uint32_t kTmemCols = 512;    // accumulators in columns [0, 128), A above
-constexpr uint32_t kAColBase = 128;
+constexpr int kKT = 128;        // K elements per work unit (one pipeline stage)
+constexpr int kMaxAStages = 6;  // A stages in tensor memory (64 columns each)
+constexpr uint32_t kTmemCols = 512;    // 2 x (outlier, background) accumulators, A above
 constexpr int kProducers = 256;  // 8 warps, two threads per weight row
-constexpr int kMmaWarp = kProducers / 32;     // warp 8 issues the MMAs
-constexpr int kCodeWarp = kMmaWarp + 1;       // warp 9 fills the code ring
-constexpr int kLoadWarp = kMmaWarp + 2;       // warp 10 fills the activation ring
-constexpr int kThreadsTc = kProducers + 96;
+constexpr int kEpiWarp = kProducers / 32;     // warps 8-11 drain the accumulators
+constexpr int kMmaWarp = kEpiWarp + 4;        // warp 12 issues the MMAs
+constexpr int kCodeWarp = kMmaWarp + 1;       // warp 13 fills the code ring
+constexpr int kLoadWarp = kMmaWarp + 2;       // warp 14 fills the activation ring
+constexpr int kThreadsTc = kProducers + 224;
+constexpr int kEpiThreads = 128;
 constexpr int kMaxBStages = 8;                // activation ring depth (smem permitting)
 constexpr size_t kBRingBytes = 80 * 1024;     // shared memory given to that ring
+constexpr int kMaxCtas = 160;   // persistent grid cap (partial slots in the workspace)
+constexpr int kMinUnits = 4;    // work units per CTA at least (its fixed start-up cost)
 constexpr uint32_t kLBO = 128;   // bytes between core matrices along K
 constexpr uint32_t kSBO = 2048;  // bytes between 8-row groups (kKT/8 * 128)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
@@ -64,15 +73,24 @@ struct TcParams {
   GemvParams g;
   int B;                // batch rows
   int Np;               // MMA N: B rounded up to 16
-  int S;                // CTAs per tile (cluster size): each does 1/S of the K tiles
-  const uint8_t *ws;    // gathered activations, one canonical B tile per K tile (or null)
   int nbs;              // stages of the activation ring
+  int nsa;              // A stages in tensor memory
+  uint32_t a_base;      // first TMEM column of the A stages (4 Np)
+  const uint8_t *ws;    // gathered activations, one canonical B tile per K tile (or null)
+  float *part;          // partials of cut tiles: [kMaxCtas][2][kM][Np] fp32 (split only)
+  unsigned *cnt;        // arrivals per cut tile and TMEM lane quarter, by its first CTA
   int ko;               // K tiles of the outlier block
   int kbt;              // K tiles of the background block
+  int KT;               // K tiles per tile: ko + kbt
+  int tiles;            // row tiles of all matrices
+  int U;                // work units: tiles * KT
+  int G;                // CTAs (persistent grid)
+  int split;            // 1: ranges of units (tiles may be cut); 0: ranges of whole tiles
   int n_tiles[QZ_MAX_GROUP];
   int tile_end[QZ_MAX_GROUP];
   int64_t mat_rows[QZ_MAX_GROUP];
 };
+
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -207,6 +225,48 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t *>(&r);
 }
 
+// Work-unit range [start(c), start(c+1)) of CTA c.  Split: an even cut of the
+// U units (a tile may span CTAs); otherwise whole tiles.
+__device__ __forceinline__ int range_start(const TcParams &tp, int c) {
+  if (tp.split) return (int)((int64_t)c * tp.U / tp.G);
+  return (int)((int64_t)c * tp.tiles / tp.G) * tp.KT;
+}
+
+// The CTA whose range holds unit u (split schedule).
+__device__ __forceinline__ int unit_owner(const TcParams &tp, int u) {
+  return (int)((((int64_t)u + 1) * tp.G - 1) / tp.U);
+}
+
+struct TileInfo {
+  int m;           // matrix of the group
+  int64_t row0;    // first row of the tile in that matrix
+  int64_t nrows;   // rows of that matrix
+};
+
+__device__ __forceinline__ TileInfo tile_info(const TcParams &tp, int t) {
+  int m = 0;
+#pragma unroll
+  for (int i = 0; i < QZ_MAX_GROUP - 1; ++i) m += (i < tp.g.n_mats - 1 && t >= tp.tile_end[i]) ? 1 : 0;
+  TileInfo r;
+  r.m = m;
+  r.row0 = (int64_t)(t - (m ? tp.tile_end[m - 1] : 0)) * kM;
+  r.nrows = tp.mat_rows[m];
+  return r;
+}
+
+// Slot of CTA q's partial of tile t: 0 if t is the first tile of its range.
+__device__ __forceinline__ int part_slot(const TcParams &tp, int q, int t) {
+  return t == range_start(tp, q) / tp.KT ? 0 : 1;
+}
+
+// Bounded wait that ignores the abort flag: used to let this CTA's own bulk
+// copies land before it exits after an abort.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = gtimer();
+  while (!mbar_try(bar, parity))
+    if (gtimer() - t0 > kWaitNs) return;
+}
+
 template <bool INT4>
 __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_constant__ TcParams tp) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -215,35 +275,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   uint8_t *base = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int bBytes = tp.Np * kKT * 2;
-  const int NB = tp.nbs;
+  const int NB = tp.nbs, NA = tp.nsa, KT = tp.KT, Np = tp.Np;
   uint8_t *b_st = base;                              // NB * bBytes
   uint8_t *raw = b_st + NB * bBytes;                 // RawRing<INT4>::BYTES
   uint64_t *bars = reinterpret_cast<uint64_t *>(raw + RawRing<INT4>::BYTES);
-  uint64_t *full = bars, *empty = bars + kStages;
-  uint64_t *bfull = bars + 2 * kStages, *bempty = bfull + kMaxBStages;
+  uint64_t *full = bars, *empty = bars + kMaxAStages;
+  uint64_t *bfull = bars + 2 * kMaxAStages, *bempty = bfull + kMaxBStages;
   uint64_t *rfull = bempty + kMaxBStages, *rempty = rfull + kMaxRaw;
-  uint64_t *done = rempty + kMaxRaw;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  uint64_t *dfull = rempty + kMaxRaw, *dempty = dfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dempty + 2);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // cluster of S CTAs per tile; this CTA takes K tiles [kt_begin, kt_end)
-  const int S = tp.S;
-  const int rank = (int)(blockIdx.x % (unsigned)S);
-  const int tile = (int)(blockIdx.x / (unsigned)S);
-  int m = 0;
-#pragma unroll
-  for (int t = 0; t < QZ_MAX_GROUP - 1; ++t) m += (t < p.n_mats - 1 && tile >= tp.tile_end[t]) ? 1 : 0;
-  const int64_t row0 = (int64_t)(tile - (m ? tp.tile_end[m - 1] : 0)) * kM;
-  const int64_t nrows = tp.mat_rows[m];
-  const int ktiles = tp.ko + tp.kbt;
-  const int kt_begin = ktiles * rank / S, kt_end = ktiles * (rank + 1) / S;
-  const bool has_out = kt_begin < (kt_end < tp.ko ? kt_end : tp.ko);
-  const bool has_bg = (kt_begin > tp.ko ? kt_begin : tp.ko) < kt_end;
-  const uint32_t ncols = kTmemCols;  // one CTA per SM (the host pads shared memory)
+  const int cta = (int)blockIdx.x;
+  const int u_begin = range_start(tp, cta), u_end = range_start(tp, cta + 1);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxAStages; ++s) {
       mbar_init(smem_u32(&full[s]), kProducers);
       mbar_init(smem_u32(&empty[s]), 1);
     }
@@ -255,14 +303,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       mbar_init(smem_u32(&rfull[s]), 1);
       mbar_init(smem_u32(&rempty[s]), kProducers);
     }
-    mbar_init(smem_u32(done), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&dfull[s]), 1);
+      mbar_init(smem_u32(&dempty[s]), kEpiThreads);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(ncols)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -270,46 +321,52 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: outlier accumulator [0, Np), background accumulator
-  // [Np, 2 Np), A stages from kAColBase.
-  const uint32_t d_out = tmem, d_bg = tmem + (uint32_t)tp.Np;
+  // TMEM columns: accumulator buffer d at [2 d Np, 2 d Np + 2 Np) (outlier
+  // then background), A stages from tp.a_base = 4 Np.
 
-  if (warp < kProducers / 32) {
+  if (warp < kEpiWarp) {
     // ------------------------------------------------------ producers ----
     // Warp w converts k slots [64 h, 64 h + 64) of the rows of TMEM lane
     // quarter w % 4 (h = w / 4): thread = one row, its 64 fp16 codes go to
     // 32 columns of its own TMEM lane with one tcgen05.st.
     const int h = warp >> 2, r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int64_t grow = row0 + r;
-    const bool live = grow < nrows;
     // Background (INT4) or all (INT8) K tiles arrive as packed codes in the
     // raw ring (filled by the code loader warp); each thread converts its bytes.
     constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB, HB = RawRing<INT4>::HB;
-    const int bgb = kt_begin > tp.ko ? kt_begin : tp.ko;  // first code tile
     const uint32_t raw_me = smem_u32(raw) + (uint32_t)r * RB + (uint32_t)h * HB;
-    // inputs may come from earlier kernels (outlier weights do not)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int kt = kt_begin; kt < kt_end; ++kt) {
-      const int q = kt - kt_begin;  // position in this CTA's ring sequence
-      const int s = q % kStages;
-      if (q >= kStages) {
-        if (!mbar_wait(smem_u32(&empty[s]), ((q / kStages) - 1) & 1, abort_flag)) break;
+    int i = 0;       // code tiles taken from the raw ring so far
+    int t_cur = -1;  // tile of the previous unit
+    TileInfo ti = {0, 0, 0};
+    for (int u = u_begin; u < u_end; ++u) {
+      const int q = u - u_begin;  // position in this CTA's ring sequence
+      const int s = q % NA;
+      if (q >= NA) {
+        const bool ok = mbar_wait(smem_u32(&empty[s]), ((q / NA) - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
         fence_after();  // the MMAs that read this A stage are complete
       }
+      const int t = u / KT, kt = u - t * KT;
+      if (t != t_cur) {
+        ti = tile_info(tp, t);
+        t_cur = t;
+      }
+      const int64_t grow = ti.row0 + r;
+      const bool live = grow < ti.nrows;
       const bool outl = kt < tp.ko;
       uint32_t o[32];  // fp16 pairs of k slots 2j, 2j+1 of this thread's 64
       if (INT4 && outl) {
         const int t0 = kt * kKT + h * (kKT / 2);
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.w_out[m] + grow * p.ld_out[m]);
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.w_out[ti.m] + grow * p.ld_out[ti.m]);
 #pragma unroll
         for (int kg = 0; kg < 8; ++kg) {
-          const int t = t0 + kg * 8;
+          const int tt = t0 + kg * 8;
           uint4 v = make_uint4(0, 0, 0, 0);
-          if (live && t < p.n_out) {
-            v = __ldg(src + t / 8);
+          if (live && tt < p.n_out) {
+            v = __ldg(src + tt / 8);
             // zero the slots past n_out inside the last group
-            const int valid = p.n_out - t;
+            const int valid = p.n_out - tt;
             if (valid < 8) {
               uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -324,8 +381,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
           o[4 * kg + 3] = v.w;
         }
       } else if (INT4) {
-        const int i = kt - bgb;
-        if (!mbar_wait(smem_u32(&rfull[i % DR]), (i / DR) & 1, abort_flag)) break;
+        const bool ok = mbar_wait(smem_u32(&rfull[i % DR]), (i / DR) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
         const uint32_t rsrc = raw_me + (uint32_t)(i % DR) * (kM * RB);
         uint4 qv[2];
 #pragma unroll
@@ -334,6 +391,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                        : "=r"(qv[c].x), "=r"(qv[c].y), "=r"(qv[c].z), "=r"(qv[c].w)
                        : "r"(rsrc + 16 * c));
         mbar_arrive(smem_u32(&rempty[i % DR]));  // the codes are in registers
+        ++i;
         const uint32_t words[8] = {qv[0].x, qv[0].y, qv[0].z, qv[0].w,
                                    qv[1].x, qv[1].y, qv[1].z, qv[1].w};
         const uint32_t bias = 0x64086408u;   // 1032 in both halves after the XOR
@@ -349,8 +407,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
           o[4 * kg + 3] = hsub2_u32(((w >> 12) & 0x000F000Fu) ^ bias, bias);
         }
       } else {
-        const int i = kt - bgb;
-        if (!mbar_wait(smem_u32(&rfull[i % DR]), (i / DR) & 1, abort_flag)) break;
+        const bool ok = mbar_wait(smem_u32(&rfull[i % DR]), (i / DR) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
         const uint32_t rsrc = raw_me + (uint32_t)(i % DR) * (kM * RB);
         uint4 vv[4];
 #pragma unroll
@@ -359,6 +417,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                        : "=r"(vv[c].x), "=r"(vv[c].y), "=r"(vv[c].z), "=r"(vv[c].w)
                        : "r"(rsrc + 16 * c));
         mbar_arrive(smem_u32(&rempty[i % DR]));  // the codes are in registers
+        ++i;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t w[4] = {vv[c].x ^ 0x80808080u, vv[c].y ^ 0x80808080u,
@@ -375,53 +434,168 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = 0;
       }
-      tmem_st32(tmem + lane_base + kAColBase + (uint32_t)s * (kKT / 2) + (uint32_t)h * 32, o);
+      tmem_st32(tmem + lane_base + tp.a_base + (uint32_t)s * (kKT / 2) + (uint32_t)h * 32, o);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       fence_before();
       mbar_arrive(smem_u32(&full[s]));
+    }
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------- epilogue ----
+    // Thread = one row of the tile (its TMEM lane).  Segment j of this CTA
+    // (its units of one tile) sits in accumulator buffer j % 2.
+    const int qtr = warp - kEpiWarp;  // == warp % 4: the TMEM lane quarter it may read
+    const int r = qtr * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(qtr * 32) << 16;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int j = 0;
+    for (int u = u_begin; u < u_end; ++j) {
+      const int t = u / KT;
+      const int k0 = u - t * KT;
+      const int seg_end = u_end < (t + 1) * KT ? u_end : (t + 1) * KT;
+      const int k1 = seg_end - t * KT;
+      u = seg_end;
+      const TileInfo ti = tile_info(tp, t);
+      const int64_t grow = ti.row0 + r;
+      const bool live = grow < ti.nrows;
+      const bool has_out = INT4 && k0 < tp.ko;
+      const bool has_bg = k1 > tp.ko;
+      const bool cut = !(k0 == 0 && k1 == KT);
+      float s_i = 1.0f;
+      if (live) s_i = INT4 ? __ldg(p.scale[ti.m] + grow) : __ldg(p.scale[ti.m]);
+      __half *yrow = p.y[ti.m] + grow;
+      const int64_t ldy = p.ldy[ti.m];
+      const int db = j & 1;
+      const bool ok = mbar_wait(smem_u32(&dfull[db]), (j >> 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      fence_after();
+      const uint32_t dcol = tmem + lane_base + (uint32_t)(db * 2 * Np);
+      // partial of a cut tile: row r's Np values contiguous in its slot
+      float4 *mine = nullptr;
+      if (cut)
+        mine = reinterpret_cast<float4 *>(tp.part +
+                                          ((size_t)(cta * 2 + part_slot(tp, cta, t)) * kM + r) * Np);
+      for (int c0 = 0; c0 < Np; c0 += 16) {
+        float vb[16], vo[16], y[16];
+        tmem_ld16(dcol + (uint32_t)Np + c0, vb);
+        if (INT4) tmem_ld16(dcol + c0, vo);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const float bg = has_bg ? vb[jj] : 0.0f;
+          const float o = has_out ? vo[jj] : 0.0f;
+          y[jj] = fmaf(s_i, bg, o);  // this CTA's units of the tile
+        }
+        if (!cut) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (live && c0 + jj < tp.B) yrow[(int64_t)(c0 + jj) * ldy] = __float2half_rn(y[jj]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mine[c0 / 4 + k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+        }
+      }
+      fence_before();
+      mbar_arrive(smem_u32(&dempty[db]));  // the MMAs may reuse this buffer
+      if (cut) {
+        // Publish the partial; the warp that brings the count of its lane
+        // quarter to the number of contributors adds them all in CTA order.
+        const int c_lo = unit_owner(tp, t * KT), c_hi = unit_owner(tp, (t + 1) * KT - 1);
+        __threadfence();
+        __syncwarp();
+        unsigned prev = 0;
+        if (lane == 0) prev = atomicAdd(tp.cnt + c_lo * 4 + qtr, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == (unsigned)(c_hi - c_lo)) {
+          __threadfence();
+          for (int n0 = 0; n0 < tp.B; n0 += 16) {
+            float acc[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.0f;
+            // four contributors' loads in flight, added in CTA order
+            for (int qq = c_lo; qq <= c_hi; qq += 4) {
+              float4 v[4][4];
+#pragma unroll
+              for (int a = 0; a < 4; ++a)
+                if (qq + a <= c_hi) {
+                  const float4 *src = reinterpret_cast<const float4 *>(
+                      tp.part + ((size_t)((qq + a) * 2 + part_slot(tp, qq + a, t)) * kM + r) * Np + n0);
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) v[a][k] = __ldcg(src + k);
+                }
+#pragma unroll
+              for (int a = 0; a < 4; ++a)
+                if (qq + a <= c_hi) {
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    acc[4 * k] += v[a][k].x;
+                    acc[4 * k + 1] += v[a][k].y;
+                    acc[4 * k + 2] += v[a][k].z;
+                    acc[4 * k + 3] += v[a][k].w;
+                  }
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              if (live && n0 + jj < tp.B) yrow[(int64_t)(n0 + jj) * ldy] = __float2half_rn(acc[jj]);
+          }
+        }
+      }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       // ---------------------------------------------------- MMA issuer ---
-      const uint32_t idesc = idesc_f16(kM, tp.Np);
-      for (int kt = kt_begin; kt < kt_end; ++kt) {
-        const int q = kt - kt_begin;
-        const int s = q % kStages, sb = q % NB;
-        if (!mbar_wait(smem_u32(&full[s]), (q / kStages) & 1, abort_flag)) break;
+      const uint32_t idesc = idesc_f16(kM, Np);
+      int j = -1, k0 = 0;
+      uint32_t dcol = 0;
+      for (int u = u_begin; u < u_end; ++u) {
+        const int q = u - u_begin;
+        const int t = u / KT, kt = u - t * KT;
+        if (q == 0 || kt == 0) {  // a new segment: next accumulator buffer
+          ++j;
+          k0 = kt;
+          dcol = (uint32_t)((j & 1) * 2 * Np);
+          if (j >= 2) {
+            if (!mbar_wait(smem_u32(&dempty[j & 1]), ((j >> 1) - 1) & 1, abort_flag)) break;
+            fence_after();
+          }
+        }
+        const int s = q % NA, sb = q % NB;
+        if (!mbar_wait(smem_u32(&full[s]), (q / NA) & 1, abort_flag)) break;
         if (!mbar_wait(smem_u32(&bfull[sb]), (q / NB) & 1, abort_flag)) break;
         fence_after();
         const bool outl = kt < tp.ko;
-        const uint32_t a0 = tmem + kAColBase + (uint32_t)s * (kKT / 2);
+        const uint32_t a0 = tmem + tp.a_base + (uint32_t)s * (kKT / 2);
         const uint32_t b0 = smem_u32(b_st + sb * bBytes);
-        const uint32_t d = outl ? d_out : d_bg;
-        const bool first = outl ? kt == kt_begin : kt == (kt_begin > tp.ko ? kt_begin : tp.ko);
+        const uint32_t d = tmem + dcol + (outl ? 0u : (uint32_t)Np);
+        const bool first = outl ? kt == k0 : kt == (k0 > tp.ko ? k0 : tp.ko);
 #pragma unroll
         for (int k16 = 0; k16 < kKT / 16; ++k16)
           mma_f16_ta(d, a0 + 8 * k16, sdesc(b0 + k16 * 2 * kLBO), idesc,
                      (first && k16 == 0) ? 0u : 1u);
         mma_commit(smem_u32(&empty[s]));
         mma_commit(smem_u32(&bempty[sb]));
+        if (u + 1 == u_end || kt + 1 == KT) mma_commit(smem_u32(&dfull[j & 1]));
       }
-      mma_commit(smem_u32(done));  // arrives once every issued MMA has completed
     }
   } else if (warp == kCodeWarp) {
     // ------------------------------------------------------ code loader ---
-    // Packed codes of the background (INT4) or all (INT8) K tiles, one 2D
-    // tensor copy of kM rows x ROWB bytes per tile, DR tiles ahead of the
-    // converters.  The codes are static: the first DR tiles are requested
-    // before the wait for the previous kernel.
+    // Packed codes of the background (INT4) or all (INT8) K tiles of this
+    // CTA's units, one 2D tensor copy of kM rows x ROWB bytes each, DR ahead
+    // of the converters.  The codes are static: no wait for earlier kernels.
     if (lane == 0) {
       constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
-      const int bgb = kt_begin > tp.ko ? kt_begin : tp.ko;  // first code tile
-      const uint64_t cmap = reinterpret_cast<uint64_t>(&tp.codes_map[m]);
-      for (int kt = bgb; kt < kt_end; ++kt) {
-        const int i = kt - bgb;
+      int i = 0;
+      for (int u = u_begin; u < u_end; ++u) {
+        const int t = u / KT, kt = u - t * KT;
+        if (kt < tp.ko) continue;  // outlier units read fp16 rows directly
         const uint32_t bar = smem_u32(&rfull[i % DR]);
         if (i >= DR) {
           if (!mbar_wait(smem_u32(&rempty[i % DR]), ((i / DR) - 1) & 1, abort_flag)) break;
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
+        const TileInfo ti = tile_info(tp, t);
+        const uint64_t cmap = reinterpret_cast<uint64_t>(&tp.codes_map[ti.m]);
         const int x = INT4 ? (kt - tp.ko) * RB : kt * RB;
         asm volatile(
             "{\n\t.reg .b64 t;\n\t"
@@ -431,20 +605,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         asm volatile(
             "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
             "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(raw) + (uint32_t)(i % DR) * (kM * RB)),
-            "l"(cmap), "r"(x), "r"((int)row0), "r"(bar)
+            "l"(cmap), "r"(x), "r"((int)ti.row0), "r"(bar)
             : "memory");
+        ++i;
       }
+      if (*(volatile int *)abort_flag)  // let the copies in flight land
+        for (int k = i > DR ? i - DR : 0; k < i; ++k) mbar_drain(smem_u32(&rfull[k % DR]), (k / DR) & 1);
     }
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------ activation loader ---
-    // Np x kKT activations per K tile, NB tiles ahead of the MMAs.  With a
+    // Np x kKT activations per unit, NB units ahead of the MMAs.  With a
     // workspace the tile was gathered once per call by tc_xprep_kernel and
     // arrives by one bulk copy; without one this warp gathers it.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int kt = kt_begin; kt < kt_end; ++kt) {
-      const int q = kt - kt_begin;
+    int q = 0;
+    for (int u = u_begin; u < u_end; ++u, ++q) {
+      const int kt = u % KT;
       const int sb = q % NB;
-      if (q >= NB && !mbar_wait(smem_u32(&bempty[sb]), ((q / NB) - 1) & 1, abort_flag)) break;
+      if (q >= NB) {
+        const bool ok = mbar_wait(smem_u32(&bempty[sb]), ((q / NB) - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
       uint8_t *Bt = b_st + sb * bBytes;
       const uint32_t bar = smem_u32(&bfull[sb]);
       if (tp.ws) {
@@ -462,14 +643,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         }
       } else {
         const bool outl = kt < tp.ko;
-        for (int idx = lane; idx < tp.Np * kKT; idx += 32) {
+        for (int idx = lane; idx < Np * kKT; idx += 32) {
           const int c = idx % kKT, n = idx / kKT;
           __half v = __float2half_rn(0.0f);
           if (n < tp.B) {
             const __half *xb = p.x + (int64_t)n * p.ldx;
             if (INT4 && outl) {
-              const int t = kt * kKT + c;
-              if (t < p.n_out) v = xb[__ldg(p.perm + t)];
+              const int tt = kt * kKT + c;
+              if (tt < p.n_out) v = xb[__ldg(p.perm + tt)];
             } else if (INT4) {
               const int e = (kt - tp.ko) * kKT + slot_elem(c);
               if (e < p.kb) v = xb[__ldg(p.perm + p.n_out + e)];
@@ -485,71 +666,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         if (lane == 0) mbar_arrive(bar);
       }
     }
+    if (tp.ws && lane == 0 && *(volatile int *)abort_flag)  // let the copies in flight land
+      for (int k = q > NB ? q - NB : 0; k < q; ++k) mbar_drain(smem_u32(&bfull[k % NB]), (k / NB) & 1);
   }
 
-  // ---------------------------------------------------------- epilogue ----
-  // Each thread of warps 0-3 owns one row of the tile (its TMEM lane).
-  // S > 1: partials [Np][kM] in the activation ring (idle once every MMA is done)
-  float *part = reinterpret_cast<float *>(b_st);
-  if (warp < 4) {
-    const bool ok = mbar_wait(smem_u32(done), 0, abort_flag);
-    fence_after();
-    const int r = tid;
-    const int64_t grow = row0 + r;
-    float s_i = 1.0f;
-    if (grow < nrows) s_i = INT4 ? __ldg(p.scale[m] + grow) : __ldg(p.scale[m]);
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    for (int c0 = 0; c0 < tp.Np; c0 += 16) {
-      float vb[16], vo[16];
-      tmem_ld16(d_bg + lane_base + c0, vb);
-      if (INT4) tmem_ld16(d_out + lane_base + c0, vo);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int n = c0 + j;
-        const float bg = has_bg ? vb[j] : 0.0f;
-        const float o = (INT4 && has_out) ? vo[j] : 0.0f;
-        const float y = fmaf(s_i, bg, o);  // partial of this CTA's K tiles
-        if (S == 1) {
-          if (ok && grow < nrows && n < tp.B)
-            p.y[m][(int64_t)n * p.ldy[m] + grow] = __float2half_rn(y);
-        } else {
-          part[n * kM + r] = ok ? y : 0.0f;
-        }
-      }
-    }
-  }
-  if (S > 1) {
-    // Cluster reduction through distributed shared memory: every CTA has its
-    // partials in its own shared memory; CTA k sums rows [k*kM/S, (k+1)*kM/S)
-    // over all S CTAs and stores them.
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-    const int rlo = kM * rank / S, rhi = kM * (rank + 1) / S;
-    const int cnt = (rhi - rlo) * tp.Np;
-    const uint32_t part_local = smem_u32(part);
-    for (int e = tid; e < cnt; e += kThreadsTc) {
-      const int n = e / (rhi - rlo), r = rlo + e % (rhi - rlo);
-      const uint32_t off = (uint32_t)(n * kM + r) * 4u;
-      float acc = 0.0f;
-      for (int q = 0; q < S; ++q) {
-        uint32_t ra;
-        float v;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(part_local + off), "r"(q));
-        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-        acc += v;
-      }
-      const int64_t grow = row0 + r;
-      if (grow < nrows && n < tp.B) p.y[m][(int64_t)n * p.ldy[m] + grow] = __float2half_rn(acc);
-    }
-    // keep every CTA's shared memory alive until all remote reads are done
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-  }
   fence_before();
   __syncthreads();
   fence_after();
   if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
 }
 
@@ -563,6 +688,9 @@ __global__ void __launch_bounds__(256) tc_xprep_kernel(const __grid_constant__ T
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int kt = blockIdx.x;
+  // the arrival counters of the cut tiles start every call at zero
+  if (kt == 0 && tp.cnt)
+    for (int i = threadIdx.x; i < 4 * tp.G; i += blockDim.x) tp.cnt[i] = 0u;
   const int bBytes = tp.Np * kKT * 2;
   uint8_t *tile = ws + (size_t)kt * bBytes;
   const bool outl = kt < tp.ko;
@@ -603,11 +731,15 @@ __global__ void __launch_bounds__(256) tc_xprep_kernel(const __grid_constant__ T
 
 }  // namespace
 
+static size_t tc_part_bytes(int64_t Np) { return (size_t)2 * kMaxCtas * Np * kM * sizeof(float); }
+
 size_t tc_workspace_bytes(bool int4, int64_t B, int64_t K, int64_t n_out) {
   const int64_t Np = (B + 15) / 16 * 16;
   const int64_t tiles = int4 ? (n_out + kKT - 1) / kKT + (K - n_out + kKT - 1) / kKT
                              : (K + kKT - 1) / kKT;
-  return (size_t)(tiles * Np * kKT * 2);
+  // gathered activations, then the partials of cut tiles (two per CTA), then
+  // one arrival counter per CTA and TMEM lane quarter
+  return (size_t)(tiles * Np * kKT * 2) + tc_part_bytes(Np) + (size_t)kMaxCtas * 4 * sizeof(unsigned);
 }
 
 // Stages of the activation ring for a batch of Np (MMA N) columns.
@@ -620,7 +752,7 @@ static int tc_b_stages(int Np) {
 size_t tc_smem_bytes(bool int4, int Np) {
   const size_t need = 1024 + (size_t)tc_b_stages(Np) * Np * kKT * 2 +
                       (int4 ? RawRing<true>::BYTES : RawRing<false>::BYTES) +
-                      (2 * kStages + 2 * kMaxBStages + 2 * kMaxRaw + 1) * 8 + 16;
+                      (2 * kMaxAStages + 2 * kMaxBStages + 2 * kMaxRaw + 4) * 8 + 16;
   // more than half of an SM's shared memory, so that one CTA (which holds
   // all 512 TMEM columns) runs per SM
   const size_t one_per_sm = 120 * 1024;
@@ -680,14 +812,22 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   tp.B = B;
   tp.Np = (B + 15) / 16 * 16;
   tp.nbs = tc_b_stages(tp.Np);
+  tp.a_base = (uint32_t)(4 * tp.Np);
+  tp.nsa = (int)((kTmemCols - tp.a_base) / (kKT / 2));
+  if (tp.nsa > kMaxAStages) tp.nsa = kMaxAStages;
   tp.ko = int4 ? (g.n_out + kKT - 1) / kKT : 0;
   tp.kbt = int4 ? (g.kb + kKT - 1) / kKT : (g.K + kKT - 1) / kKT;
-  tp.S = 1;
+  tp.KT = tp.ko + tp.kbt;
   tp.ws = nullptr;
   if (workspace) {
+    const size_t xbytes = tc_workspace_bytes(int4, B, g.K, g.n_out) - tc_part_bytes(tp.Np) -
+                          (size_t)kMaxCtas * 4 * sizeof(unsigned);
     if (workspace_bytes < tc_workspace_bytes(int4, B, g.K, g.n_out)) return QZ_ERR_INVALID_ARG;
     if ((uintptr_t)workspace & 15u) return QZ_ERR_ALIGNMENT;
     tp.ws = reinterpret_cast<const uint8_t *>(workspace);
+    tp.part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + xbytes);
+    tp.cnt = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(workspace) + xbytes +
+                                          tc_part_bytes(tp.Np));
   }
   for (int m = 0; m < g.n_mats; ++m)
     if (tp.kbt > 0) {
@@ -695,67 +835,49 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
                      int4 ? RawRing<true>::ROWB : RawRing<false>::ROWB);
       if (st != QZ_OK) return st;
     }
-  int tiles = 0;
+  int64_t tiles = 0;
   for (int m = 0; m < QZ_MAX_GROUP; ++m) {
     tp.mat_rows[m] = m < g.n_mats ? mat_rows[m] : 0;
     tp.n_tiles[m] = m < g.n_mats ? (int)((mat_rows[m] + kM - 1) / kM) : 0;
     tiles += tp.n_tiles[m];
-    tp.tile_end[m] = tiles;
+    tp.tile_end[m] = (int)tiles;
+  }
+  if (tiles == 0 || tp.KT == 0) return QZ_OK;
+  if (tiles * tp.KT > (int64_t)INT32_MAX) return QZ_ERR_UNSUPPORTED;
+  tp.tiles = (int)tiles;
+  tp.U = (int)(tiles * tp.KT);
+  // One CTA per SM.  With a workspace (room for partials) the units are cut
+  // evenly, at least kMinUnits per CTA; without one each CTA takes whole tiles.
+  const int gmax = di.sms < kMaxCtas ? di.sms : kMaxCtas;
+  if (tp.ws) {
+    tp.split = 1;
+    const int want = tp.U / kMinUnits;
+    tp.G = want < 1 ? 1 : (want < gmax ? want : gmax);
+  } else {
+    tp.split = 0;
+    tp.G = tp.tiles < gmax ? tp.tiles : gmax;
   }
   const size_t smem = tc_smem_bytes(int4, tp.Np);
   if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
-  // Split K over a cluster of S CTAs per tile so that small matrices still
-  // fill the GPU.  A CTA costs a fixed start/epilogue of about 4 K tiles plus
-  // its share of the K tiles; pick S in {1,2,4,8} minimising
-  // waves * (4 + tiles_of_K / S), keeping at least two K tiles per CTA.
-  {
-    const int per_sm_smem = (int)(233472 / (smem + 1024));
-    const int per_sm_tmem = 512 / (tp.Np <= 16 ? 32 : (tp.Np <= 32 ? 64 : 128));
-    const int per_sm = per_sm_smem < per_sm_tmem ? per_sm_smem : per_sm_tmem;
-    const long slots = (long)di.sms * (per_sm > 0 ? per_sm : 1);
-    const int kt_total = tp.ko + tp.kbt;
-    double best = 1e30;
-    for (int S = 1; S <= 8; S *= 2) {
-      if (S > 1 && kt_total < 2 * S) break;
-      const long ctas = (long)tiles * S;
-      const double t = (double)((ctas + slots - 1) / slots) * (4.0 + (double)kt_total / S);
-      if (t < best - 1e-9) {
-        best = t;
-        tp.S = S;
-      }
-    }
-  }
   auto kern = int4 ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_status(e);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * tp.S));
+  cfg.gridDim = dim3((unsigned)tp.G);
   cfg.blockDim = dim3(kThreadsTc);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  int na = 0;
-  attr[na].id = cudaLaunchAttributeClusterDimension;
-  attr[na].val.clusterDim.x = (unsigned)tp.S;
-  attr[na].val.clusterDim.y = 1;
-  attr[na].val.clusterDim.z = 1;
-  ++na;
-  if (g.overlap) {
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = na;
-  if (tp.ws) {  // gather the activations once, then the GEMM
+  cfg.numAttrs = g.overlap ? 1 : 0;
+  if (tp.ws) {  // gather the activations once (and clear the counters), then the GEMM
     cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3((unsigned)(tp.ko + tp.kbt));
+    pc.gridDim = dim3((unsigned)tp.KT);
     pc.blockDim = dim3(256);
     pc.stream = s;
-    cudaLaunchAttribute pa[1];
-    pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pa[0].val.programmaticStreamSerializationAllowed = 1;
-    pc.attrs = pa;
+    pc.attrs = attr;
     pc.numAttrs = g.overlap ? 1 : 0;
     auto prep = int4 ? tc_xprep_kernel<true> : tc_xprep_kernel<false>;
     e = cudaLaunchKernelEx(&pc, prep, tp, reinterpret_cast<uint8_t *>(workspace));
@@ -796,7 +918,7 @@ qz_status read_device_error(int *code, int clear) {
 namespace qz {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB, QZ_NOALLOC_SCRATCH_BYTES
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB, QZ_NOALLOC_SCRATCH_BYTES
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch array on the current device.  The name of a
