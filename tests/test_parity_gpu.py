@@ -291,6 +291,29 @@ def test_tensor_core_without_workspace(fmt, B):
 
 
 @pytest.mark.parametrize("fmt", ["int8", "int4o"])
+def test_tensor_core_more_tiles_than_sms_without_workspace(fmt):
+    """160 row tiles and no workspace: persistent CTAs take whole tiles, some
+    two in a row (the accumulators alternate), every output checked."""
+    N, K, B, n_out = 160 * 128 - 37, 1024, 16, 11
+    X = S.activation(B, K, 9160, device=DEV)
+    if fmt == "int8":
+        W = S.weight(N, K, 9161, device=DEV)
+        w = qz().quantize_int8(W)
+        Y = qz().gemm_int8(w, X, workspace=False)
+        q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+        y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, X.cpu().numpy())
+    else:
+        W, prof, perm = _int4_inputs(N, K, n_out, 9162)
+        w = qz().quantize_int4_outlier(W, perm, n_out)
+        Y = qz().gemm_int4_outlier(w, X, workspace=False)
+        pn = perm.cpu().numpy()
+        wo, q4, s = O.int4o_quantize(W.cpu().numpy(), pn, n_out)
+        y_ref, a_ref = O.int4o_product_ref(wo, q4, s, pn, n_out, K, X.cpu().numpy())
+    assert qz().device_error() == 0
+    assert_close(Y, y_ref, a_ref, f"{fmt} 160 tiles, no workspace")
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4o"])
 def test_tensor_core_one_tile_cut_between_many_ctas(fmt):
     """One ragged 128-row tile at K = 28672: its K tiles are cut between
     dozens of CTAs and the last to arrive adds all their partials.  Two

@@ -67,6 +67,11 @@ struct RawRing {
   static constexpr int BYTES = DEPTH * kM * ROWB;
 };
 constexpr int kMaxRaw = 8;
+constexpr int kBarBytes = 1024;  // mbarriers and flags at the start of shared memory
+// Schedules of the (tile, K tile) work units over the CTAs.
+constexpr int kWhole = 0;    // persistent, ranges of whole tiles (no workspace)
+constexpr int kStreamK = 1;  // persistent, even ranges of units; cut tiles finished in L2
+constexpr int kCluster = 2;  // a cluster of S CTAs per tile splits K; reduced in DSMEM
 
 struct TcParams {
   CUtensorMap codes_map[QZ_MAX_GROUP];  // 2D: [rows][ld_codes bytes], box kM x ROWB
@@ -77,15 +82,18 @@ struct TcParams {
   int nsa;              // A stages in tensor memory
   uint32_t a_base;      // first TMEM column of the A stages (4 Np)
   const uint8_t *ws;    // gathered activations, one canonical B tile per K tile (or null)
-  float *part;          // partials of cut tiles: [kMaxCtas][2][kM][Np] fp32 (split only)
+  float *part;          // partials of cut tiles: [kMaxCtas][2][4 quarters][Np/4][32][4] fp32
   unsigned *cnt;        // arrivals per cut tile and TMEM lane quarter, by its first CTA
+  int fx_cap;           // partials of one lane quarter the reduction stages at once (>= 2)
+  uint32_t fx_bytes;    // shared-memory staging bytes per lane quarter
   int ko;               // K tiles of the outlier block
   int kbt;              // K tiles of the background block
   int KT;               // K tiles per tile: ko + kbt
   int tiles;            // row tiles of all matrices
   int U;                // work units: tiles * KT
   int G;                // CTAs (persistent grid)
-  int split;            // 1: ranges of units (tiles may be cut); 0: ranges of whole tiles
+  int split;            // schedule: kWhole, kStreamK or kCluster
+  int S;                // kCluster: CTAs per tile (cluster size), each 1/S of its K tiles
   int n_tiles[QZ_MAX_GROUP];
   int tile_end[QZ_MAX_GROUP];
   int64_t mat_rows[QZ_MAX_GROUP];
@@ -225,10 +233,11 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// Work-unit range [start(c), start(c+1)) of CTA c.  Split: an even cut of the
-// U units (a tile may span CTAs); otherwise whole tiles.
+// Work-unit range [start(c), start(c+1)) of CTA c: an even cut of the U
+// units (a tile may span CTAs), 1/S of one tile's K tiles, or whole tiles.
 __device__ __forceinline__ int range_start(const TcParams &tp, int c) {
-  if (tp.split) return (int)((int64_t)c * tp.U / tp.G);
+  if (tp.split == kStreamK) return (int)((int64_t)c * tp.U / tp.G);
+  if (tp.split == kCluster) return (c / tp.S) * tp.KT + tp.KT * (c % tp.S) / tp.S;
   return (int)((int64_t)c * tp.tiles / tp.G) * tp.KT;
 }
 
@@ -276,14 +285,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int bBytes = tp.Np * kKT * 2;
   const int NB = tp.nbs, NA = tp.nsa, KT = tp.KT, Np = tp.Np;
-  uint8_t *b_st = base;                              // NB * bBytes
+  // [barriers | activation ring | raw-code ring | ...]; once a CTA's last
+  // MMA is done, everything past the barriers stages the cut-tile reduction
+  uint64_t *bars = reinterpret_cast<uint64_t *>(base);
+  uint8_t *b_st = base + kBarBytes;                  // NB * bBytes
   uint8_t *raw = b_st + NB * bBytes;                 // RawRing<INT4>::BYTES
-  uint64_t *bars = reinterpret_cast<uint64_t *>(raw + RawRing<INT4>::BYTES);
   uint64_t *full = bars, *empty = bars + kMaxAStages;
   uint64_t *bfull = bars + 2 * kMaxAStages, *bempty = bfull + kMaxBStages;
   uint64_t *rfull = bempty + kMaxBStages, *rempty = rfull + kMaxRaw;
   uint64_t *dfull = rempty + kMaxRaw, *dempty = dfull + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dempty + 2);
+  uint64_t *fxbar = dempty + 2;                      // one per lane quarter
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fxbar + 4);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -307,6 +319,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       mbar_init(smem_u32(&dfull[s]), 1);
       mbar_init(smem_u32(&dempty[s]), kEpiThreads);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&fxbar[s]), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -446,8 +459,94 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     const int qtr = warp - kEpiWarp;  // == warp % 4: the TMEM lane quarter it may read
     const int r = qtr * 32 + lane;
     const uint32_t lane_base = (uint32_t)(qtr * 32) << 16;
+    const uint32_t blk = (uint32_t)Np * 32u * 4u;  // one CTA's partial of one lane quarter
+    uint8_t *stg = b_st + (size_t)qtr * tp.fx_bytes;
+    const uint32_t fxb = smem_u32(&fxbar[qtr]);
+    int fx_uses = 0;
+    // Adds the partials of cut tile t (CTAs c_lo..c_hi, in that order) for
+    // this lane quarter and stores the rows.  Runs once this CTA's last MMA
+    // is done, with the rings free: the partials of up to fx_cap CTAs come
+    // in by bulk copies at once; slot 0 carries the running sum between
+    // batches.  False if a wait gave up.
+    auto finish_tile = [&](int t, int c_lo, int c_hi) -> bool {
+      const TileInfo ti = tile_info(tp, t);
+      const int64_t grow = ti.row0 + r;
+      const bool live = grow < ti.nrows;
+      __half *yrow = p.y[ti.m] + grow;
+      const int64_t ldy = p.ldy[ti.m];
+      bool have = false;
+      for (int k = c_lo; k <= c_hi;) {
+        const int s0 = have ? 1 : 0;
+        const int nb = tp.fx_cap - s0 < c_hi - k + 1 ? tp.fx_cap - s0 : c_hi - k + 1;
+        if (lane == 0) {
+          asm volatile("fence.proxy.async;" ::: "memory");
+          asm volatile(
+              "{\n\t.reg .b64 t;\n\t"
+              "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(fxb),
+              "r"((uint32_t)nb * blk)
+              : "memory");
+          for (int i = 0; i < nb; ++i) {
+            const float *src =
+                tp.part + (size_t)(((k + i) * 2 + part_slot(tp, k + i, t)) * 4 + qtr) * Np * 32;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                "%2, [%3];" ::"r"(smem_u32(stg) + (uint32_t)(s0 + i) * blk),
+                "l"(src), "r"(blk), "r"(fxb)
+                : "memory");
+          }
+        }
+        const bool okf = mbar_wait(fxb, fx_uses & 1, abort_flag);
+        ++fx_uses;
+        if (!__all_sync(0xffffffffu, okf)) {
+          if (lane == 0) mbar_drain(fxb, (fx_uses - 1) & 1);
+          return false;
+        }
+        // running sums into slot 0; element (n, lane) of a block sits at
+        // float ((n / 4) * 32 + lane) * 4 + n % 4
+        float4 *sv = reinterpret_cast<float4 *>(stg) + lane;
+        for (int n0 = 0; n0 < tp.B; n0 += 16) {
+          float4 acc[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            acc[q] = have ? sv[(n0 / 4 + q) * 32] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int i = 0; i < nb; ++i) {
+            const float4 *src = sv + (size_t)(s0 + i) * (blk / 16) + (n0 / 4) * 32;
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = src[q * 32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[q].x += v[q].x;
+              acc[q].y += v[q].y;
+              acc[q].z += v[q].z;
+              acc[q].w += v[q].w;
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sv[(n0 / 4 + q) * 32] = acc[q];
+        }
+        have = true;
+        k += nb;
+        __syncwarp();
+      }
+      // the finished rows
+      if (live) {
+        const float4 *sv = reinterpret_cast<const float4 *>(stg) + lane;
+        for (int n0 = 0; n0 < tp.B; n0 += 4) {
+          const float4 a = sv[(n0 / 4) * 32];
+          const float e[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (n0 + q < tp.B) yrow[(int64_t)(n0 + q) * ldy] = __float2half_rn(e[q]);
+        }
+      }
+      __syncwarp();
+      return true;
+    };
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int j = 0;
+    int def_t = -1, def_lo = 0, def_hi = 0;  // a cut tile to finish after the last MMA
+    bool aborted = false;
     for (int u = u_begin; u < u_end; ++j) {
       const int t = u / KT;
       const int k0 = u - t * KT;
@@ -466,14 +565,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       const int64_t ldy = p.ldy[ti.m];
       const int db = j & 1;
       const bool ok = mbar_wait(smem_u32(&dfull[db]), (j >> 1) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (!__all_sync(0xffffffffu, ok)) {
+        aborted = true;
+        break;
+      }
       fence_after();
       const uint32_t dcol = tmem + lane_base + (uint32_t)(db * 2 * Np);
-      // partial of a cut tile: row r's Np values contiguous in its slot
+      // partial of a cut tile: float4 (n / 4, lane) of its (slot, quarter) block
       float4 *mine = nullptr;
-      if (cut)
-        mine = reinterpret_cast<float4 *>(tp.part +
-                                          ((size_t)(cta * 2 + part_slot(tp, cta, t)) * kM + r) * Np);
+      float *mine_c = reinterpret_cast<float *>(b_st) + r;  // kCluster: [n][kM] in its own rings
+      if (cut && tp.split != kCluster)
+        mine = reinterpret_cast<float4 *>(
+                   tp.part + (size_t)((cta * 2 + part_slot(tp, cta, t)) * 4 + qtr) * Np * 32) +
+               lane;
       for (int c0 = 0; c0 < Np; c0 += 16) {
         float vb[16], vo[16], y[16];
         tmem_ld16(dcol + (uint32_t)Np + c0, vb);
@@ -488,59 +592,41 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
             if (live && c0 + jj < tp.B) yrow[(int64_t)(c0 + jj) * ldy] = __float2half_rn(y[jj]);
+        } else if (tp.split == kCluster) {  // this CTA's only segment; its rings are free
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) mine_c[(c0 + jj) * kM] = y[jj];
         } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mine[c0 / 4 + k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+          for (int q = 0; q < 4; ++q)
+            mine[(c0 / 4 + q) * 32] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
         }
       }
       fence_before();
       mbar_arrive(smem_u32(&dempty[db]));  // the MMAs may reuse this buffer
-      if (cut) {
-        // Publish the partial; the warp that brings the count of its lane
-        // quarter to the number of contributors adds them all in CTA order.
-        const int c_lo = unit_owner(tp, t * KT), c_hi = unit_owner(tp, (t + 1) * KT - 1);
-        __threadfence();
-        __syncwarp();
-        unsigned prev = 0;
-        if (lane == 0) prev = atomicAdd(tp.cnt + c_lo * 4 + qtr, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == (unsigned)(c_hi - c_lo)) {
-          __threadfence();
-          for (int n0 = 0; n0 < tp.B; n0 += 16) {
-            float acc[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.0f;
-            // four contributors' loads in flight, added in CTA order
-            for (int qq = c_lo; qq <= c_hi; qq += 4) {
-              float4 v[4][4];
-#pragma unroll
-              for (int a = 0; a < 4; ++a)
-                if (qq + a <= c_hi) {
-                  const float4 *src = reinterpret_cast<const float4 *>(
-                      tp.part + ((size_t)((qq + a) * 2 + part_slot(tp, qq + a, t)) * kM + r) * Np + n0);
-#pragma unroll
-                  for (int k = 0; k < 4; ++k) v[a][k] = __ldcg(src + k);
-                }
-#pragma unroll
-              for (int a = 0; a < 4; ++a)
-                if (qq + a <= c_hi) {
-#pragma unroll
-                  for (int k = 0; k < 4; ++k) {
-                    acc[4 * k] += v[a][k].x;
-                    acc[4 * k + 1] += v[a][k].y;
-                    acc[4 * k + 2] += v[a][k].z;
-                    acc[4 * k + 3] += v[a][k].w;
-                  }
-                }
-            }
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              if (live && n0 + jj < tp.B) yrow[(int64_t)(n0 + jj) * ldy] = __float2half_rn(acc[jj]);
-          }
-        }
+      if (!cut || tp.split == kCluster) continue;
+      // Publish the partial (release: the warp's stores, ordered by the warp
+      // barrier, before the count); the warp that brings the count of its
+      // lane quarter to the number of contributors adds them all in CTA order.
+      const int c_lo = unit_owner(tp, t * KT), c_hi = unit_owner(tp, (t + 1) * KT - 1);
+      __syncwarp();
+      unsigned prev = 0;
+      if (lane == 0)
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(tp.cnt + c_lo * 4 + qtr)
+                     : "memory");
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev != (unsigned)(c_hi - c_lo)) continue;
+      // (lane 0's acquire orders its bulk copies of the others' partials)
+      if (u == u_end) {
+        if (!finish_tile(t, c_lo, c_hi)) aborted = true;
+      } else {  // only a first segment: finish it after the last MMA
+        def_t = t;
+        def_lo = c_lo;
+        def_hi = c_hi;
       }
     }
+    if (def_t >= 0 && !aborted) finish_tile(def_t, def_lo, def_hi);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -670,6 +756,40 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       for (int k = q > NB ? q - NB : 0; k < q; ++k) mbar_drain(smem_u32(&bfull[k % NB]), (k / NB) & 1);
   }
 
+  __syncwarp();
+  if (tp.split == kCluster && tp.S > 1) {
+    // Cluster reduction through distributed shared memory: each CTA holds
+    // the partial of its K tiles, [n][row] fp32 at the start of its rings;
+    // CTA k adds rows [k kM / S, (k + 1) kM / S) over the S CTAs in rank
+    // order and stores them.
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+    const int S = tp.S, rank = cta % S, t = cta / S;
+    const TileInfo ti = tile_info(tp, t);
+    const int rlo = kM * rank / S, nr = kM * (rank + 1) / S - rlo;
+    const uint32_t local = smem_u32(b_st);
+    for (int e = tid; e < nr * tp.B; e += kThreadsTc) {
+      const int n = e / nr, rr = rlo + e % nr;
+      const uint32_t off = (uint32_t)(n * kM + rr) * 4u;
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)  // all S loads in flight, then the sum in rank order
+        if (q < S) {
+          uint32_t ra;
+          asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local + off), "r"(q));
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v[q]) : "r"(ra));
+        }
+      float acc = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < S) acc += v[q];
+      const int64_t grow = ti.row0 + rr;
+      if (grow < ti.nrows) p.y[ti.m][(int64_t)n * p.ldy[ti.m] + grow] = __float2half_rn(acc);
+    }
+    // keep every CTA's shared memory alive until all remote reads are done
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+  }
   fence_before();
   __syncthreads();
   fence_after();
@@ -750,13 +870,11 @@ static int tc_b_stages(int Np) {
 }
 
 size_t tc_smem_bytes(bool int4, int Np) {
-  const size_t need = 1024 + (size_t)tc_b_stages(Np) * Np * kKT * 2 +
-                      (int4 ? RawRing<true>::BYTES : RawRing<false>::BYTES) +
-                      (2 * kMaxAStages + 2 * kMaxBStages + 2 * kMaxRaw + 4) * 8 + 16;
-  // more than half of an SM's shared memory, so that one CTA (which holds
-  // all 512 TMEM columns) runs per SM
-  const size_t one_per_sm = 120 * 1024;
-  return need > one_per_sm ? need : one_per_sm;
+  // barriers, activation ring, raw-code ring; the host launches with the
+  // device's whole per-CTA maximum (one CTA per SM, which holds all 512 TMEM
+  // columns), the space past the rings staging the cut-tile reduction
+  return 1024 + kBarBytes + (size_t)tc_b_stages(Np) * Np * kKT * 2 +
+         (int4 ? RawRing<true>::BYTES : RawRing<false>::BYTES);
 }
 
 namespace {
@@ -800,6 +918,50 @@ qz_status codes_map(CUtensorMap *map, const uint8_t *codes, int64_t ld, int64_t 
 }
 
 }  // namespace
+
+// Clusters of S CTAs of the GEMM kernel that the GPU holds at once (one CTA
+// per SM; GPCs whose SM count is not a multiple of S strand some SMs).
+// Asked of the runtime once per device, format and S.
+template <typename Kern>
+qz_status tc_resident_clusters(bool int4, Kern kern, int S, size_t smem, int sms, int *out) {
+  if (S == 1) {
+    *out = sms;
+    return QZ_OK;
+  }
+  constexpr int kDev = 16;
+  static int cache[kDev][2][4];  // 0 = not asked yet, -1 = not launchable
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  const int si = S == 2 ? 1 : (S == 4 ? 2 : 3);
+  if (dev < 0 || dev >= kDev) {
+    *out = 0;
+    return QZ_OK;
+  }
+  int &c = cache[dev][int4 ? 1 : 0][si];
+  if (c == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)S);
+    cfg.blockDim = dim3(kThreadsTc);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = (unsigned)S;
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // not a sticky error: this S is just not used
+      n = -1;
+    }
+    c = n > 0 ? n : -1;
+  }
+  *out = c > 0 ? c : 0;
+  return QZ_OK;
+}
 
 qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_rows,
                     void *workspace, size_t workspace_bytes, cudaStream_t s) {
@@ -846,39 +1008,103 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   if (tiles * tp.KT > (int64_t)INT32_MAX) return QZ_ERR_UNSUPPORTED;
   tp.tiles = (int)tiles;
   tp.U = (int)(tiles * tp.KT);
-  // One CTA per SM.  With a workspace (room for partials) the units are cut
-  // evenly, at least kMinUnits per CTA; without one each CTA takes whole tiles.
-  const int gmax = di.sms < kMaxCtas ? di.sms : kMaxCtas;
-  if (tp.ws) {
-    tp.split = 1;
-    const int want = tp.U / kMinUnits;
-    tp.G = want < 1 ? 1 : (want < gmax ? want : gmax);
-  } else {
-    tp.split = 0;
-    tp.G = tp.tiles < gmax ? tp.tiles : gmax;
+  if (tc_smem_bytes(int4, tp.Np) > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
+  const size_t smem = (size_t)di.max_smem_optin;
+  {
+    // staging per lane quarter: whole partials of one quarter (Np x 32 fp32)
+    const size_t blk = (size_t)tp.Np * 32 * 4;
+    const size_t per_q = (smem - 1024 - kBarBytes) / 4 / blk * blk;
+    tp.fx_bytes = (uint32_t)per_q;
+    tp.fx_cap = (int)(per_q / blk);
+    if (tp.fx_cap < 2) return QZ_ERR_UNSUPPORTED;
   }
-  const size_t smem = tc_smem_bytes(int4, tp.Np);
-  if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
   auto kern = int4 ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_status(e);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  if (e != cudaSuccess) return cuda_status(e);
+
+  // Schedule.  Estimated times in microseconds (GB300 measurements): a
+  // launch costs kStart (start-up to the first MMA and the drain after the
+  // last), a unit 0.9 (8 MMAs); stream-K adds the L2 reduction of its cut
+  // tiles, a cluster of S > 1 its shared-memory reduction, and clusters come
+  // in waves of what fits on the GPCs at once.
+  const int gmax = di.sms < kMaxCtas ? di.sms : kMaxCtas;
+  const double kStart = 3.5, kUnit = 0.9;
+  double best = 1e30;
+  int best_mode = kWhole, best_S = 1;
+  {
+    const int per = (tp.tiles + gmax - 1) / gmax;  // whole tiles per CTA
+    best = kStart + kUnit * per * tp.KT;
+  }
+  if (tp.ws) {
+    const int want = tp.U / kMinUnits;
+    const int G = want < 1 ? 1 : (want < gmax ? want : gmax);
+    const int per = (tp.U + G - 1) / G;
+    const bool cuts = !(tp.U % G == 0 && (tp.U / G) % tp.KT == 0);
+    const double t = kStart + kUnit * per + (cuts ? 5.5 + tp.B / 16.0 : 0.0);
+    if (t < best) {
+      best = t;
+      best_mode = kStreamK;
+    }
+  }
+  for (int S = 1; S <= 8; S *= 2) {
+    if (S > 1 && tp.KT < 2 * S) break;
+    int clusters = 0;
+    st = tc_resident_clusters(int4, kern, S, smem, di.sms, &clusters);
+    if (st != QZ_OK) return st;
+    if (clusters < 1) continue;
+    const int waves = (tp.tiles + clusters - 1) / clusters;
+    const double t = waves * (kStart + kUnit * ((tp.KT + S - 1) / S) +
+                              (S > 1 ? 1.0 + tp.B / 40.0 : 0.0));
+    if (t < best - 1e-9) {
+      best = t;
+      best_mode = kCluster;
+      best_S = S;
+    }
+  }
+  tp.split = best_mode;
+  tp.S = best_S;
+  if (best_mode == kStreamK) {
+    const int want = tp.U / kMinUnits;
+    tp.G = want < 1 ? 1 : (want < gmax ? want : gmax);
+  } else if (best_mode == kCluster) {
+    tp.G = tp.tiles * tp.S;
+    tp.cnt = nullptr;  // no cut-tile counters (and none to clear)
+  } else {
+    tp.G = tp.tiles < gmax ? tp.tiles : gmax;
+    tp.cnt = nullptr;
+  }
+
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)tp.G);
   cfg.blockDim = dim3(kThreadsTc);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (g.overlap) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  const int n_pdl = na;
+  if (tp.split == kCluster) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)tp.S;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = g.overlap ? 1 : 0;
+  cfg.numAttrs = na;
   if (tp.ws) {  // gather the activations once (and clear the counters), then the GEMM
     cudaLaunchConfig_t pc = {};
     pc.gridDim = dim3((unsigned)tp.KT);
     pc.blockDim = dim3(256);
     pc.stream = s;
     pc.attrs = attr;
-    pc.numAttrs = g.overlap ? 1 : 0;
+    pc.numAttrs = n_pdl;
     auto prep = int4 ? tc_xprep_kernel<true> : tc_xprep_kernel<false>;
     e = cudaLaunchKernelEx(&pc, prep, tp, reinterpret_cast<uint8_t *>(workspace));
     if (e != cudaSuccess) return cuda_status(e);
