@@ -162,10 +162,27 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(wl_name: str, budget_s: float = 12.0):
+def cpu_baseline_one_thread(wl_name: str):
+    """The same oracle on one host thread (BLAS pinned to one thread in a
+    child process, since the thread count is fixed when numpy loads), on the
+    gate matrix of layer 0: (GB/s, sample text), or None if it fails."""
+    code = ("import json, bench; g, t, smp, th = bench.cpu_baseline(%r, 4.0, ('gate',)); "
+            "print(json.dumps([g, smp]))" % wl_name)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                             text=True, timeout=120)
+        g, smp = json.loads(out.stdout.strip().splitlines()[-1])
+        return g, smp
+    except Exception:
+        return None
+
+
+def cpu_baseline(wl_name: str, budget_s: float = 12.0, only=None):
     """The CPU oracle, as it stands, on a bounded sample: the products of one
-    layer's matrices (quantized by the oracle itself), repeated until about
-    budget_s of CPU work.  Returns (GB/s, seconds, sample text, threads)."""
+    layer's matrices (quantized by the oracle itself; `only`: a subset of
+    them), repeated until about budget_s of CPU work.  Returns (GB/s,
+    seconds, sample text, threads)."""
     import numpy as np
 
     from oracle import qz_oracle as O
@@ -174,6 +191,8 @@ def cpu_baseline(wl_name: str, budget_s: float = 12.0):
     wl = S.WORKLOADS[wl_name]
     mats = []
     for m in S.MATS:
+        if only is not None and m not in only:
+            continue
         N, K = wl.shape(m)
         W = S.weight(N, K, S.matrix_seed(wl, 0, m), dist=wl.dist).numpy()
         x = S.activation(1, K, 11 + len(mats)).numpy()
@@ -204,7 +223,8 @@ def cpu_baseline(wl_name: str, budget_s: float = 12.0):
             threads = max(i.get("num_threads", 1) for i in info)
     except Exception:
         pass
-    sample = (f"oracle fp64 products of all 7 matrices of layer 0 of {wl_name}, "
+    which = "all 7 matrices" if only is None else "+".join(only)
+    sample = (f"oracle fp64 products of {which} of layer 0 of {wl_name}, "
               f"{reps} pass(es), {done_bytes / 1e9:.2f} GB of packed weights")
     return done_bytes / t_total / 1e9, t_total, sample, threads
 
@@ -702,6 +722,10 @@ def main():
         gbs_cpu, t_cpu, sample, threads = cpu_baseline(a.workload)
         cpu = {"value": round(gbs_cpu, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": sample, "seconds": round(t_cpu, 2)}
+        one = cpu_baseline_one_thread(a.workload)
+        if one is not None:
+            cpu["single_thread"] = {"value": round(one[0], 4), "unit": "GB/s", "cores": 1,
+                                    "sample": one[1]}
 
     if rank != 0:
         if dist_ctx is not None:

@@ -290,6 +290,49 @@ def test_tensor_core_without_workspace(fmt, B):
         assert_close(a, y_ref, a_ref, f"{fmt} B={B} workspace={ws}")
 
 
+@pytest.mark.parametrize("B", [16, 64])
+def test_tensor_core_grouped_large_int4(B):
+    """q,k,v-sized grouped call (84 row tiles, ragged ends) at K = 4096: the
+    persistent schedule cuts tiles between SMs, also across the matrix
+    boundaries; every output of the three matrices against the oracle."""
+    K, n_out = 4096, 41
+    Ns = [4096, 4096 + 300, 2048 + 77]
+    Ws = [S.weight(n, K, 9600 + i, device=DEV) for i, n in enumerate(Ns)]
+    prof = S.x_profile(K, n_out, 9610, device=DEV)
+    colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+    for W in Ws:
+        qz().saliency_accumulate(W, colsum)
+    perm = qz().select_outliers(colsum, prof, n_out)
+    ws = [qz().quantize_int4_outlier(W, perm, n_out) for W in Ws]
+    X = S.activation(B, K, 9620 + B, device=DEV)
+    Ys = qz().gemm_int4_outlier_grouped(ws, X)
+    assert qz().device_error() == 0
+    pn = perm.cpu().numpy()
+    Xn = X.cpu().numpy()
+    for i, (W, Y) in enumerate(zip(Ws, Ys)):
+        wo, q4, s = O.int4o_quantize(W.cpu().numpy(), pn, n_out)
+        y_ref, a_ref = O.int4o_product_ref(wo, q4, s, pn, n_out, K, Xn)
+        assert_close(Y, y_ref, a_ref, f"grouped int4 large B={B} m={i}")
+
+
+@pytest.mark.parametrize("B", [16, 64])
+def test_tensor_core_grouped_large_int8(B):
+    """gate,up-sized grouped INT8 call (225 row tiles, ragged ends, K = 3584):
+    every output against the oracle."""
+    K = 3584
+    Ns = [14336 - 77, 14336 + 45]
+    Ws = [S.weight(n, K, 9700 + i, device=DEV) for i, n in enumerate(Ns)]
+    ws = [qz().quantize_int8(W) for W in Ws]
+    X = S.activation(B, K, 9720 + B, device=DEV)
+    Ys = qz().gemm_int8_grouped(ws, X)
+    assert qz().device_error() == 0
+    Xn = X.cpu().numpy()
+    for i, (W, Y) in enumerate(zip(Ws, Ys)):
+        q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+        y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, Xn)
+        assert_close(Y, y_ref, a_ref, f"grouped int8 large B={B} m={i}")
+
+
 @pytest.mark.parametrize("fmt", ["int8", "int4o"])
 def test_tensor_core_more_tiles_than_sms_without_workspace(fmt):
     """160 row tiles and no workspace: persistent CTAs take whole tiles, some
