@@ -348,7 +348,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     // raw ring (filled by the code loader warp); each thread converts its bytes.
     constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB, HB = RawRing<INT4>::HB;
     const uint32_t raw_me = smem_u32(raw) + (uint32_t)r * RB + (uint32_t)h * HB;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Weights only: no wait for the preceding kernel (under programmatic
+    // launch the caller guarantees that nothing in flight writes them).
     int i = 0;       // code tiles taken from the raw ring so far
     int t_cur = -1;  // tile of the previous unit
     TileInfo ti = {0, 0, 0};
@@ -1009,7 +1010,12 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   tp.tiles = (int)tiles;
   tp.U = (int)(tiles * tp.KT);
   if (tc_smem_bytes(int4, tp.Np) > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
-  const size_t smem = (size_t)di.max_smem_optin;
+  // 200 KB: room to stage six partials of a lane quarter at batch 64, and
+  // below the SM's total, so that a small kernel launched before this one
+  // (the input gather) can still run beside it under programmatic launch
+  const size_t smem = (size_t)di.max_smem_optin < (size_t)200 * 1024 ? (size_t)di.max_smem_optin
+                                                                      : (size_t)200 * 1024;
+  if (smem < tc_smem_bytes(int4, tp.Np)) return QZ_ERR_UNSUPPORTED;
   {
     // staging per lane quarter: whole partials of one quarter (Np x 32 fp32)
     const size_t blk = (size_t)tp.Np * 32 * 4;
