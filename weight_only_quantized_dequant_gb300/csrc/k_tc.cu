@@ -16,11 +16,14 @@
 //  * One thread issues tcgen05.mma (kind::f16, fp32 accumulate) into two
 //    TMEM accumulators: outlier channels and INT4 background, so that the
 //    per-row scale multiplies the background only: y = D_out + s_i * D_bg.
-//  * Persistent stream-K schedule: the (tile, K tile) work units of all
-//    matrices of the call are cut into one contiguous range per CTA, one CTA
-//    per SM, so every SM gets the same number of MMAs whatever the tile
-//    count.  A tile cut between CTAs is finished by the last of its CTAs to
-//    arrive, which adds the fp32 partials in CTA order (deterministic).
+//  * Schedules of the (tile, K tile) work units of all matrices of the call,
+//    chosen per call by a cost model: persistent stream-K (one contiguous
+//    range per CTA, one CTA per SM, so every SM gets the same number of MMAs
+//    whatever the tile count; a tile cut between CTAs is finished by the
+//    last of its CTAs to arrive, which adds the fp32 partials in CTA order),
+//    a cluster of S CTAs per tile that split its K tiles and add their
+//    partials in rank order through distributed shared memory (few tiles),
+//    or persistent whole tiles (no workspace).  All are deterministic.
 //  * The accumulators are double-buffered, so the epilogue warps drain one
 //    tile while the MMAs of the next run.  Every wait is bounded in time and
 //    reports a timeout through a device flag.
