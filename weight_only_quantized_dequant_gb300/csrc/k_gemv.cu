@@ -186,6 +186,11 @@ struct Ring {
   static constexpr int MINB = 1;               // CTAs per SM the registers allow
   static constexpr uint32_t STAGE_ROW = RPS * kRoundBytes;  // bytes of one row in a stage
 };
+// gemv_smem_bytes sizes every B > 1 by Ring<2>
+static_assert(Ring<3>::NS == Ring<2>::NS && Ring<3>::R == Ring<2>::R &&
+                  Ring<3>::STAGE_ROW == Ring<2>::STAGE_ROW && Ring<4>::NS == Ring<2>::NS &&
+                  Ring<4>::R == Ring<2>::R && Ring<4>::STAGE_ROW == Ring<2>::STAGE_ROW,
+              "one ring shape for all batches > 1");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
   return (uint32_t)__cvta_generic_to_shared(ptr);
@@ -872,8 +877,12 @@ size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p) {
   const size_t cs = int4 ? 80 : 48;  // padded staged fp16 bytes per chunk
   const size_t rounds = p.cpr > 0 ? (size_t)(p.cpr + 31) / 32 : 1;
   const size_t staged = (rounds * 32 * cs + (int4 ? (size_t)p.ocpr * 16 : 0)) * (size_t)B;
-  const size_t R = B == 1 ? 2 : 1, NS = 2, RPS = B == 1 ? 4 : 2;
-  const size_t ring = (size_t)kWarps * NS * R * RPS * kRoundBytes;
+  // the ring and its barriers as the kernel carves them (Ring<B> is the same
+  // for every B > 1)
+  const size_t NS = B == 1 ? Ring<1>::NS : Ring<2>::NS;
+  const size_t R = B == 1 ? Ring<1>::R : Ring<2>::R;
+  const size_t stage_row = B == 1 ? Ring<1>::STAGE_ROW : Ring<2>::STAGE_ROW;
+  const size_t ring = (size_t)kWarps * NS * R * stage_row;
   return ((staged + 127) & ~(size_t)127) + ring + (size_t)kWarps * NS * 8;
 }
 
