@@ -24,9 +24,10 @@
 //    immediate offset.
 //  * A warp computes R rows at once: each staged granule is read once for
 //    all R rows, halving the shared-memory traffic per weight.
-//  * Loads are software-pipelined in registers: the next group of chunks
-//    (possibly of the next rows) is issued before the current one is
-//    consumed, and each warp bulk-prefetches its following rows into L2.
+//  * Each warp streams its rows' codes through its own ring of shared-memory
+//    stages, filled by bulk copies (cp.async.bulk completing on an mbarrier)
+//    one stage ahead of the stage it computes; the first rows of each CTA are
+//    pulled into L2 before the wait for the previous kernel.
 //  * CTAs own contiguous, equal row ranges; the grid is the SM count times
 //    the resident CTAs per SM.
 #include "qz_internal.cuh"
@@ -673,7 +674,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
   for (int k = 0; k < sp.n; ++k) {
     const GemvParams &p = sp.t[k];
     const Work w = plan(k);
-    const int cpr = p.cpr;
     const int staged = (w.Jw > 0 ? w.Jw : 1) * 32;
     const uint32_t bstride = (uint32_t)staged * CS;
     __half *xo = reinterpret_cast<__half *>(smem_raw + bstride);
