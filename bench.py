@@ -229,6 +229,23 @@ def cpu_baseline(wl_name: str, budget_s: float = 12.0, only=None):
     return done_bytes / t_total / 1e9, t_total, sample, threads
 
 
+def max_over_ranks(dist_ctx, values, device=None):
+    """Each timing's largest value over all ranks: the slowest replica sets
+    the job's time.  Without a process group, the values themselves."""
+    if dist_ctx is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist_ctx.all_reduce(t, op=dist_ctx.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_gbs(world: int, bytes_per_step: float, ms_per_step: float) -> float:
+    """Whole-job GB/s: each of the world replicas moves bytes_per_step per
+    step, and the job's step takes ms_per_step (the slowest rank)."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def run_reference(a):
     """--impl reference: the CPU oracle timed on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -681,12 +698,7 @@ def main():
 
     r = measure(a.workload, a.batch, a.steps, a.warmup, dist_ctx, clocks=(rank == 0), device=device,
                 layers=a.layers, overlap=not a.no_overlap, fused=a.fused)
-    ms_all = r["ms_per_step"]
-    e2e_all = r["e2e_ms"]
-    if dist_ctx is not None:
-        t = torch.tensor([r["ms_per_step"], r["e2e_ms"]], device=device)
-        dist_ctx.all_reduce(t, op=dist_ctx.ReduceOp.MAX)
-        ms_all, e2e_all = float(t[0]), float(t[1])
+    ms_all, e2e_all = max_over_ranks(dist_ctx, [r["ms_per_step"], r["e2e_ms"]], device)
 
     extra = {}
     if a.extra and rank == 0:
@@ -732,7 +744,7 @@ def main():
             dist_ctx.destroy_process_group()
         return 0
     peak, peak_src = peaks()
-    value = world * r["bytes_per_step"] / (ms_all * 1e-3) / 1e9
+    value = job_gbs(world, r["bytes_per_step"], ms_all)
     dom = r["dominant"]
     if a.batch <= 4:
         roofline = {"bound": "hbm", "achieved": round(dom["gbs"], 2), "peak": peak,
@@ -782,7 +794,7 @@ def main():
         "peak_source": f"{peak:.0f} GB/s of {peak_src}",
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * r["bytes_per_step"] / (e2e_all * 1e-3) / 1e9, 2),
+        "e2e": {"value": round(job_gbs(world, r["bytes_per_step"], e2e_all), 2),
                 "unit": "GB/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "ms_per_step": round(e2e_all, 4)},
         "gpu_launches": r["launches_per_step"] * a.steps,
