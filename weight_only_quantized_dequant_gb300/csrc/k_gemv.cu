@@ -26,8 +26,8 @@
 //    all R rows, halving the shared-memory traffic per weight.
 //  * Each warp streams its rows' codes through its own ring of shared-memory
 //    stages, filled by bulk copies (cp.async.bulk completing on an mbarrier)
-//    one stage ahead of the stage it computes; the first rows of each CTA are
-//    pulled into L2 before the wait for the previous kernel.
+//    one stage ahead of the stage it computes; each warp requests its first
+//    stage before the wait for the previous kernel.
 //  * CTAs own contiguous, equal row ranges; the grid is the SM count times
 //    the resident CTAs per SM.
 #include "qz_internal.cuh"
@@ -37,7 +37,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int64_t kPrefetchBytes = 64 * 1024;  // per CTA, issued before the wait
+constexpr int64_t kPrefetchBytes = 64 * 1024;  // sequence kernel: next product's rows per CTA
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   uint4 r;
@@ -268,25 +268,9 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
   const int64_t r1 = p.total_rows * (blockIdx.x + 1) / gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // The first rows of this CTA are pulled into L2 right away.  With
-  // programmatic overlap this CTA may start while the previous kernel on the
-  // stream is still running; the weights are static by the caller's promise,
-  // and x (which that kernel may produce) is only read after the wait.
-  if (threadIdx.x == 0) {
-    int64_t budget = kPrefetchBytes;
-    int64_t r = r0;
-    for (int m = 0; m < p.n_mats && budget > 0 && r < r1; ++m) {
-      const int64_t m_lo = m ? p.row_end[m - 1] : 0, m_hi = p.row_end[m];
-      if (r >= m_hi) continue;
-      const int64_t e = r1 < m_hi ? r1 : m_hi;
-      int64_t bytes = (e - r) * p.ld_codes[m];
-      if (bytes > budget) bytes = budget;
-      bytes &= ~(int64_t)15;
-      if (bytes > 0) prefetch_l2(p.codes[m] + (r - m_lo) * p.ld_codes[m], (uint32_t)bytes);
-      budget -= bytes;
-      r = e;
-    }
-  }
+  // No L2 prefetch of the CTA's first rows: measured, a 16-256 KiB prefetch
+  // before the wait gained nothing (16 KiB) or lost 5-10% (the ring's own
+  // first stages are already requested before the wait).
   if (lane == 0) {
     for (int st = 0; st < NS; ++st)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[warp * NS + st]))
