@@ -246,9 +246,11 @@ __device__ __forceinline__ void locate(const Bounds &bd, int r, int &m, int &i) 
   i = r - lo;
 }
 
-template <bool INT4, int B>
-__global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
+// W: warps per CTA (16, or 20 at batch 1 when shared memory allows).
+template <bool INT4, int B, int W>
+__global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
     gemv_kernel(const __grid_constant__ GemvParams p) {
+  constexpr int kWarps = W, kThreads = W * 32;
   constexpr int R = Ring<B>::R, NS = Ring<B>::NS, kRPS = Ring<B>::RPS;
   constexpr uint32_t kStageRow = Ring<B>::STAGE_ROW;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, Ring<B>::MINB)
 // the y of an earlier product.  The weight ring is not drained at the
 // barriers: the producers run into the next product's rows (weights are
 // static), and thread 0 pulls the next product's first rows into L2 while the
-// current one is computed.  Same per-row arithmetic as gemv_kernel<INT4, 1>.
+// current one is computed.  Same per-row arithmetic as gemv_kernel<INT4, 1, W>.
 // The grid must be co-resident (one CTA per SM; every wait is bounded).
 // ---------------------------------------------------------------------------
 template <bool INT4>
@@ -819,30 +821,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
   }
 }
 
-template <bool INT4, int B>
-qz_status launch_t(const GemvParams &p, cudaStream_t s) {
+// Shared memory of gemv_kernel with W warps: staged inputs, then the ring
+// and its barriers as the kernel carves them (Ring<B> is the same for every
+// B > 1).
+size_t gemv_smem_bytes_w(bool int4, int B, const GemvParams &p, int W) {
+  const size_t cs = int4 ? 80 : 48;  // padded staged fp16 bytes per chunk
+  const size_t rounds = p.cpr > 0 ? (size_t)(p.cpr + 31) / 32 : 1;
+  const size_t staged = (rounds * 32 * cs + (int4 ? (size_t)p.ocpr * 16 : 0)) * (size_t)B;
+  const size_t NS = B == 1 ? Ring<1>::NS : Ring<2>::NS;
+  const size_t R = B == 1 ? Ring<1>::R : Ring<2>::R;
+  const size_t stage_row = B == 1 ? Ring<1>::STAGE_ROW : Ring<2>::STAGE_ROW;
+  const size_t ring = (size_t)W * NS * R * stage_row;
+  return ((staged + 127) & ~(size_t)127) + ring + (size_t)W * NS * 8;
+}
+
+template <bool INT4, int B, int W>
+qz_status launch_w(const GemvParams &p, const DeviceInfo &di, cudaStream_t s) {
   constexpr int R = Ring<B>::R;
-  auto kern = gemv_kernel<INT4, B>;
-  DeviceInfo di;
-  qz_status st = device_info(&di);
-  if (st != QZ_OK) return st;
-  const size_t smem = gemv_smem_bytes(INT4, B, p);
+  auto kern = gemv_kernel<INT4, B, W>;
+  const size_t smem = gemv_smem_bytes_w(INT4, B, p, W);
   if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return cuda_status(e);
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, W * 32, smem);
   if (e != cudaSuccess) return cuda_status(e);
   if (occ < 1) return QZ_ERR_UNSUPPORTED;
   // Whole waves only: every SM gets the same number of CTAs (and CTAs equal
   // row ranges), so no SM carries a second CTA while another idles.
   int64_t per_sm = occ;
-  while (per_sm > 1 && (int64_t)di.sms * per_sm * kWarps * R > p.total_rows * 2) --per_sm;
+  while (per_sm > 1 && (int64_t)di.sms * per_sm * W * R > p.total_rows * 2) --per_sm;
   int64_t grid = (int64_t)di.sms * per_sm;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(W * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -855,19 +868,26 @@ qz_status launch_t(const GemvParams &p, cudaStream_t s) {
   return launch_status();
 }
 
+// Batch 1 takes 20 warps per CTA when their rings fit in shared memory:
+// more bytes in flight per SM (measured on GB300: Gemma INT8 +1%, 3B INT4
+// +5%, 70B INT4 +2%; 24 warps lost 1% on Gemma).  Batches 2..4 keep 16.
+template <bool INT4, int B>
+qz_status launch_t(const GemvParams &p, cudaStream_t s) {
+  DeviceInfo di;
+  qz_status st = device_info(&di);
+  if (st != QZ_OK) return st;
+  const size_t cap = (size_t)di.max_smem_optin;
+  if constexpr (B == 1)
+    if (gemv_smem_bytes_w(INT4, B, p, 20) <= cap) return launch_w<INT4, B, 20>(p, di, s);
+  return launch_w<INT4, B, 16>(p, di, s);
+}
+
 }  // namespace
 
+// The 16-warp size: the least any batch-1..4 launch needs (the path choice
+// between CUDA cores and tensor cores tests this).
 size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p) {
-  const size_t cs = int4 ? 80 : 48;  // padded staged fp16 bytes per chunk
-  const size_t rounds = p.cpr > 0 ? (size_t)(p.cpr + 31) / 32 : 1;
-  const size_t staged = (rounds * 32 * cs + (int4 ? (size_t)p.ocpr * 16 : 0)) * (size_t)B;
-  // the ring and its barriers as the kernel carves them (Ring<B> is the same
-  // for every B > 1)
-  const size_t NS = B == 1 ? Ring<1>::NS : Ring<2>::NS;
-  const size_t R = B == 1 ? Ring<1>::R : Ring<2>::R;
-  const size_t stage_row = B == 1 ? Ring<1>::STAGE_ROW : Ring<2>::STAGE_ROW;
-  const size_t ring = (size_t)kWarps * NS * R * stage_row;
-  return ((staged + 127) & ~(size_t)127) + ring + (size_t)kWarps * NS * 8;
+  return gemv_smem_bytes_w(int4, B, p, kWarps);
 }
 
 size_t gemv_seq_smem_bytes(bool int4, const SeqParams &sp, uint32_t *xs_bytes) {
