@@ -34,7 +34,7 @@ DOMINANT_GROUP = 2  # {gate, up}: the largest launch of every layer
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=600)  # ~1 s timed: several clock samples
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="gemma2_9b_int8")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -112,15 +112,26 @@ def tensor_peak():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing.
+    Each sample carries nvidia-smi's timestamp; the summary keeps the samples
+    taken inside the window between mark_start() and mark_end() (the timed
+    region), and says how many there were."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.window = None
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def mark_start(self):
+        self.window = [time.time(), None]
+
+    def mark_end(self):
+        if self.window:
+            self.window[1] = time.time()
 
     def __enter__(self):
         try:
@@ -141,25 +152,40 @@ class Clocks:
         if not self.proc:
             return None
         self.f.flush()
-        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r]
+        return self.parse(open(self.f.name).read(), self.window)
+
+    @staticmethod
+    def parse(text: str, window=None):
+        """Median SM clock, the maximum clock and the throttle reasons seen,
+        over the samples inside window = [t0, t1] (host epoch seconds) when
+        there are any, else over all samples."""
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sm, mx, reasons = [], [], set()
-        for r in rows:
-            r = [c.strip() for c in r]
-            if len(r) < 9:
+        samples = []
+        for line in text.strip().splitlines():
+            r = [c.strip() for c in line.split(",")]
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
+                t = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((t, float(r[2]), float(r[3]),
+                                {n for n, v in zip(names, r[6:10]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for n, v in zip(names, r[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside, in_region = samples, 0
+        if window and window[1] is not None:
+            w = [x for x in samples if window[0] - 0.05 <= x[0] <= window[1] + 0.05]
+            if w:
+                inside, in_region = w, len(w)
+        reasons = set()
+        for x in inside:
+            reasons |= x[3]
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": max(x[2] for x in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "samples_in_timed_region": in_region,
+                "samples_total": len(samples)}
 
 
 def cpu_baseline_one_thread(wl_name: str):
@@ -404,6 +430,8 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
     if clk:
         clk.__enter__()
         time.sleep(0.3)
+    if clk:
+        clk.mark_start()
     with torch.cuda.stream(s):
         t0.record(s)
         for _ in range(steps):
@@ -411,6 +439,7 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
         t1.record(s)
     barrier()
     if clk:
+        clk.mark_end()
         clk.__exit__(None, None, None)
     ms = t0.elapsed_time(t1) / steps
     # instrumented graph: same warm-up and step count, dominant launches timed
