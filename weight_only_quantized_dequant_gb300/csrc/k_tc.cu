@@ -30,6 +30,7 @@
 #include <cuda.h>
 
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "qz_internal.cuh"
@@ -933,7 +934,9 @@ qz_status tc_resident_clusters(bool int4, Kern kern, int S, size_t smem, int sms
     return QZ_OK;
   }
   constexpr int kDev = 16;
-  static int cache[kDev][2][4];  // 0 = not asked yet, -1 = not launchable
+  // 0 = not asked yet, -1 = not launchable; threads that race ask the
+  // runtime twice and store the same answer
+  static std::atomic<int> cache[kDev][2][4];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_status(e);
@@ -942,8 +945,9 @@ qz_status tc_resident_clusters(bool int4, Kern kern, int S, size_t smem, int sms
     *out = 0;
     return QZ_OK;
   }
-  int &c = cache[dev][int4 ? 1 : 0][si];
-  if (c == 0) {
+  std::atomic<int> &c = cache[dev][int4 ? 1 : 0][si];
+  int v = c.load(std::memory_order_relaxed);
+  if (v == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)S);
     cfg.blockDim = dim3(kThreadsTc);
@@ -961,9 +965,10 @@ qz_status tc_resident_clusters(bool int4, Kern kern, int S, size_t smem, int sms
       (void)cudaGetLastError();  // not a sticky error: this S is just not used
       n = -1;
     }
-    c = n > 0 ? n : -1;
+    v = n > 0 ? n : -1;
+    c.store(v, std::memory_order_relaxed);
   }
-  *out = c > 0 ? c : 0;
+  *out = v > 0 ? v : 0;
   return QZ_OK;
 }
 
