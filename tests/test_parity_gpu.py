@@ -336,6 +336,36 @@ def test_tensor_core_grouped_large_int8(B):
         assert_close(Y, y_ref, a_ref, f"grouped int8 large B={B} m={i}")
 
 
+def test_tensor_core_workspace_validation():
+    """A workspace one byte short, or not 16-byte aligned, is refused before
+    anything is enqueued (the output stays untouched); the exact size works."""
+    import ctypes
+    from weight_only_quantized_dequant_gb300 import _lib
+    lib = _lib.load()
+    N, K, B = 300, 1024, 16
+    w = qz().quantize_int8(S.weight(N, K, 9170, device=DEV))
+    X = S.activation(B, K, 9171, device=DEV)
+    need = qz().gemm_workspace_bytes(B, K, 0)
+    ws = torch.empty((need + 32,), dtype=torch.uint8, device=DEV)
+    Y = torch.full((B, N), 7.0, dtype=torch.float16, device=DEV)
+    f = lib.qz_gemm_int8
+    st = f(ctypes.byref(w.struct()), B, X.data_ptr(), K, Y.data_ptr(), N, ws.data_ptr(),
+           need - 1, None)
+    assert st == 1  # QZ_ERR_INVALID_ARG
+    st = f(ctypes.byref(w.struct()), B, X.data_ptr(), K, Y.data_ptr(), N, ws.data_ptr() + 8,
+           need, None)
+    assert st == 2  # QZ_ERR_ALIGNMENT
+    torch.cuda.synchronize()
+    assert (Y == 7.0).all()
+    st = f(ctypes.byref(w.struct()), B, X.data_ptr(), K, Y.data_ptr(), N, ws.data_ptr(), need,
+           None)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert qz().device_error() == 0
+    ref = qz().gemm_int8(w, X)  # the same call through the binding
+    assert torch.equal(Y, ref)
+
+
 @pytest.mark.parametrize("fmt", ["int8", "int4o"])
 def test_tensor_core_more_tiles_than_sms_without_workspace(fmt):
     """160 row tiles and no workspace: persistent CTAs take whole tiles, some
