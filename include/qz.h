@@ -67,9 +67,9 @@ int qz_last_cuda_error(void);
 /* Launch overlap for the GEMV/GEMM entry points, per host thread (off by
  * default).  When on, each product kernel is launched with programmatic
  * dependent launch: it may start while the preceding kernel on the stream is
- * still running, prefetches (GEMV) or already converts (tensor-core GEMM) the
- * first weight tiles of each CTA, and waits for that kernel
- * (griddepcontrol.wait) before it reads x or writes y.
+ * still running, starts loading (GEMV: the first ring stage of each warp) or
+ * already converts (tensor-core GEMM) the first weight tiles of each CTA, and
+ * waits for that kernel (griddepcontrol.wait) before it reads x or writes y.
  * The caller promises that no work still in flight on the stream writes the
  * WEIGHTS of the call (q/q4/w_out/scale/perm); inputs and outputs keep normal
  * stream order.  Returns QZ_ERR_INVALID_ARG unless enable is 0 or 1. */
