@@ -231,7 +231,10 @@ qz_status qz_check_perm(const int32_t *perm, int64_t K, int32_t *flag,
 /* Quantize W [N][ldw] fp16 with the given perm into the format above.
  * w_out may be NULL when n_out == 0.  ld_out/ld_q4 must be at least the
  * values of qz_int4o_layout and keep the 16-B rule; all padding is written
- * as 0.  K <= 2^17. */
+ * as 0.  Each CTA stages one fp16 row of W in shared memory, so K is limited
+ * by the device's opt-in shared memory per block: 2 * roundup(K, 8) bytes
+ * must fit (K <= 116224 on GB300's 227 KiB); beyond that, and beyond
+ * K = 2^17 on any device, the call returns QZ_ERR_UNSUPPORTED. */
 qz_status qz_quantize_int4_outlier(const qz_half *W, int64_t ldw,
                                    const int32_t *perm, int64_t N, int64_t K,
                                    int64_t n_out, qz_half *w_out,

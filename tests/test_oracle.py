@@ -344,6 +344,26 @@ def test_fp16_ulp_closed_forms():
     assert O.fp16_ulp(v).tolist() == want
 
 
+def test_tolerance_hand_values():
+    """The acceptance bound 1e-3 * sum_j |w_ij x_j| + 1 fp16 ulp of y_ref,
+    evaluated by hand: a normal, a negative, a subnormal and a zero y_ref,
+    the largest finite fp16, and a zero magnitude sum (ulp alone)."""
+    y_ref = np.array([1.0, -3.0, 1e-6, 0.0, 65504.0, 0.75])
+    abs_ref = np.array([2.0, 10.0, 0.5, 0.0, 70000.0, 0.0])
+    want = [2e-3 + 2 ** -10,        # ulp(1) = 2^-10
+            1e-2 + 2 ** -9,         # ulp(3) = 2^-9
+            5e-4 + 2 ** -24,        # subnormal: spacing 2^-24
+            2 ** -24,               # zero: the subnormal spacing
+            70.0 + 32.0,            # ulp(65504) = 32
+            2 ** -11]               # ulp(0.75) = 2^-11, no magnitude term
+    got = O.tolerance(y_ref, abs_ref)
+    assert np.allclose(got, want, rtol=1e-15, atol=0)
+    # the relative term is 1e-3, not 1e-2 or 1e-4: an error of 1.5e-3 on a
+    # magnitude sum of 1 at y_ref = 0 fails, 0.9e-3 passes
+    assert 1.5e-3 > O.tolerance(np.array([0.0]), np.array([1.0]))[0]
+    assert 0.9e-3 < O.tolerance(np.array([0.0]), np.array([1.0]))[0]
+
+
 # ------------------------------------------------- byte counts (pages) ----
 def _golden():
     with open(os.path.join(GOLDEN, "page_byte_counts.json")) as f:

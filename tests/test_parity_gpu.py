@@ -525,6 +525,11 @@ def test_pager_streams_layers_and_reports_injected_failure():
     x = S.activation(1, K, 400, device=DEV)[0]
     ref = [m.gemv_int8(w, x) for w in ws]
     torch.cuda.synchronize()
+    # the oracle's product of each layer, from the seeded fp16 weights
+    oref = []
+    for l in range(L):
+        q_ref, s_ref = O.int8_quantize(S.weight(N, K, 300 + l, device=DEV).cpu().numpy())
+        oref.append(O.int8_product_ref(q_ref, s_ref, x.cpu().numpy()[None]))
     pager = m.Pager(hosts, slots, copy_s, comp_s)
     outs = [torch.empty((N,), dtype=torch.float16, device=DEV) for _ in range(L)]
     for rnd in range(2):
@@ -539,6 +544,7 @@ def test_pager_streams_layers_and_reports_injected_failure():
             pager.release(l)
         comp_s.synchronize()
         for l in range(L):
+            assert_close(outs[l], oref[l][0][0], oref[l][1][0], f"paged layer {l} pass {rnd}")
             assert torch.equal(outs[l], ref[l]), (rnd, l)
     # host-side injected copy failure: acquire reports QZ_ERR_IO, nothing hangs
     pager.inject_copy_failure(2)

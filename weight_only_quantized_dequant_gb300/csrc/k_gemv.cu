@@ -228,6 +228,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// After a warp gave up a wait: stages first..issued-1 of its ring may still
+// have bulk copies in flight.  Stage i lives in slot i % NS and completes
+// phase i / NS of that slot's barrier, so each is waited for (bounded) on its
+// own parity before the CTA's shared memory can be handed to another CTA.
+template <int NS>
+__device__ __forceinline__ void ring_drain(uint32_t bar_w, int first, int issued) {
+  const unsigned long long t0 = gtimer();
+  for (int i = first; i < issued; ++i) {
+    const uint32_t bar = bar_w + (uint32_t)(i % NS) * 8u;
+    const uint32_t parity = (uint32_t)(i / NS) & 1u;
+    while (!mbar_try(bar, parity)) {
+      if (gtimer() - t0 > kWaitNs) return;
+    }
+  }
+}
+
 // Row boundaries of the grouped matrices, kept in registers (32-bit rows:
 // the host limits a launch to < 2^31 rows).
 struct Bounds {
@@ -402,6 +418,8 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
   bool ok = true;
   int cst = 0;            // consumer ring slot
   uint32_t cphase = 0;    // parity of the slot's current use
+  int cidx = 0;           // stages consumed (ring position of the consumer)
+  int fail_at = -1;       // first stage whose wait gave up
   for (int g = 0; g < P; ++g) {
     // rows of this group: matrix, row, scale, first outlier chunk
     const int rb = first + g * stride;
@@ -427,7 +445,10 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
         if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         issue_next();
       }
-      if (ok) ok = mbar_wait(bar_w + cst * 8, cphase);
+      if (ok) {
+        ok = mbar_wait(bar_w + cst * 8, cphase);
+        if (!ok) fail_at = cidx;
+      }
       if (ok) {
         // Lanes whose chunk lies past the row's end read stale (finite) codes
         // of the slot; their staged inputs are zero, so they add exact zeros.
@@ -451,6 +472,7 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
         }
       }
       __syncwarp();
+      ++cidx;
       if (++cst == NS) {
         cst = 0;
         cphase ^= 1u;
@@ -494,16 +516,9 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
       }
     }
   }
-  // A warp that gave up a wait still has copies in flight into its ring;
-  // give them a bounded time to land before the CTA's shared memory goes.
-  if (!ok && lane == 0) {
-    for (int st = 0; st < NS; ++st) {
-      const unsigned long long t0 = gtimer();
-      while (!mbar_try(bar_w + st * 8, 0) && !mbar_try(bar_w + st * 8, 1) &&
-             gtimer() - t0 < kWaitNs) {
-      }
-    }
-  }
+  // A warp that gave up a wait may still have copies in flight into its
+  // ring; give them a bounded time to land before the CTA's shared memory goes.
+  if (!ok && lane == 0) ring_drain<NS>(bar_w, fail_at, items - pleft);
 }
 
 // ---------------------------------------------------------------------------
@@ -579,8 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
   const uint32_t bar_w = smem_u32(&bars[warp * NS]);
 
   // Producer state, across products: product pk, row group pg, stage psj,
-  // ring slot pst, stages left in product pk.
-  int pk = 0, pg = 0, psj = 0, pst = 0, pleft = 0;
+  // ring slot pst, stages left in product pk, stages issued in all.
+  int pk = 0, pg = 0, psj = 0, pst = 0, pleft = 0, issued = 0;
   Work pw = plan(0);
   Bounds pbd;
   const uint8_t *pptr[R];
@@ -633,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
       }
     }
     pst = pst + 1 == NS ? 0 : pst + 1;
+    ++issued;
     if (--pleft == 0) {
       enter(pk + 1);
     } else if (++psj == pw.SPR) {
@@ -656,6 +672,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
   bool ok = true;
   int cst = 0;            // consumer ring slot
   uint32_t cphase = 0;    // parity of the slot's current use
+  int cidx = 0;           // stages consumed (ring position of the consumer)
+  int fail_at = -1;       // first stage not consumed after an abort
 
   for (int k = 0; k < sp.n; ++k) {
     const GemvParams &p = sp.t[k];
@@ -684,7 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
         if (k + 1 < sp.n) prefetch_rows(k + 1);
       }
       __syncthreads();
-      if (*(volatile int *)abort_flag) ok = false;
+      if (*(volatile int *)abort_flag && ok) {
+        ok = false;
+        fail_at = cidx;
+      }
     } else if (threadIdx.x == 0 && sp.n > 1) {
       prefetch_rows(1);
     }
@@ -747,7 +768,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
           if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           issue_next();
         }
-        if (ok) ok = mbar_wait(bar_w + cst * 8, cphase);
+        if (ok) {
+          ok = mbar_wait(bar_w + cst * 8, cphase);
+          if (!ok) fail_at = cidx;
+        }
         if (ok) {
           const uint32_t sbase = ring_w + (uint32_t)cst * R * kStageRow + lane * 16;
 #pragma unroll
@@ -769,6 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
           }
         }
         __syncwarp();
+        ++cidx;
         if (++cst == NS) {
           cst = 0;
           cphase ^= 1u;
@@ -809,16 +834,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
     const unsigned old = atomicAdd(sp.sync, 1u);
     if (old == (unsigned)(sp.n * G - 1)) atomicExch(sp.sync, 0u);
   }
-  // A warp that gave up a wait still has copies in flight into its ring;
-  // give them a bounded time to land before the CTA's shared memory goes.
-  if (!ok && lane == 0) {
-    for (int st = 0; st < NS; ++st) {
-      const unsigned long long t0 = gtimer();
-      while (!mbar_try(bar_w + st * 8, 0) && !mbar_try(bar_w + st * 8, 1) &&
-             gtimer() - t0 < kWaitNs) {
-      }
-    }
-  }
+  // A warp that gave up a wait may still have copies in flight into its
+  // ring; give them a bounded time to land before the CTA's shared memory goes.
+  if (!ok && lane == 0) ring_drain<NS>(bar_w, fail_at, issued);
 }
 
 // Shared memory of gemv_kernel with W warps: staged inputs, then the ring

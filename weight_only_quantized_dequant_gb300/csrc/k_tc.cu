@@ -1158,7 +1158,7 @@ qz_status read_device_error(int *code, int clear) {
 namespace qz {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB, QZ_NOALLOC_SCRATCH_BYTES
+constexpr size_t kNoAllocScratchBytes = QZ_NOALLOC_SCRATCH_BYTES;  // the header's stated limit
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch array on the current device.  The name of a
@@ -1187,9 +1187,15 @@ qz_status noalloc_scratch(void **out) {
 extern "C" qz_status qz_gemm_int4_outlier_noalloc(const qz_int4o_weight *w, int64_t B,
                                                   const qz_half *X, int64_t ldx, qz_half *Y,
                                                   int64_t ldy, qz_stream s) {
+  // The batch and weight-size checks come first, in the order and with the
+  // statuses of qz_gemm_int4_outlier, so that only the scratch limit below
+  // can make the two calls answer differently.
   if (!w) return QZ_ERR_INVALID_ARG;
+  if (w->N < 1 || w->K < 1 || w->n_out < 0 || w->n_out > w->K) return QZ_ERR_INVALID_ARG;
+  if (B < 1) return QZ_ERR_INVALID_ARG;
+  if (B > QZ_MAX_BATCH) return QZ_ERR_UNSUPPORTED;
   const size_t need = qz_gemm_workspace_bytes(B, w->K, w->n_out);
-  if (need == 0) return QZ_ERR_INVALID_ARG;  // B, K or n_out out of range
+  if (need == 0) return QZ_ERR_INVALID_ARG;  // not reached: B, K and n_out are in range
   if (need > qz::kNoAllocScratchBytes) return QZ_ERR_UNSUPPORTED;
   void *scratch = nullptr;
   qz_status st = qz::noalloc_scratch(&scratch);
