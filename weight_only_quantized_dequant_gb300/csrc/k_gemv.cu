@@ -309,7 +309,12 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
   const int items = P * SPR;
   const uint32_t lane_off = (uint32_t)lane * CS;
   constexpr uint32_t kRound = 32u * CS;  // staged bytes per round of 32 chunks
-  const uint32_t ring_w = smem_u32(ring) + (uint32_t)warp * NS * R * kStageRow;
+  // Ring slots are laid out stage-major ([stage][warp]): slot st of this
+  // warp at ring_w + st * slot_stride.  Only the first stage of every warp
+  // is requested before the input is staged, so the second stages of all
+  // warps form one free block meanwhile (used for the permutation table).
+  constexpr uint32_t slot_stride = (uint32_t)kWarps * R * kStageRow;
+  const uint32_t ring_w = smem_u32(ring) + (uint32_t)warp * R * kStageRow;
   const uint32_t bar_w = smem_u32(&bars[warp * NS]);
 
   // Producer state (tracked by every lane so control flow stays uniform;
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
           : "memory");
 #pragma unroll
       for (int rr = 0; rr < R; ++rr) {
-        const uint32_t dst = ring_w + (uint32_t)(pst * R + rr) * kStageRow;
+        const uint32_t dst = ring_w + (uint32_t)pst * slot_stride + (uint32_t)rr * kStageRow;
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
                 "r"(dst),
@@ -362,17 +367,92 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
   if (items > 0) prow_setup(0);
   for (int it = 0; it < NS - 1 && pleft > 0; ++it) issue_next();
 
+  // INT4: the permutation (static) goes into the free ring block before the
+  // wait, read with coalesced 16-byte loads, as 16-bit entries (K <= 57344):
+  // background entry t' at pb[t'], outlier entry t at pb[kb_pad + t].  The
+  // gather after the wait then needs no global round trip for it.
+  uint16_t *pb = reinterpret_cast<uint16_t *>(ring + slot_stride);
+  const int elems = staged * EPC;           // staged inputs per batch row (multiple of 8)
+  // (measured: pays for K > 4096; at smaller K the gather after the wait is
+  // short and the extra barrier costs more than it saves)
+  const bool perm_smem = INT4 && NS == 2 && p.K > 4096 &&
+                         (size_t)(elems + p.ocpr * 8) * 2 <= slot_stride;
+  if (INT4 && perm_smem) {
+    const int K = p.K, n_out = p.n_out;
+    auto place = [&](int e, int v) {
+      if (e < n_out) pb[elems + e] = (uint16_t)v;
+      else pb[e - n_out] = (uint16_t)v;
+    };
+    const int nv = K / 4;
+#pragma unroll 4
+    for (int c = threadIdx.x; c < nv; c += kThreads) {
+      const int4 v = __ldg(reinterpret_cast<const int4 *>(p.perm) + c);
+      place(4 * c, v.x);
+      place(4 * c + 1, v.y);
+      place(4 * c + 2, v.z);
+      place(4 * c + 3, v.w);
+    }
+    for (int e = 4 * nv + threadIdx.x; e < K; e += kThreads) place(e, __ldg(p.perm + e));
+    for (int t = p.kb + threadIdx.x; t < elems; t += kThreads) pb[t] = 0xFFFFu;
+    for (int t = n_out + threadIdx.x; t < p.ocpr * 8; t += kThreads) pb[elems + t] = 0xFFFFu;
+  }
+
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // let the next kernel on the stream get scheduled as SMs free up
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (INT4 && perm_smem) __syncthreads();
 
   // ---- stage x (gathered through perm for INT4) in shared memory, fp16 ----
   // Eight consecutive inputs per step and thread: eight perm entries, eight
   // independent gathers, one 16-byte shared store (8 inputs never straddle a
-  // staged chunk); INT8 inputs are read in order.
-  const int elems = staged * EPC;           // multiple of 8
+  // staged chunk); INT8 inputs are read in order.  With the permutation in
+  // shared memory, each thread issues the loads of up to kGroups steps
+  // before it stores any of them.
   const __half hzero = __ushort_as_half((unsigned short)0);
   const int step8 = kThreads * 8;
+  constexpr int kGroups = 4;
+  if (INT4 && perm_smem) {
+#pragma unroll 1
+    for (int b = 0; b < B; ++b) {
+      const __half *xb = p.x + b * p.ldx;
+#pragma unroll 1
+      for (int g0 = threadIdx.x * 8; g0 < elems; g0 += kGroups * step8) {
+        uint4 v[kGroups];
+#pragma unroll
+        for (int gi = 0; gi < kGroups; ++gi) {
+          const int e0 = g0 + gi * step8;
+          uint32_t h[8];
+          if (e0 < elems) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(pb + e0);
+            const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t lo = qq[k] & 0xFFFFu, hi = qq[k] >> 16;
+              h[2 * k] = lo != 0xFFFFu ? __half_as_ushort(__ldg(xb + lo)) : 0u;
+              h[2 * k + 1] = hi != 0xFFFFu ? __half_as_ushort(__ldg(xb + hi)) : 0u;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) h[k] = 0u;
+          }
+          v[gi] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                             h[6] | (h[7] << 16));
+        }
+#pragma unroll
+        for (int gi = 0; gi < kGroups; ++gi) {
+          const int e0 = g0 + gi * step8;
+          if (e0 < elems)
+            *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(xs) + b * bstride + (e0 / EPC) * CS +
+                                       (e0 % EPC) * 2) = v[gi];
+        }
+      }
+#pragma unroll 1
+      for (int e = threadIdx.x; e < p.ocpr * 8; e += kThreads) {
+        const uint32_t src = pb[elems + e];
+        xo[b * ostride / 2 + e] = src != 0xFFFFu ? __ldg(xb + src) : hzero;
+      }
+    }
+  } else {
 #pragma unroll 1
   for (int b = 0; b < B; ++b) {
     const __half *xb = p.x + b * p.ldx;
@@ -405,6 +485,7 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
       for (int e = threadIdx.x; e < p.ocpr * 8; e += kThreads)
         xo[b * ostride / 2 + e] = e < p.n_out ? xb[__ldg(p.perm + e)] : hzero;
     }
+  }
   }
   __syncthreads();
   if (!has_rows) return;  // no barrier follows
@@ -452,7 +533,7 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
       if (ok) {
         // Lanes whose chunk lies past the row's end read stale (finite) codes
         // of the slot; their staged inputs are zero, so they add exact zeros.
-        const uint32_t sbase = ring_w + (uint32_t)cst * R * kStageRow + lane * 16;
+        const uint32_t sbase = ring_w + (uint32_t)cst * slot_stride + lane * 16;
 #pragma unroll
         for (int u = 0; u < kRPS; ++u) {
           const int j = sj * kRPS + u;

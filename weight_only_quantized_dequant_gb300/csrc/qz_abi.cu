@@ -163,9 +163,15 @@ qz_status gemm_common(bool int4, GemvParams &p, int64_t B, const qz_half *X, int
   for (int m = 0; m < n; ++m) p.y[m] = reinterpret_cast<__half *>(Ys[m]);
   DeviceInfo di;
   QZ_TRY(device_info(&di));
-  // Batches of 1..4 run on CUDA cores when their staged inputs fit in shared
-  // memory; larger batches are dense enough for the tensor cores, which also
-  // take B <= 4 at the few K too large to stage (their inputs stream in tiles).
+  // Batch 1 runs on the CUDA-core GEMV (one fp32 FMA per weight keeps pace
+  // with HBM at one input row); batches 2..8 on the warp-MMA GEMV, where the
+  // CUDA cores would need one FMA per weight and input row.  Either takes
+  // the call when its staged inputs fit in shared memory; larger batches are
+  // dense enough for the tcgen05 GEMM, which also takes the small batches at
+  // the few K too large to stage (its inputs stream in tiles).
+  if (B == 1 && gemv_smem_bytes(int4, 1, p) <= (size_t)di.max_smem_optin)
+    return launch_gemv(int4, 1, p, s);
+  if (B <= kMvMaxBatch && mv_fits(int4, (int)B, p)) return launch_mv(int4, (int)B, p, s);
   if (B <= 4 && gemv_smem_bytes(int4, (int)B, p) <= (size_t)di.max_smem_optin)
     return launch_gemv(int4, (int)B, p, s);
   int64_t rows[QZ_MAX_GROUP];
@@ -240,11 +246,12 @@ int qz_get_overlap(void) { return g_overlap; }
 
 qz_status qz_device_error(int *code, int clear) {
   if (!code || (clear != 0 && clear != 1)) return QZ_ERR_INVALID_ARG;
-  int a = 0, b = 0, c = 0;
+  int a = 0, b = 0, c = 0, d = 0;
   QZ_TRY(read_device_error(&a, clear));
   QZ_TRY(read_gemv_error(&b, clear));
   QZ_TRY(read_embed_error(&c, clear));
-  *code = a | b | c;
+  QZ_TRY(read_mv_error(&d, clear));
+  *code = a | b | c | d;
   return QZ_OK;
 }
 

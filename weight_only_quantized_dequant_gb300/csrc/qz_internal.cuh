@@ -64,6 +64,31 @@ size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p);
 // Enqueue the CUDA-core GEMV for batch 1 <= B <= 4.
 qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s);
 
+// Warp-MMA GEMV (mma.sync on dequantized codes) for batch 1..kMvMaxBatch.
+constexpr int kMvMaxBatch = 8;
+struct MvProduct {  // shapes of the product, chosen by the host
+  int Ko, Kb;         // 64-byte K blocks per row: outliers (INT4), codes
+  int nst, skc;       // ring stages per 16-row tile, K blocks per stage
+  uint32_t pitch;     // bytes between the rows of a stage
+  uint32_t bstride;   // staged input bytes per batch row (codes' inputs)
+  uint32_t ostride;   // staged outlier-input bytes per batch row
+  uint32_t rawstride; // contiguous input bytes per batch row (raw)
+  int raw;            // INT4: input copied to shared memory, then gathered
+};
+struct MvLaunch {
+  GemvParams t;
+  MvProduct pr;
+  int B;
+  int ns;                // ring stages
+  int early;             // stages issued before the input is staged
+  uint32_t slot_bytes;   // bytes of one ring stage
+  uint32_t xo_off, raw_off, ring_off, bar_off, part_off, cnt_off;  // shared-memory offsets
+};
+// Whether a batch-B product fits the kernel's shared memory.
+bool mv_fits(bool int4, int B, const GemvParams &p);
+qz_status launch_mv(bool int4, int B, const GemvParams &p, cudaStream_t s);
+qz_status read_mv_error(int *code, int clear);
+
 // Tensor-core (tcgen05) GEMM for any batch 1..64; rows of each matrix are
 // p.row_end differences.
 size_t tc_smem_bytes(bool int4, int Np);
