@@ -2,11 +2,15 @@
 
 One step = every quantized linear of every layer (4 dependent launches per
 layer), replayed from a CUDA graph.  The stack (several GB) is far larger
-than the 129 MB L2, so no flush is needed between steps.
+than the 129 MB L2, so no flush is needed between steps.  The headline is
+the 70B-shaped outlier-aware INT4 stack (80 layers, 35.3 GB, the largest
+configuration on one GPU); the line also carries one sub-result per other
+configuration (Gemma-2-9B INT8, Llama-3.2-3B INT4, 7B INT4 at batch 1/4/16/64,
+the 256 x 256 INT8 check) under "workloads".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--extra] [--head] [--paged] [--tiered] [--stream-quant]
-                  [--no-cpu]
+                  [--impl ours|reference] [--no-sub] [--head] [--paged] [--tiered]
+                  [--stream-quant] [--no-cpu]
 
 Prints ONE JSON line.  Under torchrun (N > 1) every rank runs an independent
 replica (the method targets one GPU; no collectives) and rank 0 prints.
@@ -36,10 +40,10 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=600)  # ~1 s timed: several clock samples
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gemma2_9b_int8")
+    ap.add_argument("--workload", default="llama_70b_int4o")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--extra", action="store_true",
-                    help="also measure the other workloads (reported under 'workloads')")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the sub-results of the other configurations ('workloads')")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--paged", action="store_true",
                     help="also stream the 70B and Gemma stacks through the pager")
@@ -191,9 +195,11 @@ class Clocks:
 def cpu_baseline_one_thread(wl_name: str):
     """The same oracle on one host thread (BLAS pinned to one thread in a
     child process, since the thread count is fixed when numpy loads), on the
-    gate matrix of layer 0: (GB/s, sample text), or None if it fails."""
-    code = ("import json, bench; g, t, smp, th = bench.cpu_baseline(%r, 4.0, ('gate',)); "
-            "print(json.dumps([g, smp]))" % wl_name)
+    gate matrix of layer 0 (k for the 70B layer): (GB/s, sample text), or
+    None if it fails."""
+    one = ("k",) if wl_name in CPU_SAMPLE else ("gate",)
+    code = ("import json, bench; g, t, smp, th = bench.cpu_baseline(%r, 4.0, %r); "
+            "print(json.dumps([g, smp]))" % (wl_name, one))
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     try:
         out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
@@ -202,6 +208,12 @@ def cpu_baseline_one_thread(wl_name: str):
         return g, smp
     except Exception:
         return None
+
+
+# Matrices of layer 0 the CPU baseline samples per workload (the 70B layer's
+# 28672-wide matrices would take minutes to generate and quantize in fp64 on
+# the host; its k and v projections are the same format at a bounded size).
+CPU_SAMPLE = {"llama_70b_int4o": ("k", "v")}
 
 
 def cpu_baseline(wl_name: str, budget_s: float = 12.0, only=None):
@@ -215,6 +227,8 @@ def cpu_baseline(wl_name: str, budget_s: float = 12.0, only=None):
     from weight_only_quantized_dequant_gb300 import synthetic as S
 
     wl = S.WORKLOADS[wl_name]
+    if only is None:
+        only = CPU_SAMPLE.get(wl_name)
     mats = []
     for m in S.MATS:
         if only is not None and m not in only:
@@ -284,6 +298,9 @@ def run_reference(a):
 
     wl = S.WORKLOADS[a.workload]
     N, K = wl.shape("down")
+    # a bounded sample: at most 16 M weights of the down projection's rows
+    # (all of them but for the 70B layer, 512 of its 8192 rows)
+    N = min(N, max(1, (1 << 24) // K))
     W = S.weight(N, K, S.matrix_seed(wl, 0, "down"), dist=wl.dist).numpy()
     x = S.activation(1, K, 5).numpy()
     if wl.fmt == "int8":
@@ -304,12 +321,13 @@ def run_reference(a):
     dt = (time.perf_counter() - t0) / a.steps
     gbs = nbytes / dt / 1e9
     cores = len(os.sched_getaffinity(0))
-    sample = f"oracle fp64 product of the down projection ({N}x{K}) of layer 0, per step"
+    rows = "" if N == wl.shape("down")[0] else f", {N} of its {wl.shape('down')[0]} rows"
+    sample = f"oracle fp64 product of the down projection ({N}x{K}{rows}) of layer 0, per step"
     out = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
            "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": a.workload, "sample": "down projection of layer 0"},
+           "config": {"workload": a.workload, "sample": f"down projection of layer 0{rows}"},
            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -337,9 +355,55 @@ def copy_probe_gbs(device) -> float:
     return gbs
 
 
+# The other configurations, reported as sub-results of the headline line.
+SUB_CONFIGS = [("gemma2_9b_int8", 1), ("llama32_3b_int4o", 1), ("llama_7b_int4o", 1),
+               ("llama_7b_int4o", 4), ("llama_7b_int4o", 16), ("llama_7b_int4o", 64),
+               ("llama_70b_int4o", 1)]
+
+
+def measure_tiny(steps: int, warmup: int, device, peak: float) -> dict:
+    """The 256 x 256 INT8 check (W ~ N(0, 0.02^2), x ~ N(0, 1), CPU seed 0):
+    quantized on the GPU, one GEMV launch per step replayed from a CUDA
+    graph of `steps` launches.  The 64 KiB matrix stays in L2, so this is a
+    launch-latency figure, not an HBM one."""
+    import torch
+
+    from weight_only_quantized_dequant_gb300 import api
+    from weight_only_quantized_dequant_gb300 import synthetic as S
+
+    W, x = S.tiny_int8_inputs()
+    w = api.quantize_int8(W.to(device))
+    xd = x[0].to(device)
+    y = torch.empty((256,), dtype=torch.float16, device=device)
+    s = torch.cuda.Stream(device=device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            api.gemv_int8(w, xd, y, stream=s)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(steps):
+            api.gemv_int8(w, xd, y, stream=s)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        g.replay()
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+    torch.cuda.synchronize(device)
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    nbytes = w.nbytes() + 2 * 256 + 2 * 256
+    return {"batch": 1, "layers": 1, "us_per_launch": round(us, 3),
+            "ms_per_step": round(us * 1e-3, 6), "gbs": round(nbytes / (us * 1e-6) / 1e9, 2),
+            "pct_of_peak": round(100.0 * nbytes / (us * 1e-6) / 1e9 / peak, 3),
+            "note": "64 KiB matrix, L2-resident: launch-bound"}
+
+
 def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
-            clocks=False, device=None, layers=None, overlap=True, fused=False):
-    """Build the stack, capture one step, time it.  Returns a dict."""
+            clocks=False, device=None, layers=None, overlap=True, fused=False, e2e=True):
+    """Build the stack, capture one step, time it.  Returns a dict (e2e:
+    also time the step with its host copies)."""
     import torch
 
     from weight_only_quantized_dequant_gb300 import stack as ST
@@ -458,25 +522,27 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
     dom_avg_ms = dom_sum / n_dom
 
     # e2e: pinned host inputs -> device, step, outputs -> pinned host
-    with torch.cuda.stream(s):
-        for _ in range(warmup):
-            x_dev.copy_(x_host, non_blocking=True)
-            graph.replay()
-            y_host.copy_(y_dev, non_blocking=True)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        e0.record(s)
-        for _ in range(steps):
-            x_dev.copy_(x_host, non_blocking=True)
-            graph.replay()
-            y_host.copy_(y_dev, non_blocking=True)
-        e1.record(s)
-    barrier()
-    e2e_serial_ms = e0.elapsed_time(e1) / steps
-    e2e_ms = e2e_pipelined(st, s, graph, x_dev, x_host, y_dev, y_host, steps, warmup, barrier,
-                           overlap, device)
+    e2e_serial_ms = e2e_ms = float("nan")
+    if e2e:
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                x_dev.copy_(x_host, non_blocking=True)
+                graph.replay()
+                y_host.copy_(y_dev, non_blocking=True)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(steps):
+                x_dev.copy_(x_host, non_blocking=True)
+                graph.replay()
+                y_host.copy_(y_dev, non_blocking=True)
+            e1.record(s)
+        barrier()
+        e2e_serial_ms = e0.elapsed_time(e1) / steps
+        e2e_ms = e2e_pipelined(st, s, graph, x_dev, x_host, y_dev, y_host, steps, warmup, barrier,
+                               overlap, device)
 
     dom_names = S.GROUPS[DOMINANT_GROUP]
     dom_bytes = sum(st.layers[0].mats[m].nbytes() for m in dom_names)
@@ -809,14 +875,20 @@ def main():
     ms_all, e2e_all = max_over_ranks(dist_ctx, [r["ms_per_step"], r["e2e_ms"]], device)
 
     extra = {}
-    if a.extra and rank == 0:
-        for name, b in [("llama32_3b_int4o", 1), ("llama_7b_int4o", 1), ("llama_7b_int4o", 4),
-                        ("llama_7b_int4o", 16), ("llama_7b_int4o", 64), ("llama_70b_int4o", 1)]:
-            e = measure(name, b, max(5, a.steps // 2), a.warmup, None, device=device,
-                        overlap=not a.no_overlap)
-            extra[f"{name}_b{b}"] = {k: e[k] for k in ("us_per_layer", "gbs", "ms_per_step",
-                                                          "stack_gb")}
-            extra[f"{name}_b{b}"]["dominant_gbs"] = e["dominant"]["gbs"]
+    if not a.no_sub and rank == 0 and a.layers is None:
+        peak_sub, _ = peaks()
+        for name, b in SUB_CONFIGS:
+            if (name, b) == (a.workload, a.batch):
+                continue
+            e = measure(name, b, max(20, a.steps // 4), a.warmup, None, device=device,
+                        overlap=not a.no_overlap, e2e=False)
+            extra[f"{name}_b{b}"] = {
+                "batch": b, "layers": e["layers"], "ms_per_step": round(e["ms_per_step"], 4),
+                "us_per_layer": round(e["us_per_layer"], 3), "gbs": round(e["gbs"], 2),
+                "pct_of_peak": round(100.0 * e["gbs"] / peak_sub, 2),
+                "dominant_gbs": round(e["dominant"]["gbs"], 2),
+                "stack_gb": round(e["stack_gb"], 3)}
+        extra["tiny_int8_b1"] = measure_tiny(max(100, a.steps), a.warmup, device, peak_sub)
 
     if a.head and rank == 0:
         extra["llama32_3b_head"] = measure_head("llama32_3b_head", max(10, a.steps), a.warmup,
