@@ -201,3 +201,22 @@ def test_tiered_3b_step_both_tiers_against_oracle():
             check_outputs(ts.host.y[hl], oracle_layer(wl, hl), f"tiered 3b host layer {hl}")
     finally:
         ts.close()
+
+
+def test_fused_stack_graph_against_oracle():
+    """A decode step of two Gemma layers captured as one sequence launch per
+    layer (with programmatic overlap), replayed three times: every output
+    against the oracle; the barrier words left at zero."""
+    from weight_only_quantized_dequant_gb300 import stack as ST
+    import weight_only_quantized_dequant_gb300 as qz
+    wl = S.WORKLOADS["gemma2_9b_int8"]
+    b = ST.LayerStack(wl, layers=2, fused=True)
+    g = b.capture(overlap=True)
+    _clear(b.y)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert qz.device_error() == 0
+    assert not b.sync.any()
+    for l in range(2):
+        check_outputs(b.y[l], oracle_layer(wl, l), f"fused gemma layer {l}")
