@@ -116,19 +116,30 @@ def tensor_peak():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons while timing.
-    Each sample carries nvidia-smi's timestamp; the summary keeps the samples
+    """SM clocks and throttle reasons sampled while timing.
+
+    Samples come from NVML (libnvidia-ml, read-only queries: SM clock, its
+    maximum, the active clock-event reasons) every 10 ms on a host thread,
+    else from an `nvidia-smi -lms 200` child.  The summary keeps the samples
     taken inside the window between mark_start() and mark_end() (the timed
     region), and says how many there were."""
     Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    PERIOD_S = 0.01
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.window = None
-        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.samples = []
+        self.backend = None
+        self._stop = None
+        self._thread = None
+        self.f = None
 
     def mark_start(self):
         self.window = [time.time(), None]
@@ -137,32 +148,94 @@ class Clocks:
         if self.window:
             self.window[1] = time.time()
 
+    @classmethod
+    def decode(cls, mask: int) -> set:
+        return {n for bit, n in cls.REASON_BITS.items() if mask & bit}
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        rc = -1
+        try:  # the device torch calls `index`, by UUID (robust to CUDA_VISIBLE_DEVICES)
+            import torch
+            u = getattr(torch.cuda.get_device_properties(self.index), "uuid", None)
+            if u is not None:
+                rc = lib.nvmlDeviceGetHandleByUUID(("GPU-" + str(u)).encode(), ctypes.byref(h))
+        except Exception:
+            rc = -1
+        if rc != 0 and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index),
+                                                         ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:   # 1 = SM clock
+            raise OSError("no max clock")
+
+        def sample():
+            mhz, r = ctypes.c_uint(), ctypes.c_ulonglong()
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) != 0:
+                return None
+            if reasons(h, ctypes.byref(r)) != 0:
+                return None
+            return (time.time(), float(mhz.value), float(mx.value), self.decode(r.value))
+        return sample
+
     def __enter__(self):
+        import threading
         try:
+            sample = self._nvml_open()
+            self.backend = "nvml"
+            self._stop = threading.Event()
+
+            def loop():
+                while not self._stop.is_set():
+                    x = sample()
+                    if x is not None:
+                        self.samples.append(x)
+                    self._stop.wait(self.PERIOD_S)
+            self._thread = threading.Thread(target=loop, daemon=True)
+            self._thread.start()
+            return self
+        except Exception:
+            pass
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
+            self.backend = "nvidia-smi"
         except (FileNotFoundError, OSError):
             self.proc = None
         return self
 
     def __exit__(self, *exc):
+        if self._thread:
+            self._stop.set()
+            self._thread.join(timeout=5)
         if self.proc:
             self.proc.terminate()
             self.proc.wait(timeout=10)
 
     def summary(self):
-        if not self.proc:
+        if self.backend == "nvml":
+            out = self.summarize(list(self.samples), self.window, slack=0.0)
+        elif self.proc:
+            self.f.flush()
+            out = self.parse(open(self.f.name).read(), self.window)
+        else:
             return None
-        self.f.flush()
-        return self.parse(open(self.f.name).read(), self.window)
+        if out:
+            out["source"] = self.backend
+        return out
 
     @staticmethod
     def parse(text: str, window=None):
-        """Median SM clock, the maximum clock and the throttle reasons seen,
-        over the samples inside window = [t0, t1] (host epoch seconds) when
-        there are any, else over all samples."""
+        """nvidia-smi CSV lines to samples, then summarize()."""
         import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         samples = []
@@ -176,11 +249,19 @@ class Clocks:
                                 {n for n, v in zip(names, r[6:10]) if v.lower() == "active"}))
             except ValueError:
                 continue
+        return Clocks.summarize(samples, window)
+
+    @staticmethod
+    def summarize(samples, window=None, slack=0.05):
+        """Median SM clock, the maximum clock and the throttle reasons seen,
+        over the samples (t, sm_mhz, max_mhz, reasons) inside window = [t0, t1]
+        (host epoch seconds, widened by `slack` for nvidia-smi's coarser
+        timestamps) when there are any, else over all samples."""
         if not samples:
             return None
         inside, in_region = samples, 0
         if window and window[1] is not None:
-            w = [x for x in samples if window[0] - 0.05 <= x[0] <= window[1] + 0.05]
+            w = [x for x in samples if window[0] - slack <= x[0] <= window[1] + slack]
             if w:
                 inside, in_region = w, len(w)
         reasons = set()
@@ -670,6 +751,41 @@ def h2d_probe_gbs(device, nbytes=1 << 30) -> float:
     return nbytes * 5 / (e0.elapsed_time(e1) * 1e-3) / 1e9
 
 
+def paged_parts(ps, device, layers: int = 8) -> dict:
+    """The pager's two halves timed alone, per layer: the host->device copy
+    of a packed layer into a slot (copy stream, no GEMVs) and the layer's
+    GEMV launches from a filled slot (compute stream, no copies).  A paged
+    layer that overlaps them perfectly takes max(t_copy, t_gemv)."""
+    import torch
+    n = max(2, layers)
+    cp, cs = ps.copy_stream, ps.compute_stream
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(cp):
+        e0.record(cp)
+        for l in range(n):
+            ps.slots[l % 2].copy_(ps.blobs[l % ps.distinct], non_blocking=True)
+        e1.record(cp)
+    torch.cuda.synchronize(device)
+    t_copy = e0.elapsed_time(e1) / n
+    # slot j <- host layer j, then the GEMVs of those two layers alternately
+    with torch.cuda.stream(cp):
+        for j in range(2):
+            ps.slots[j].copy_(ps.blobs[j % ps.distinct], non_blocking=True)
+    torch.cuda.synchronize(device)
+    for l in range(2):                                   # warm-up
+        ps.run_layer(ps._views[l % 2], l % 2 % ps.distinct, cs)
+    torch.cuda.synchronize(device)
+    e0.record(cs)
+    for l in range(n):
+        ps.run_layer(ps._views[l % 2], l % 2 % ps.distinct, cs)
+    e1.record(cs)
+    torch.cuda.synchronize(device)
+    t_gemv = e0.elapsed_time(e1) / n
+    return {"t_copy_us": round(t_copy * 1e3, 2), "t_gemv_us": round(t_gemv * 1e3, 2),
+            "copy_gbs": round(ps.blob_bytes / (t_copy * 1e-3) / 1e9, 1)}
+
+
 def measure_paged(wl_name: str, steps: int, warmup: int, device, distinct: int = 4):
     """Stack streamed layer by layer from pinned host memory through the
     pager (two device slots, copy stream + compute stream)."""
@@ -692,11 +808,18 @@ def measure_paged(wl_name: str, steps: int, warmup: int, device, distinct: int =
     torch.cuda.synchronize(device)
     ms = e0.elapsed_time(e1) / steps
     out = {"workload": wl_name, "layers": ps.n_layers, "distinct_host_layers": ps.distinct,
-           "layer_bytes": ps.blob_bytes, "ms_per_step": ms,
-           "us_per_layer": ms * 1e3 / ps.n_layers,
-           "h2d_gbs": ps.n_layers * ps.blob_bytes / (ms * 1e-3) / 1e9,
-           "link_probe_gbs": h2d_probe_gbs(device)}
-    out["link_frac"] = out["h2d_gbs"] / out["link_probe_gbs"]
+           "layer_bytes": ps.blob_bytes, "ms_per_step": round(ms, 3),
+           "us_per_layer": round(ms * 1e3 / ps.n_layers, 2),
+           "h2d_gbs": round(ps.n_layers * ps.blob_bytes / (ms * 1e-3) / 1e9, 1),
+           "link_probe_gbs": round(h2d_probe_gbs(device), 1),
+           "link": "pinned host -> device cudaMemcpyAsync, 1 GiB, 5 copies"}
+    out["link_frac"] = round(out["h2d_gbs"] / out["link_probe_gbs"], 4)
+    parts = paged_parts(ps, device)
+    out.update(parts)
+    t_layer = ms * 1e3 / ps.n_layers
+    # 1.0 = the layer costs exactly its slower half (copy and GEMVs fully overlapped)
+    out["t_layer_over_max_copy_gemv"] = round(t_layer / max(parts["t_copy_us"],
+                                                            parts["t_gemv_us"]), 4)
     ps.close()
     del ps
     torch.cuda.empty_cache()
@@ -798,6 +921,13 @@ def measure_tiered(wl_name: str, resident: int, steps: int, warmup: int, device,
            "ms_per_step": round(ms, 3), "us_per_layer": round(ms * 1e3 / ts.n_layers, 2),
            "gbs": round(ts.bytes_per_step() / (ms * 1e-3) / 1e9, 1),
            "host_layer_bytes": ts.weight_bytes_per_layer}
+    if tier_b:
+        parts = paged_parts(ts.host, device)
+        out.update(parts)
+        # resident layers cost their GEMVs; paged ones the slower half
+        ideal_ms = (ts.resident * parts["t_gemv_us"] +
+                    tier_b * max(parts["t_copy_us"], parts["t_gemv_us"])) * 1e-3
+        out["t_step_over_ideal"] = round(ms / ideal_ms, 4)
     ts.close()
     del ts
     torch.cuda.empty_cache()
@@ -889,6 +1019,9 @@ def main():
                 "dominant_gbs": round(e["dominant"]["gbs"], 2),
                 "stack_gb": round(e["stack_gb"], 3)}
         extra["tiny_int8_b1"] = measure_tiny(max(100, a.steps), a.warmup, device, peak_sub)
+        # the Gemma INT8 stack as the ELG page runs it: every layer streamed
+        # from pinned host memory through the pager
+        extra["gemma2_9b_int8_paged"] = measure_paged("gemma2_9b_int8", 3, 1, device)
 
     if a.head and rank == 0:
         extra["llama32_3b_head"] = measure_head("llama32_3b_head", max(10, a.steps), a.warmup,
@@ -906,7 +1039,7 @@ def main():
         extra["stream_quant_gemma2_9b"] = measure_stream_quant("gemma2_9b_int8", 2, device)
 
     if a.paged and rank == 0:
-        for name in ("llama_70b_int4o", "gemma2_9b_int8"):
+        for name in ("llama_70b_int4o",) + (("gemma2_9b_int8",) if a.no_sub else ()):
             extra[f"{name}_paged"] = measure_paged(name, max(2, a.steps // 10), 1, device)
 
     cpu = None
@@ -938,9 +1071,10 @@ def main():
                     "avg_launch_us": round(dom["avg_ms"] * 1e3, 3),
                     "peak_kind": peak_src}
     else:
-        # tensor-core GEMM: fp16 x fp16 MMAs of N = batch rounded up to 16;
-        # tcgen05 issues one K-16 MMA per ~101 ns whatever N, so the N-256
-        # dense peak scales by N / 256 for these shapes
+        # tensor-core GEMM: fp16 x fp16 MMAs of N = batch rounded up to 16.
+        # An N-wide MMA does N/256 of the work of the N-256 shape the dense
+        # peak is quoted for; frac_of_n_scaled_peak assumes the MMA issue
+        # rate does not depend on N (an assumption, not a measurement)
         tpk, tpk_src = tensor_peak()
         tflops = dom["flops_per_launch"] / (dom["avg_ms"] * 1e-3) / 1e12
         np_ = (a.batch + 15) // 16 * 16

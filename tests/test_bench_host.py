@@ -42,3 +42,22 @@ def test_clock_samples_fall_back_to_all_when_none_inside():
 def test_clock_parser_ignores_garbage():
     assert bench.Clocks.parse("", None) is None
     assert bench.Clocks.parse("No devices were found\n", None) is None
+
+
+def test_nvml_reason_bits_decode():
+    assert bench.Clocks.decode(0) == set()
+    assert bench.Clocks.decode(0x4) == {"sw_power_cap"}
+    assert bench.Clocks.decode(0x1 | 0x8 | 0x40) == {"hw_slowdown", "hw_thermal_slowdown"}
+    assert bench.Clocks.decode(0x20) == {"sw_thermal_slowdown"}
+
+
+def test_sample_summary_window():
+    now = time.time()
+    samples = [(now - 1.0, 300.0, 2070.0, set()),
+               (now + 0.01, 2070.0, 2070.0, set()),
+               (now + 0.02, 2040.0, 2070.0, {"sw_power_cap"}),
+               (now + 0.03, 2070.0, 2070.0, set())]
+    got = bench.Clocks.summarize(samples, [now, now + 0.04])
+    assert got["samples_in_timed_region"] == 3 and got["sm_mhz"] == 2070.0
+    assert got["reasons"] == ["sw_power_cap"] and got["samples_total"] == 4
+    assert bench.Clocks.summarize([], None) is None

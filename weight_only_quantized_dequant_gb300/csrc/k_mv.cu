@@ -392,10 +392,16 @@ __device__ __forceinline__ void stage_input(uint8_t *smem, const MvLaunch &L, co
   }
 }
 
-template <bool INT4>
+// TP: 16-row tiles per ring stage; the W consumer warps split into TP
+// groups of WT = W / TP, group q owning tile q of every stage, its warps
+// taking alternate K blocks of it.  A CTA's rows are cut into super-tiles of
+// at most 16 TP rows (evenly), each super-tile into TP tiles (evenly).
+template <bool INT4, int TP>
 __global__ void __launch_bounds__(kMaxThreads, 1) mv_kernel(const __grid_constant__ MvLaunch L) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int W = kConsumers;                     // consumer warps; warps W.. produce
+  constexpr int WT = W / TP;                        // warps per tile
+  static_assert(W % TP == 0, "tiles per stage must divide the consumer warps");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
   const int B = L.B;
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mv_kernel(const __grid_constan
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empty + 8 * st), "r"(W) : "memory");
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(xready) : "memory");
-    for (int i = 0; i < nslot; ++i) cnt[i] = 0;
+    for (int i = 0; i < nslot * TP; ++i) cnt[i] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -425,9 +431,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mv_kernel(const __grid_constan
     // ---- producers: the stages of every product, one after another; stage
     // S is issued by producer warp S % kProducers (one warp's bulk-copy
     // issue does not keep up with short row pieces).  Lanes 0..15 copy the
-    // outlier piece of row `lane` of the stage, lanes 16..31 the code piece
-    // of row lane - 16.  Weights only: they never wait for the previous
-    // kernel or for earlier products.
+    // outlier piece of row `lane` of each tile of the stage, lanes 16..31
+    // the code piece of row lane - 16.  Weights only: they never wait for
+    // the previous kernel or for earlier products.
     const int pw = warp - W;
     bool xr = false;  // the first input has been staged
     uint64_t policy;
@@ -439,17 +445,24 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mv_kernel(const __grid_constan
       const MvProduct &pr = L.pr;
       const int64_t r0 = p.total_rows * blockIdx.x / G;
       const int rows = (int)(p.total_rows * (blockIdx.x + 1) / G - r0);
-      const int Tc = (rows + 15) >> 4;
+      const int Tc = (rows + 16 * TP - 1) / (16 * TP);
       const int Ko = pr.Ko, Kc = pr.Ko + pr.Kb;
       const uint32_t P = pr.pitch;
       int te = 0;
       for (int t = 0; t < Tc && ok; ++t) {
         const int ts = te;
         te = rows * (t + 1) / Tc;
-        const int live = te - ts;
-        int m = 0, i = 0;
+        const int live = te - ts;  // rows of the super-tile
         const int row = lane & 15;
-        if (row < live) locate(p, (int)r0 + ts + row, m, i);
+        int m[TP], i[TP];
+        bool lv[TP];
+#pragma unroll
+        for (int q = 0; q < TP; ++q) {  // this lane's row of tile q
+          const int q0 = live * q / TP, nq = live * (q + 1) / TP - q0;
+          lv[q] = row < nq;
+          m[q] = i[q] = 0;
+          if (lv[q]) locate(p, (int)r0 + ts + q0 + row, m[q], i[q]);
+        }
         for (int j = 0; j < pr.nst; ++j) {
           if (S % kProducers != pw) {  // another producer's stage
             ++S;
@@ -490,19 +503,24 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mv_kernel(const __grid_constan
                 : "memory");
           const bool is_code = lane >= 16;
           const int nb = is_code ? cb : ob;
-          if (row < live && nb > 0) {
-            const uint8_t *src =
-                is_code ? p.codes[m] + (int64_t)i * p.ld_codes[m] + (ca - Ko) * kKB
-                        : reinterpret_cast<const uint8_t *>(p.w_out[m] + (int64_t)i * p.ld_out[m]) +
-                              oa * kKB;
-            const uint32_t dst = ring + (uint32_t)slot * slot_bytes + (uint32_t)row * P +
-                                 (uint32_t)((is_code ? ca : oa) - ka) * kKB;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-                " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-                "l"(src), "r"((uint32_t)nb), "r"(fb), "l"(policy)
-                : "memory");
+          if (nb > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#pragma unroll
+          for (int q = 0; q < TP; ++q) {
+            if (lv[q] && nb > 0) {
+              const uint8_t *src =
+                  is_code ? p.codes[m[q]] + (int64_t)i[q] * p.ld_codes[m[q]] + (ca - Ko) * kKB
+                          : reinterpret_cast<const uint8_t *>(p.w_out[m[q]] +
+                                                              (int64_t)i[q] * p.ld_out[m[q]]) +
+                                oa * kKB;
+              const uint32_t dst = ring + (uint32_t)slot * slot_bytes +
+                                   (uint32_t)(16 * q + row) * P +
+                                   (uint32_t)((is_code ? ca : oa) - ka) * kKB;
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                  " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+                  "l"(src), "r"((uint32_t)nb), "r"(fb), "l"(policy)
+                  : "memory");
+            }
           }
           ++S;
           if (++slot == NS) {
@@ -553,19 +571,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mv_kernel(const __grid_constan
     const uint32_t orow = smem_u32(smem + L.xo_off) + (uint32_t)bsel * pr.ostride;
     const int64_t r0 = p.total_rows * blockIdx.x / G;
     const int rows = (int)(p.total_rows * (blockIdx.x + 1) / G - r0);
-    const int Tc = (rows + 15) >> 4;
+    const int Tc = (rows + 16 * TP - 1) / (16 * TP);
     const int Ko = pr.Ko, Kc = pr.Ko + pr.Kb;
     const int NST = pr.nst, SKc = pr.skc;
     const uint32_t P = pr.pitch;
+    const int q = warp / WT, phi = warp % WT;  // this warp's tile of a stage, its K phase
     int ts = 0, te = 0;
     for (int t = 0; t < Tc && ok; ++t) {
       ts = te;
       te = rows * (t + 1) / Tc;
+      const int q0 = ts + (te - ts) * q / TP;            // first row of tile q
+      const int nq = ts + (te - ts) * (q + 1) / TP - q0;  // its rows (0..16)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // the tile's rows, scales, fresh accumulators
-        const int rr = ts + g + 8 * h;
-        live[h] = rr < te;
-        locate(p, (int)r0 + (live[h] ? rr : te - 1), mrow[h], irow[h]);
+        const int rr = g + 8 * h;
+        live[h] = rr < nq;
+        locate(p, (int)r0 + q0 + (live[h] ? rr : (nq > 0 ? nq - 1 : 0)), mrow[h], irow[h]);
         srow[h] = INT4 ? __ldg(p.scale[mrow[h]] + irow[h]) : __ldg(p.scale[mrow[h]]);
       }
 #pragma unroll
@@ -574,11 +595,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mv_kernel(const __grid_constan
         ok = mbar_wait(full + 8u * slot, phase);
         if (!ok) break;
         const int ka = j * SKc, kz = ka + SKc < Kc ? ka + SKc : Kc;
-        const uint32_t sb = ring + (uint32_t)slot * slot_bytes + (uint32_t)g * P + (uint32_t)tig * 16u;
-        int kk = ka + warp;                           // this warp's K blocks: kk, kk + W, ...
+        const uint32_t sb = ring + (uint32_t)slot * slot_bytes + (uint32_t)(16 * q + g) * P +
+                            (uint32_t)tig * 16u;
+        int kk = ka + phi;                            // this warp's K blocks: kk, kk + WT, ...
         if constexpr (INT4) {
 #pragma unroll 1
-          for (; kk < kz && kk < Ko; kk += W) {       // outlier columns (fp16)
+          for (; kk < kz && kk < Ko; kk += WT) {      // outlier columns (fp16)
             const uint32_t a_off = (uint32_t)(kk - ka) * kKB;
             uint4 a = lds128(sb + a_off), a8 = lds128(sb + 8 * P + a_off);
             if (kk * 4 + tig >= p.ocpr) a = a8 = make_uint4(0, 0, 0, 0);  // past the row's outliers
@@ -592,14 +614,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mv_kernel(const __grid_constan
           uint32_t x_addr = INT4 ? xrow + (uint32_t)(kk - Ko) * 256u + tig * 16u
                                  : xrow + (uint32_t)kk * 128u + tig * 8u;
 #pragma unroll 2
-          for (; kk < kz; kk += W) {
+          for (; kk < kz; kk += WT) {
             const uint4 a = lds128(a_addr), a8 = lds128(a_addr + 8 * P);
             if constexpr (INT4)
               int4_block(a, a8, x_addr, de, dd, de1, dd1);
             else
               int8_block(a, a8, x_addr, de, de1);
-            a_addr += (uint32_t)W * kKB;
-            x_addr += (uint32_t)W * (INT4 ? 256u : 128u);
+            a_addr += (uint32_t)WT * kKB;
+            x_addr += (uint32_t)WT * (INT4 ? 256u : 128u);
           }
         }
         __syncwarp();
@@ -614,39 +636,55 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mv_kernel(const __grid_constan
         }
       }
       if (!ok) break;
-      // ---- tile epilogue: this warp's part of every output of the tile,
-      // then the last warp to arrive adds the parts in warp order ---------
-      float *pw = part + ((size_t)ps * W + warp) * 16 * B;
+      if constexpr (WT == 1) {
+        // ---- tile epilogue, one warp per tile: its outputs straight out
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int col = 2 * tig + c, ci = 2 * h + c;
-          const float e = de[ci] + de1[ci], o = dd[ci] + dd1[ci];
-          const float v = INT4 ? fmaf(srow[h], e + 0.0625f * o, dout[ci]) : srow[h] * e;
-          if (col < B) pw[(g + 8 * h) * B + col] = v;
-        }
-      __threadfence_block();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) last = atomicAdd(&cnt[ps], 1) == W - 1;
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence_block();
-        const int rr = lane & 15;
-        if (ts + rr < te) {
-          int m, i;
-          locate(p, (int)r0 + ts + rr, m, i);
-          for (int col = lane >> 4; col < B; col += 2) {
-            float acc = 0.f;
-            for (int w = 0; w < W; ++w) acc += part[(((size_t)ps * W + w) * 16 + rr) * B + col];
-            p.y[m][col * p.ldy[m] + i] = __float2half_rn(acc);
+          for (int c = 0; c < 2; ++c) {
+            const int col = 2 * tig + c, ci = 2 * h + c;
+            const float e = de[ci] + de1[ci], o = dd[ci] + dd1[ci];
+            const float v = INT4 ? fmaf(srow[h], e + 0.0625f * o, dout[ci]) : srow[h] * e;
+            if (col < B && live[h])
+              p.y[mrow[h]][col * p.ldy[mrow[h]] + irow[h]] = __float2half_rn(v);
           }
-        }
+      } else {
+        // ---- tile epilogue: this warp's part of every output of the tile,
+        // then the last of the tile's warps to arrive adds the parts in warp
+        // order ---------------------------------------------------------
+        float *pw = part + ((size_t)ps * W + warp) * 16 * B;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int col = 2 * tig + c, ci = 2 * h + c;
+            const float e = de[ci] + de1[ci], o = dd[ci] + dd1[ci];
+            const float v = INT4 ? fmaf(srow[h], e + 0.0625f * o, dout[ci]) : srow[h] * e;
+            if (col < B) pw[(g + 8 * h) * B + col] = v;
+          }
+        __threadfence_block();
         __syncwarp();
-        if (lane == 0) cnt[ps] = 0;
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&cnt[ps * TP + q], 1) == WT - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence_block();
+          const int rr = lane & 15;
+          if (rr < nq) {
+            int m, i;
+            locate(p, (int)r0 + q0 + rr, m, i);
+            for (int col = lane >> 4; col < B; col += 2) {
+              float acc = 0.f;
+              for (int w = q * WT; w < q * WT + WT; ++w)
+                acc += part[(((size_t)ps * W + w) * 16 + rr) * B + col];
+              p.y[m][col * p.ldy[m] + i] = __float2half_rn(acc);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) cnt[ps * TP + q] = 0;
+        }
+        if (++ps == nslot) ps = 0;
       }
-      if (++ps == nslot) ps = 0;
     }
   }
 }
@@ -658,14 +696,15 @@ namespace {
 constexpr int kMaxStages = 6;
 // Row pieces per stage tried in turn (bytes): whole rows up to the first,
 // then shorter pieces until the ring fits.
-constexpr int kRowCaps[] = {4352, 3456, 2688, 2112, 1600, 1088, 576, 320, 64};
+constexpr int kRowCaps[] = {4352, 3456, 2688, 2112, 1600, 1344, 1088, 832, 576, 320, 64};
 
 // Shared-memory layout and shapes of a launch.  raw: copy INT4 inputs
 // contiguously before the gather.  Returns the bytes of shared memory, or 0
 // if no ring of min_ns stages fits.
-size_t mv_layout(bool int4, const GemvParams &p, int B, int raw, int cap, int min_ns,
+size_t mv_layout(bool int4, const GemvParams &p, int B, int raw, int cap, int min_ns, int tp,
                  size_t avail, MvLaunch &L) {
   L.B = B;
+  L.tp = tp;
   MvProduct &pr = L.pr;
   pr.Ko = int4 ? (p.ocpr + 3) / 4 : 0;
   pr.Kb = (p.cpr + 3) / 4;
@@ -686,7 +725,7 @@ size_t mv_layout(bool int4, const GemvParams &p, int B, int raw, int cap, int mi
   pr.rawstride = (uint32_t)((p.K * 2 + 15) / 16 * 16);
   const size_t xs = (size_t)B * pr.bstride, xo = int4 ? (size_t)B * pr.ostride : 0;
   const size_t rw = pr.raw ? (size_t)B * pr.rawstride : 0;
-  const size_t slot = (size_t)16 * pr.pitch;
+  const size_t slot = (size_t)16 * tp * pr.pitch;
   L.slot_bytes = (uint32_t)slot;
   // The contiguous input copy borrows the ring's last slots, which the
   // producer fills only after the input is staged.
@@ -703,10 +742,10 @@ size_t mv_layout(bool int4, const GemvParams &p, int B, int raw, int cap, int mi
     size_t o = off + (size_t)ns * slot;
     const size_t bar = o;
     o += (size_t)ns * 16 + 16;
-    const size_t prt = o;
-    o += (size_t)(ns + 1) * kConsumers * 16 * B * sizeof(float);
+    const size_t prt = o;  // tile parts, when several warps share a tile
+    if (kConsumers / tp > 1) o += (size_t)(ns + 1) * kConsumers * 16 * B * sizeof(float);
     const size_t cn = o;
-    o += (size_t)(ns + 1) * sizeof(int);
+    o += (size_t)(ns + 1) * tp * sizeof(int);
     o = (o + 15) & ~(size_t)15;
     if (o <= avail) {
       L.ns = ns;
@@ -719,13 +758,39 @@ size_t mv_layout(bool int4, const GemvParams &p, int B, int raw, int cap, int mi
   return 0;
 }
 
-// Pick the launch's shapes: copy-then-gather inputs when they fit, three or
-// more ring stages before shorter row pieces, then whatever fits.
+// Launch shapes, as measured on every grouped launch of the 3B/7B/70B INT4
+// and Gemma INT8 layers at batches 2, 4 and 8:
+//  * Two tiles per stage when a CTA holds at most kTwoTileRows rows and a
+//    stage still holds whole rows (INT4) or at least half of every row
+//    (INT8): there the per-tile setup and the sum of eight warps' parts cost
+//    more than the ring stages of 32 rows do.  Otherwise one tile per stage
+//    (the 70B launches, the long-row down projections); four or eight tiles
+//    per stage lost everywhere (their stages leave too few bytes in flight).
+//  * One tile per stage: whole rows in two or more stages when they fit,
+//    else three or more stages of the longest pieces, then two.
+//  * Inputs copied to shared memory before the gather whenever that fits.
+constexpr int64_t kTwoTileRows = 200;
+
 size_t mv_plan(bool int4, const GemvParams &p, int B, const DeviceInfo &di, MvLaunch &L) {
+  const size_t avail = (size_t)di.max_smem_optin;
+  const int64_t tiles = (p.total_rows + 15) / 16;
+  const int64_t grid = tiles < di.sms ? tiles : di.sms;
+  const int64_t R = (p.total_rows + grid - 1) / grid;  // rows of a CTA
+  if (R <= kTwoTileRows)
+    for (int raw = int4 ? 1 : 0; raw >= 0; --raw)
+      for (int cap : kRowCaps) {
+        const size_t smem = mv_layout(int4, p, B, raw, cap, 2, 2, avail, L);
+        if (smem && L.pr.nst <= (int4 ? 1 : 2)) return smem;
+      }
+  const int row = (int4 ? (p.ocpr + 3) / 4 + (p.cpr + 3) / 4 : (p.cpr + 3) / 4) * kKB;
+  for (int raw = int4 ? 1 : 0; raw >= 0; --raw) {
+    const size_t smem = mv_layout(int4, p, B, raw, row, 2, 1, avail, L);
+    if (smem) return smem;
+  }
   for (int raw = int4 ? 1 : 0; raw >= 0; --raw)
     for (int min_ns = 3; min_ns >= 2; --min_ns)
       for (int cap : kRowCaps) {
-        const size_t smem = mv_layout(int4, p, B, raw, cap, min_ns, (size_t)di.max_smem_optin, L);
+        const size_t smem = mv_layout(int4, p, B, raw, cap, min_ns, 1, avail, L);
         if (smem) return smem;
       }
   return 0;
@@ -741,7 +806,7 @@ qz_status launch_mv_t(const GemvParams &p, int B, cudaStream_t s) {
   L.t = p;
   const size_t smem = mv_plan(INT4, p, B, di, L);
   if (!smem) return QZ_ERR_UNSUPPORTED;
-  auto kern = mv_kernel<INT4>;
+  auto kern = L.tp == 2 ? mv_kernel<INT4, 2> : mv_kernel<INT4, 1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_status(e);
   const int64_t tiles = (p.total_rows + 15) / 16;

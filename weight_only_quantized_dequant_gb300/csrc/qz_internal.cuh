@@ -79,6 +79,7 @@ struct MvLaunch {
   GemvParams t;
   MvProduct pr;
   int B;
+  int tp;                // 16-row tiles per ring stage (1 or 2)
   int ns;                // ring stages
   int early;             // stages issued before the input is staged
   uint32_t slot_bytes;   // bytes of one ring stage

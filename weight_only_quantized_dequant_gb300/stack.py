@@ -327,23 +327,28 @@ class PagedStack:
                                           parts[m]["scale"], N, K, api.default_n_out(K))
         return mats
 
+    def run_layer(self, mats: dict, hl: int, stream):
+        """The four group launches of one layer whose matrices are `mats`
+        (views into a device slot), on the inputs and outputs of host layer
+        hl."""
+        int8 = self.wl.fmt == "int8"
+        xs, ys = self.x[hl], self.y[hl]
+        for g, names in enumerate(S.GROUPS):
+            ws = [mats[m] for m in names]
+            outs = [y[0] for y in ys[g]]
+            if len(ws) == 1:
+                (api.gemv_int8 if int8 else api.gemv_int4_outlier)(ws[0], xs[g][0], outs[0],
+                                                                   stream=stream)
+            else:
+                (api.gemv_int8_grouped if int8 else api.gemv_int4_outlier_grouped)(
+                    ws, xs[g][0], outs, stream=stream)
+
     def run_step(self):
         """All n_layers layers once, each acquired from the pager."""
-        cs = self.compute_stream
-        int8 = self.wl.fmt == "int8"
         for l in range(self.n_layers):
             ptr = self.pager.acquire(l)
             mats = self._views[0 if ptr == self.slots[0].data_ptr() else 1]
-            xs, ys = self.x[l % self.distinct], self.y[l % self.distinct]
-            for g, names in enumerate(S.GROUPS):
-                ws = [mats[m] for m in names]
-                outs = [y[0] for y in ys[g]]
-                if len(ws) == 1:
-                    (api.gemv_int8 if int8 else api.gemv_int4_outlier)(ws[0], xs[g][0], outs[0],
-                                                                       stream=cs)
-                else:
-                    (api.gemv_int8_grouped if int8 else api.gemv_int4_outlier_grouped)(
-                        ws, xs[g][0], outs, stream=cs)
+            self.run_layer(mats, l % self.distinct, self.compute_stream)
             self.pager.release(l)
 
     def close(self):
