@@ -627,6 +627,7 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
 
     dom_names = S.GROUPS[DOMINANT_GROUP]
     dom_bytes = sum(st.layers[0].mats[m].nbytes() for m in dom_names)
+    dom_wbytes = dom_bytes
     K_dom = wl.shape(dom_names[0])[1]
     dom_bytes += 2 * batch * K_dom + sum(2 * batch * wl.shape(m)[0] for m in dom_names)
     if wl.fmt == "int4o":
@@ -641,6 +642,7 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
         "ms_per_step": ms, "us_per_layer": ms * 1e3 / st.n_layers,
         "gbs": st.bytes_per_step() / (ms * 1e-3) / 1e9,
         "dominant": {"group": "+".join(dom_names), "bytes_per_launch": dom_bytes,
+                     "weight_bytes": dom_wbytes,
                      "avg_ms": dom_avg_ms, "gbs": dom_bytes / (dom_avg_ms * 1e-3) / 1e9,
                      # multiply-adds of the launch (every weight times every input row)
                      "flops_per_launch": 2.0 * batch * sum(
@@ -1059,14 +1061,19 @@ def main():
     peak, peak_src = peaks()
     value = job_gbs(world, r["bytes_per_step"], ms_all)
     dom = r["dominant"]
-    if a.batch <= 4:
+    if a.batch <= 8:
+        # the library's dispatch: batch 1 on the CUDA-core GEMV except INT4
+        # launches of >= 96 MiB of weights; batches 2..8 on the warp-MMA GEMV
+        mv = a.batch > 1 or ("int4" in a.workload and dom["weight_bytes"] >= 96 << 20)
+        prof, src = ((f"mv_{a.workload}_gateup_b{a.batch}.md", "k_mv.cu") if mv
+                     else (f"gemv_{a.workload}_gateup.md", "k_gemv.cu"))
         roofline = {"bound": "hbm", "achieved": round(dom["gbs"], 2), "peak": peak,
                     "unit": "GB/s", "frac": round(dom["gbs"] / peak, 4),
                     "traffic": profiled_traffic(
-                        f"gemv_{a.workload}_gateup.md",
-                        "weight_only_quantized_dequant_gb300/csrc/k_gemv.cu"),
+                        prof, "weight_only_quantized_dequant_gb300/csrc/" + src),
                     "kernel": ("gemv sequence (one layer per launch)" if a.fused
-                               else f"gemv ({dom['group']} grouped launch)"),
+                               else f"{'mv_kernel (warp MMA)' if mv else 'gemv_kernel'} "
+                                    f"({dom['group']} grouped launch)"),
                     "bytes_per_launch": dom["bytes_per_launch"],
                     "avg_launch_us": round(dom["avg_ms"] * 1e3, 3),
                     "peak_kind": peak_src}

@@ -124,10 +124,12 @@ qz_status qz_gemv_int8(const qz_int8_weight *w, const qz_half *x, qz_half *y,
                        qz_stream s);
 
 /* Y[b][i] = fp16( scale * sum_j q[i][j] * X[b][j] ) for b < B.
- * X [B][ldx], Y [B][ldy]; 1 <= B <= QZ_MAX_BATCH.  B <= 4 runs on CUDA
- * cores when the batch's fp32 inputs fit in shared memory (about 4*B*K
- * bytes <= 227 KiB); larger batches, and B = 2..4 beyond that, run on the
- * tensor cores (tcgen05, fp16 x fp16 products of the exact codes, fp32
+ * X [B][ldx], Y [B][ldy]; 1 <= B <= QZ_MAX_BATCH.  The path depends on the
+ * shape, never the result bound: B = 1 as qz_gemv_int8; B = 2..8 on the
+ * warp-MMA kernel (mma.sync on the exact codes, fp32 accumulation) when the
+ * batch's fp16 inputs and a ring of weight stages fit in shared memory
+ * (roughly 2*B*K bytes well under 227 KiB); otherwise, and for B > 8, on
+ * the tensor cores (tcgen05, fp16 x fp16 products of the exact codes, fp32
  * accumulation in tensor memory). */
 qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X,
                        int64_t ldx, qz_half *Y, int64_t ldy, void *workspace,
@@ -143,10 +145,12 @@ qz_status qz_gemm_int8(const qz_int8_weight *w, int64_t B, const qz_half *X,
  * or the device.  The workspace argument of qz_gemm_* may be NULL (the
  * tensor-core kernel then gathers its inputs itself and gives each SM whole
  * 128-row tiles only, much more slowly); if given it must be 16-byte aligned
- * and at least this many bytes, caller-owned, and not used by other work
- * while the call runs.  The CUDA-core path ignores it.  Results with and
- * without a workspace agree within the products' rounding bound, not bit for
- * bit (the fp32 partial sums are added in a different order). */
+ * and at least this many bytes (checked whatever path the call takes:
+ * QZ_ERR_INVALID_ARG if short, QZ_ERR_ALIGNMENT if misaligned, before
+ * anything is enqueued), caller-owned, and not used by other work while the
+ * call runs.  Only the tensor-core path uses it.  Results with and without a
+ * workspace agree within the products' rounding bound, not bit for bit (the
+ * fp32 partial sums are added in a different order). */
 size_t qz_gemm_workspace_bytes(int64_t B, int64_t K, int64_t n_out);
 
 /* n matrices (1 <= n <= QZ_MAX_GROUP) that read the same input x, in one
@@ -258,10 +262,11 @@ typedef struct {
 qz_status qz_gemv_int4_outlier(const qz_int4o_weight *w, const qz_half *x,
                                qz_half *y, qz_stream s);
 
-/* The same for a batch: X [B][ldx], Y [B][ldy], 1 <= B <= QZ_MAX_BATCH; same
- * CUDA-core / tensor-core split as qz_gemm_int8.  On the tensor cores the
- * outlier and background products accumulate separately (two accumulators)
- * and meet as y = D_out + s_i * D_bg. */
+/* The same for a batch: X [B][ldx], Y [B][ldy], 1 <= B <= QZ_MAX_BATCH; the
+ * same choice of kernels as qz_gemm_int8, except that batch-1 launches of
+ * at least 96 MiB of weights (rows times padded row bytes) also run on the
+ * warp-MMA kernel.  Every kernel keeps the outlier and background products
+ * apart and combines them as y = D_out + s_i * D_bg. */
 qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B,
                                const qz_half *X, int64_t ldx, qz_half *Y,
                                int64_t ldy, void *workspace,

@@ -506,6 +506,39 @@ def test_full_70b_down_proj_int4_sampled():
     assert_close(y[rows], y_ref[0], a_ref[0], "70b down sampled")
 
 
+@pytest.mark.slow
+def test_full_70b_gate_up_grouped_int4_sampled():
+    """The largest batch-1 launch of the 70B layer: gate and up (2 x 28672 x
+    8192, one permutation table from both matrices' saliency) in one grouped
+    call.  Saliency and permutation exact; codes and outputs checked on 64
+    sampled rows of each matrix plus the rows at both ends."""
+    N, K = 28672, 8192
+    n_out = O.default_n_out(K)
+    Ws = [S.weight(N, K, 81 + i, device=DEV) for i in range(2)]
+    prof = S.x_profile(K, n_out, 83, device=DEV)
+    colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+    for W in Ws:
+        qz().saliency_accumulate(W, colsum)
+    perm = qz().select_outliers(colsum, prof, n_out)
+    ws = [qz().quantize_int4_outlier(W, perm, n_out) for W in Ws]
+    x = S.activation(1, K, 84, device=DEV)
+    ys = qz().gemv_int4_outlier_grouped(ws, x[0])
+    assert qz().device_error() == 0
+    sal = sum(O.saliency_fixed(W.cpu().numpy()) for W in Ws)
+    assert np.array_equal(colsum.cpu().numpy(), sal)
+    pn = O.select_outliers(sal, prof.cpu().numpy(), n_out)
+    assert np.array_equal(perm.cpu().numpy(), pn)
+    rng = np.random.default_rng(1)
+    for i, (W, w, y) in enumerate(zip(Ws, ws, ys)):
+        rows = np.unique(np.concatenate([rng.choice(N, 64, replace=False),
+                                         [0, 1, 15, 16, N - 17, N - 16, N - 1]]))
+        wo, q4, sc = O.int4o_quantize(W[torch.from_numpy(rows).to(DEV)].cpu().numpy(), pn, n_out)
+        assert np.array_equal(w.q4.cpu().numpy()[rows], q4)
+        assert np.array_equal(w.scale.cpu().numpy()[rows], sc)
+        y_ref, a_ref = O.int4o_product_ref(wo, q4, sc, pn, n_out, K, x.cpu().numpy())
+        assert_close(y[rows], y_ref[0], a_ref[0], f"70b gate+up sampled m={i}")
+
+
 # ----------------------------------------------------------------- pager ---
 def test_pager_streams_layers_and_reports_injected_failure():
     import weight_only_quantized_dequant_gb300 as m

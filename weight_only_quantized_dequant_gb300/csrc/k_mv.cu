@@ -1,5 +1,5 @@
-// Dequant-GEMV for small batches (2..8) with the multiply-adds on warp-level
-// MMA.
+// Dequant-GEMV for small batches (2..8, and the largest batch-1 INT4
+// launches) with the multiply-adds on warp-level MMA.
 //
 // What is computed (per output row i and batch row b), as in k_gemv.cu:
 //   INT8  ("Open Origin - ELG Stream Layer", INT8 Quantization & Direct
@@ -33,9 +33,15 @@
 //    per copy keep HBM efficient; the copies carry an L2 evict-first hint so
 //    that the small, reused tensors (permutations, inputs, outputs) stay in
 //    L2 while the weights stream past.
-//  * Eight consumer warps split the K blocks of every stage; a 16-row tile's
-//    parts are added in shared memory by the last warp to finish the tile, in
-//    warp order (the result does not depend on timing).
+//  * A stage holds TP 16-row tiles (1 or 2); the eight consumer warps split
+//    into TP groups, each splitting the K blocks of its tile; a tile's parts
+//    are added in shared memory by the last warp of its group to finish it,
+//    in warp order (the result does not depend on timing), or stored
+//    directly when one warp owns the tile.
+//  * Batches 9..16 were tried with two 8-column blocks per converted weight
+//    fragment (inputs of 16 rows staged in shared memory): slower than the
+//    tensor-core GEMM on 30 of the 32 launches of the 3B/7B/70B/Gemma layers
+//    (7B o at batch 16: 31.9 against 15.4 us), so batches above 8 stay there.
 //  * INT4 inputs are first copied contiguously into shared memory (into ring
 //    slots that the producer fills only after the input is staged) and then
 //    gathered there through the permutation, which is read with coalesced
@@ -770,6 +776,7 @@ size_t mv_layout(bool int4, const GemvParams &p, int B, int raw, int cap, int mi
 //    else three or more stages of the longest pieces, then two.
 //  * Inputs copied to shared memory before the gather whenever that fits.
 constexpr int64_t kTwoTileRows = 200;
+constexpr uint32_t kMinPiece = 576;  // bytes of a row per stage, unless whole rows
 
 size_t mv_plan(bool int4, const GemvParams &p, int B, const DeviceInfo &di, MvLaunch &L) {
   const size_t avail = (size_t)di.max_smem_optin;
@@ -791,7 +798,9 @@ size_t mv_plan(bool int4, const GemvParams &p, int B, const DeviceInfo &di, MvLa
     for (int min_ns = 3; min_ns >= 2; --min_ns)
       for (int cap : kRowCaps) {
         const size_t smem = mv_layout(int4, p, B, raw, cap, min_ns, 1, avail, L);
-        if (smem) return smem;
+        // pieces shorter than kMinPiece stream poorly: leave those launches
+        // to the tensor-core GEMM
+        if (smem && (L.pr.nst == 1 || (uint32_t)L.pr.skc * kKB >= kMinPiece)) return smem;
       }
   return 0;
 }
