@@ -1062,9 +1062,9 @@ def main():
     value = job_gbs(world, r["bytes_per_step"], ms_all)
     dom = r["dominant"]
     if a.batch <= 8:
-        # the library's dispatch: batch 1 on the CUDA-core GEMV except INT4
-        # launches of >= 96 MiB of weights; batches 2..8 on the warp-MMA GEMV
-        mv = a.batch > 1 or ("int4" in a.workload and dom["weight_bytes"] >= 96 << 20)
+        # the library's dispatch: batch 1 on the CUDA-core GEMV, batches 2..8
+        # on the warp-MMA GEMV (when the staged inputs fit)
+        mv = a.batch > 1
         prof, src = ((f"mv_{a.workload}_gateup_b{a.batch}.md", "k_mv.cu") if mv
                      else (f"gemv_{a.workload}_gateup.md", "k_gemv.cu"))
         roofline = {"bound": "hbm", "achieved": round(dom["gbs"], 2), "peak": peak,

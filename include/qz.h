@@ -263,10 +263,8 @@ qz_status qz_gemv_int4_outlier(const qz_int4o_weight *w, const qz_half *x,
                                qz_half *y, qz_stream s);
 
 /* The same for a batch: X [B][ldx], Y [B][ldy], 1 <= B <= QZ_MAX_BATCH; the
- * same choice of kernels as qz_gemm_int8, except that batch-1 launches of
- * at least 96 MiB of weights (rows times padded row bytes) also run on the
- * warp-MMA kernel.  Every kernel keeps the outlier and background products
- * apart and combines them as y = D_out + s_i * D_bg. */
+ * same choice of kernels as qz_gemm_int8.  Every kernel keeps the outlier
+ * and background products apart and combines them as y = D_out + s_i * D_bg. */
 qz_status qz_gemm_int4_outlier(const qz_int4o_weight *w, int64_t B,
                                const qz_half *X, int64_t ldx, qz_half *Y,
                                int64_t ldy, void *workspace,

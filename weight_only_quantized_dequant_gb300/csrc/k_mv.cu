@@ -1,5 +1,5 @@
-// Dequant-GEMV for small batches (2..8, and the largest batch-1 INT4
-// launches) with the multiply-adds on warp-level MMA.
+// Dequant-GEMV for small batches (2..8) with the multiply-adds on warp-level
+// MMA.
 //
 // What is computed (per output row i and batch row b), as in k_gemv.cu:
 //   INT8  ("Open Origin - ELG Stream Layer", INT8 Quantization & Direct

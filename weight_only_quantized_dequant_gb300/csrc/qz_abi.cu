@@ -169,21 +169,11 @@ qz_status gemm_common(bool int4, GemvParams &p, int64_t B, const qz_half *X, int
     if ((uintptr_t)ws & 15u) return QZ_ERR_ALIGNMENT;
   }
   // Batch 1 runs on the CUDA-core GEMV (one fp32 FMA per weight keeps pace
-  // with HBM at one input row), except INT4 launches of at least
-  // kMvBatch1Bytes of weights, where the warp-MMA GEMV's cheaper conversion
-  // outweighs its per-tile costs (measured: the 70B gate+up and down launches
-  // 3-5% faster, the 70B step +1%; every smaller launch, and INT8, is faster
-  // on the CUDA cores).  Batches 2..8 run on the warp-MMA GEMV, where the
+  // with HBM at one input row); batches 2..8 on the warp-MMA GEMV, where the
   // CUDA cores would need one FMA per weight and input row.  Either takes
   // the call when its staged inputs fit in shared memory; larger batches are
   // dense enough for the tcgen05 GEMM, which also takes the small batches at
   // the few K too large to stage (its inputs stream in tiles).
-  if (B == 1 && int4) {
-    int64_t rows_all = 0;
-    for (int m = 0; m < n; ++m) rows_all += p.row_end[m] - (m ? p.row_end[m - 1] : 0);
-    if (rows_all * (int64_t)(p.cpr + p.ocpr) * 16 >= kMvBatch1Bytes && mv_fits(int4, 1, p))
-      return launch_mv(int4, 1, p, s);
-  }
   if (B == 1 && gemv_smem_bytes(int4, 1, p) <= (size_t)di.max_smem_optin)
     return launch_gemv(int4, 1, p, s);
   if (B <= kMvMaxBatch && mv_fits(int4, (int)B, p)) return launch_mv(int4, (int)B, p, s);

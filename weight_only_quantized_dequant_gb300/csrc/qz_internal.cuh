@@ -66,7 +66,6 @@ qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s);
 
 // Warp-MMA GEMV (mma.sync on dequantized codes) for batch 1..kMvMaxBatch.
 constexpr int kMvMaxBatch = 8;
-constexpr int64_t kMvBatch1Bytes = (int64_t)96 << 20;  // batch-1 INT4 launches this large use it
 struct MvProduct {  // shapes of the product, chosen by the host
   int Ko, Kb;         // 64-byte K blocks per row: outliers (INT4), codes
   int nst, skc;       // ring stages per 16-row tile, K blocks per stage
