@@ -51,7 +51,8 @@ def parse():
                     help="also time the 3B vocabulary lookup + lm_head (tied INT8, untied INT4)")
     ap.add_argument("--tiered", action="store_true",
                     help="also time the 70B stack with its first 40 (60) layers in HBM and "
-                         "the rest streamed from pinned host memory")
+                         "the rest streamed from pinned host memory, and with 0 (40) layers "
+                         "in HBM and the rest read in place from pinned host memory")
     ap.add_argument("--stream-quant", action="store_true",
                     help="also time the streaming quantizer (checkpoint file -> pool file)")
     ap.add_argument("--fused", action="store_true",
@@ -895,16 +896,18 @@ def measure_head(name: str, steps: int, warmup: int, device):
 
 
 def measure_tiered(wl_name: str, resident: int, steps: int, warmup: int, device,
-                   distinct: int = 4):
-    """First `resident` layers in HBM, the rest streamed from pinned host
-    memory through the pager."""
+                   distinct: int = 4, mode: str = "paged"):
+    """First `resident` layers in HBM, the rest in pinned host memory,
+    streamed through the pager (mode "paged") or read in place by the
+    zero-copy GEMV (mode "zero_copy")."""
     import torch
 
     from weight_only_quantized_dequant_gb300 import api
     from weight_only_quantized_dequant_gb300 import stack as ST
     from weight_only_quantized_dequant_gb300 import synthetic as S
 
-    ts = ST.TieredStack(S.WORKLOADS[wl_name], resident, distinct=distinct, device=device)
+    ts = ST.TieredStack(S.WORKLOADS[wl_name], resident, distinct=distinct, device=device,
+                        mode=mode)
     torch.cuda.synchronize(device)
     cs = ts.stream
     for _ in range(warmup):
@@ -919,11 +922,14 @@ def measure_tiered(wl_name: str, resident: int, steps: int, warmup: int, device,
     assert api.device_error() == 0
     ms = e0.elapsed_time(e1) / steps
     tier_b = ts.n_layers - ts.resident
-    out = {"workload": wl_name, "layers": ts.n_layers, "resident": ts.resident,
+    out = {"workload": wl_name, "mode": mode, "layers": ts.n_layers, "resident": ts.resident,
            "ms_per_step": round(ms, 3), "us_per_layer": round(ms * 1e3 / ts.n_layers, 2),
            "gbs": round(ts.bytes_per_step() / (ms * 1e-3) / 1e9, 1),
            "host_layer_bytes": ts.weight_bytes_per_layer}
-    if tier_b:
+    if tier_b and mode == "zero_copy" and ts.resident == 0:
+        # every weight byte crossed the host link once: the in-place read rate
+        out["host_read_gbs"] = round(tier_b * ts.weight_bytes_per_layer / (ms * 1e-3) / 1e9, 1)
+    if tier_b and mode == "paged":
         parts = paged_parts(ts.host, device)
         out.update(parts)
         # resident layers cost their GEMVs; paged ones the slower half
@@ -1031,9 +1037,9 @@ def main():
 
     if a.tiered and rank == 0:
         wl70 = "llama_70b_int4o"
-        for res in (40, 60):
-            extra[f"{wl70}_tiered_{res}"] = measure_tiered(wl70, res, max(2, a.steps // 10), 1,
-                                                           device)
+        for res, mode in ((40, "paged"), (60, "paged"), (0, "zero_copy"), (40, "zero_copy")):
+            extra[f"{wl70}_tiered_{res}_{mode}"] = measure_tiered(
+                wl70, res, max(2, a.steps // 10), 1, device, mode=mode)
         extra["link_probe_gbs"] = round(h2d_probe_gbs(device), 1)
 
     if a.stream_quant and rank == 0:

@@ -337,6 +337,32 @@ qz_status qz_gemv_int4_outlier_sequence(const qz_int4o_weight *ws, const int *co
                                         qz_stream s);
 
 /* ======================================================================
+ * Zero-copy products  ["Open Origin - ELG Stream Layer", Technical
+ * Architecture > INT8 Quantization & Direct Mapping: INT8 tensors kept in a
+ * pre-allocated pinned memory pool and reached by zero-copy DMA; "NTransformer"
+ * summary, 3-Tier Adaptive Caching, Tier B: layers kept in pinned RAM]
+ *
+ * The batch-1 grouped products with the weights read in place by the GPU:
+ * every weight buffer of ws (codes, scales, and for INT4 outliers and perm)
+ * may be pinned host memory mapped into the device's address space
+ * (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped; under
+ * unified addressing the host pointer is the device pointer) or device
+ * memory.  Each call asks the runtime for the device address of every buffer
+ * (cudaPointerGetAttributes); pageable or unknown memory gives
+ * QZ_ERR_INVALID_ARG and nothing is launched.  x and ys are device memory.
+ * Results equal the device-resident calls bit for bit; only the way codes
+ * are read differs (plain loads by every lane, over the host link, instead
+ * of bulk copies).  The host memory must stay pinned and unchanged until the
+ * stream has passed the call.  Same sizes and errors as the grouped calls.
+ * ====================================================================== */
+qz_status qz_gemv_int8_grouped_mapped(const qz_int8_weight *ws, int n,
+                                      const qz_half *x, qz_half *const *ys,
+                                      qz_stream s);
+qz_status qz_gemv_int4_outlier_grouped_mapped(const qz_int4o_weight *ws, int n,
+                                              const qz_half *x,
+                                              qz_half *const *ys, qz_stream s);
+
+/* ======================================================================
  * Layer pager  [ELG "Key Features" 2 (prefetch, transfer, reconstruct,
  * purge) and 3 (a second CUDA stream copies layer N+1 while layer N
  * computes); NTR "3-Tier Adaptive Caching", Tier B (pinned RAM, H2D DMA)]

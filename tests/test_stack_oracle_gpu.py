@@ -12,7 +12,7 @@ dependent launch (Gemma-2-9B INT8 and the 7B INT4-outlier shapes), the
 paged Gemma stack (layers streamed from pinned host memory through the
 pager, "Open Origin - ELG Stream Layer", Key Features 1-3) and a tiered 3B
 stack with both tiers in use ("NTransformer" summary, 3-Tier Adaptive
-Caching, tiers A and B).
+Caching, tiers A and B), tier B paged or read in place (zero-copy).
 """
 import numpy as np
 import pytest
@@ -199,6 +199,29 @@ def test_tiered_3b_step_both_tiers_against_oracle():
         # tier B: positions 1 and 2 read host layers 0 and 1
         for hl in range(2):
             check_outputs(ts.host.y[hl], oracle_layer(wl, hl), f"tiered 3b host layer {hl}")
+    finally:
+        ts.close()
+
+
+def test_tiered_3b_zero_copy_step_against_oracle():
+    """The same 3-layer 3B stack with tier B read in place from pinned host
+    memory by the zero-copy GEMV ("Open Origin - ELG Stream Layer", INT8
+    Quantization & Direct Mapping, zero-copy DMA; "NTransformer", Tier B):
+    every output of both tiers against the oracle."""
+    from weight_only_quantized_dequant_gb300 import stack as ST
+    import weight_only_quantized_dequant_gb300 as qz
+    wl = S.WORKLOADS["llama32_3b_int4o"]
+    ts = ST.TieredStack(wl, resident=1, n_layers=3, distinct=2, mode="zero_copy")
+    try:
+        _clear(ts.dev.y)
+        _clear(ts.host.y)
+        torch.cuda.synchronize()
+        ts.run_step()
+        ts.stream.synchronize()
+        assert qz.device_error() == 0
+        check_outputs(ts.dev.y[0], oracle_layer(wl, 0), "zero-copy tiered 3b resident layer 0")
+        for hl in range(2):
+            check_outputs(ts.host.y[hl], oracle_layer(wl, hl), f"zero-copy tiered 3b host layer {hl}")
     finally:
         ts.close()
 

@@ -74,6 +74,10 @@ _SIGS = {
                                           c_void_p, c_int64, c_void_p]),
     "qz_gemv_int4_outlier_grouped": (_S, [POINTER(Int4oWeight), c_int, c_void_p,
                                           POINTER(c_void_p), c_void_p]),
+    "qz_gemv_int8_grouped_mapped": (_S, [POINTER(Int8Weight), c_int, c_void_p,
+                                         POINTER(c_void_p), c_void_p]),
+    "qz_gemv_int4_outlier_grouped_mapped": (_S, [POINTER(Int4oWeight), c_int, c_void_p,
+                                                 POINTER(c_void_p), c_void_p]),
     "qz_gemm_int4_outlier_grouped": (_S, [POINTER(Int4oWeight), c_int, c_int64, c_void_p,
                                           c_int64, POINTER(c_void_p), POINTER(c_int64),
                                           c_void_p, c_size_t, c_void_p]),

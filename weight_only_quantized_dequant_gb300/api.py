@@ -307,6 +307,26 @@ def gemv_int4_outlier_grouped(ws, x: torch.Tensor, ys=None, stream=None):
     return ys
 
 
+def gemv_mapped(ws, x: torch.Tensor, ys=None, stream=None):
+    """Batch-1 grouped product with the weights read in place (zero-copy,
+    qz_gemv_*_grouped_mapped): the matrices' tensors may be pinned host
+    tensors (or device tensors).  ws: Int8Matrix or Int4oMatrix list sharing
+    K (INT4: and the permutation); x and ys on the GPU."""
+    _need_cuda(x)
+    n = len(ws)
+    ys = [_vec_out(x, w.N) for w in ws] if ys is None else ys
+    for w in ws:
+        for t in w.tensors():
+            if t.numel() and not (t.is_cuda or t.is_pinned()):
+                raise ValueError("zero-copy weights must be device or pinned host tensors")
+    int8 = isinstance(ws[0], Int8Matrix)
+    arr = ((Int8Weight if int8 else Int4oWeight) * n)(*[w.struct() for w in ws])
+    yp = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    fn = "qz_gemv_int8_grouped_mapped" if int8 else "qz_gemv_int4_outlier_grouped_mapped"
+    _lib.call(fn, arr, n, x.data_ptr(), yp, _stream(stream))
+    return ys
+
+
 def _grouped_gemm(fn: str, struct_t, ws, X: torch.Tensor, Ys, stream, workspace, n_out: int):
     _need_cuda(X)
     n, B = len(ws), X.shape[0]

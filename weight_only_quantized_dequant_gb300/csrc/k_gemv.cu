@@ -47,6 +47,44 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   return r;
 }
 
+// Weight loads.  Device-resident weights go through the non-coherent path
+// (codes arrive by bulk copies); weights read in place from mapped pinned host
+// memory (ZC, zero-copy) use plain global loads.
+template <bool ZC>
+__device__ __forceinline__ uint4 ld_w4(const uint4 *p) {
+  if constexpr (ZC) {
+    uint4 r;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+  } else {
+    return ld_stream(p);
+  }
+}
+
+template <bool ZC>
+__device__ __forceinline__ float ld_wf(const float *p) {
+  if constexpr (ZC) {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+  } else {
+    return __ldg(p);
+  }
+}
+
+template <bool ZC>
+__device__ __forceinline__ int ld_wi(const int32_t *p) {
+  if constexpr (ZC) {
+    int v;
+    asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+  } else {
+    return __ldg(p);
+  }
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -263,9 +301,14 @@ __device__ __forceinline__ void locate(const Bounds &bd, int r, int &m, int &i) 
 }
 
 // W: warps per CTA (16, or 20 at batch 1 when shared memory allows).
-template <bool INT4, int B, int W>
+// ZC (batch 1): the weights (codes, outliers, scales, permutation) may be in
+// mapped pinned host memory; every lane then reads its chunks of each round
+// with plain loads, without the bulk-copy ring (whose engine is not asked to
+// read host memory), and the permutation is read from where it lies.
+template <bool INT4, int B, int W, bool ZC = false>
 __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
     gemv_kernel(const __grid_constant__ GemvParams p) {
+  static_assert(!ZC || B == 1, "zero-copy reads at batch 1 only");
   constexpr int kWarps = W, kThreads = W * 32;
   constexpr int R = Ring<B>::R, NS = Ring<B>::NS, kRPS = Ring<B>::RPS;
   constexpr uint32_t kStageRow = Ring<B>::STAGE_ROW;
@@ -280,7 +323,8 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
   __half *xs = reinterpret_cast<__half *>(smem_raw);
   __half *xo = reinterpret_cast<__half *>(smem_raw + B * bstride);
   uint8_t *ring = smem_raw + (((size_t)B * bstride + (size_t)B * ostride + 127) & ~(size_t)127);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)kWarps * NS * R * kStageRow);
+  uint64_t *bars =
+      reinterpret_cast<uint64_t *>(ring + (ZC ? 0 : (size_t)kWarps * NS * R * kStageRow));
 
   const int64_t r0 = p.total_rows * blockIdx.x / gridDim.x;
   const int64_t r1 = p.total_rows * (blockIdx.x + 1) / gridDim.x;
@@ -364,8 +408,10 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
 
   // The first stages are issued before the wait: weights are static, so
   // under programmatic overlap they stream in during the previous kernel.
-  if (items > 0) prow_setup(0);
-  for (int it = 0; it < NS - 1 && pleft > 0; ++it) issue_next();
+  if constexpr (!ZC) {
+    if (items > 0) prow_setup(0);
+    for (int it = 0; it < NS - 1 && pleft > 0; ++it) issue_next();
+  }
 
   // INT4: the permutation (static) goes into the free ring block before the
   // wait, read with coalesced 16-byte loads, as 16-bit entries (K <= 57344):
@@ -375,7 +421,7 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
   const int elems = staged * EPC;           // staged inputs per batch row (multiple of 8)
   // (measured: pays for K > 4096; at smaller K the gather after the wait is
   // short and the extra barrier costs more than it saves)
-  const bool perm_smem = INT4 && NS == 2 && p.K > 4096 &&
+  const bool perm_smem = !ZC && INT4 && NS == 2 && p.K > 4096 &&
                          (size_t)(elems + p.ocpr * 8) * 2 <= slot_stride;
   if (INT4 && perm_smem) {
     const int K = p.K, n_out = p.n_out;
@@ -462,7 +508,7 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
       if constexpr (INT4) {
         int idx[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) idx[k] = e0 + k < p.kb ? __ldg(p.perm + p.n_out + e0 + k) : -1;
+        for (int k = 0; k < 8; ++k) idx[k] = e0 + k < p.kb ? ld_wi<ZC>(p.perm + p.n_out + e0 + k) : -1;
         __half v[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) v[k] = idx[k] >= 0 ? xb[idx[k]] : hzero;
@@ -483,7 +529,7 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
     if constexpr (INT4) {
 #pragma unroll 1
       for (int e = threadIdx.x; e < p.ocpr * 8; e += kThreads)
-        xo[b * ostride / 2 + e] = e < p.n_out ? xb[__ldg(p.perm + e)] : hzero;
+        xo[b * ostride / 2 + e] = e < p.n_out ? xb[ld_wi<ZC>(p.perm + e)] : hzero;
     }
   }
   }
@@ -512,14 +558,38 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
     for (int rr = 0; rr < R; ++rr) {
       live[rr] = rb + rr < rhi;
       locate(bd, live[rr] ? rb + rr : rhi - 1, mrow[rr], irow[rr]);
-      srow[rr] = INT4 ? __ldg(p.scale[mrow[rr]] + irow[rr]) : __ldg(p.scale[mrow[rr]]);
+      srow[rr] = INT4 ? ld_wf<ZC>(p.scale[mrow[rr]] + irow[rr]) : ld_wf<ZC>(p.scale[mrow[rr]]);
       ov[rr] = make_uint4(0, 0, 0, 0);
       if (INT4 && lane < p.ocpr)
-        ov[rr] = ld_stream(reinterpret_cast<const uint4 *>(
+        ov[rr] = ld_w4<ZC>(reinterpret_cast<const uint4 *>(
                                p.w_out[mrow[rr]] + (int64_t)irow[rr] * p.ld_out[mrow[rr]]) +
                            lane);
     }
     for (int sj = 0; sj < SPR; ++sj) {
+      if constexpr (ZC) {
+        // every lane loads its chunk of each round of the stage in place
+        uint4 v[kRPS][R];
+#pragma unroll
+        for (int u = 0; u < kRPS; ++u) {
+          const int c = (sj * kRPS + u) * 32 + lane;  // chunk of the row
+#pragma unroll
+          for (int rr = 0; rr < R; ++rr)
+            v[u][rr] = c < cpr ? ld_w4<true>(reinterpret_cast<const uint4 *>(
+                                     p.codes[mrow[rr]] + (int64_t)irow[rr] * p.ld_codes[mrow[rr]]) +
+                                 c)
+                               : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kRPS; ++u) {
+          const int j = sj * kRPS + u;
+          if (j < Jw) {  // warp-uniform
+            const uint32_t o = lane_off + (uint32_t)j * kRound;
+            if constexpr (INT4) int4_chunk<B, R>(v[u], xs, o, bstride, acc);
+            else int8_chunk<B, R>(v[u], xs, o, bstride, acc);
+          }
+        }
+        continue;
+      }
       if (ok && pleft > 0) {
         // the slot being refilled was read by every lane before the last
         // __syncwarp; order those reads before the async-proxy write
@@ -572,7 +642,7 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
                                                             (int64_t)irow[rr] * p.ld_out[mrow[rr]]);
 #pragma unroll 1
         for (int c = lane; c < p.ocpr; c += 32) {
-          const uint4 v = c == lane ? ov[rr] : ld_stream(orow + c);
+          const uint4 v = c == lane ? ov[rr] : ld_w4<ZC>(orow + c);
 #pragma unroll
           for (int b = 0; b < B; ++b) {
             const uint4 xv = *reinterpret_cast<const uint4 *>(
@@ -599,7 +669,7 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
   }
   // A warp that gave up a wait may still have copies in flight into its
   // ring; give them a bounded time to land before the CTA's shared memory goes.
-  if (!ok && lane == 0) ring_drain<NS>(bar_w, fail_at, items - pleft);
+  if (!ZC && !ok && lane == 0) ring_drain<NS>(bar_w, fail_at, items - pleft);
 }
 
 // ---------------------------------------------------------------------------
@@ -923,22 +993,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_seq_kernel(const __grid_cons
 // Shared memory of gemv_kernel with W warps: staged inputs, then the ring
 // and its barriers as the kernel carves them (Ring<B> is the same for every
 // B > 1).
-size_t gemv_smem_bytes_w(bool int4, int B, const GemvParams &p, int W) {
+size_t gemv_smem_bytes_w(bool int4, int B, const GemvParams &p, int W, bool zc = false) {
   const size_t cs = int4 ? 80 : 48;  // padded staged fp16 bytes per chunk
   const size_t rounds = p.cpr > 0 ? (size_t)(p.cpr + 31) / 32 : 1;
   const size_t staged = (rounds * 32 * cs + (int4 ? (size_t)p.ocpr * 16 : 0)) * (size_t)B;
   const size_t NS = B == 1 ? Ring<1>::NS : Ring<2>::NS;
   const size_t R = B == 1 ? Ring<1>::R : Ring<2>::R;
   const size_t stage_row = B == 1 ? Ring<1>::STAGE_ROW : Ring<2>::STAGE_ROW;
-  const size_t ring = (size_t)W * NS * R * stage_row;
+  const size_t ring = zc ? 0 : (size_t)W * NS * R * stage_row;
   return ((staged + 127) & ~(size_t)127) + ring + (size_t)W * NS * 8;
 }
 
-template <bool INT4, int B, int W>
+template <bool INT4, int B, int W, bool ZC = false>
 qz_status launch_w(const GemvParams &p, const DeviceInfo &di, cudaStream_t s) {
   constexpr int R = Ring<B>::R;
-  auto kern = gemv_kernel<INT4, B, W>;
-  const size_t smem = gemv_smem_bytes_w(INT4, B, p, W);
+  auto kern = gemv_kernel<INT4, B, W, ZC>;
+  const size_t smem = gemv_smem_bytes_w(INT4, B, p, W, ZC);
   if (smem > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -1042,6 +1112,18 @@ qz_status read_gemv_error(int *code, int clear) {
   }
   *code = v;
   return QZ_OK;
+}
+
+// Batch-1 product with the weights read in place (zero-copy), 20 warps.
+qz_status launch_gemv_mapped(bool int4, const GemvParams &p, cudaStream_t s) {
+  DeviceInfo di;
+  qz_status st = device_info(&di);
+  if (st != QZ_OK) return st;
+  return int4 ? launch_w<true, 1, 20, true>(p, di, s) : launch_w<false, 1, 20, true>(p, di, s);
+}
+
+size_t gemv_mapped_smem_bytes(bool int4, const GemvParams &p) {
+  return gemv_smem_bytes_w(int4, 1, p, 20, true);
 }
 
 qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s) {

@@ -217,6 +217,47 @@ qz_status sequence_common(bool int4, const W *ws, const int *counts, int n,
   sp.sync = reinterpret_cast<unsigned int *>(sync);
   return launch_gemv_seq(int4, sp, s);
 }
+// The address under which the device reads a weight buffer in place: device
+// memory, or host memory that is pinned and mapped (unified addressing).
+// Pageable or unknown memory is refused, so nothing is launched on it.
+qz_status device_view(const void *ptr, const void **dev) {
+  if (!ptr) {
+    *dev = nullptr;
+    return QZ_OK;
+  }
+  cudaPointerAttributes a;
+  const cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return QZ_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeUnregistered || !a.devicePointer) return QZ_ERR_INVALID_ARG;
+  *dev = a.devicePointer;
+  return QZ_OK;
+}
+
+template <typename T>
+qz_status device_view_t(T *&ptr) {
+  const void *d = nullptr;
+  QZ_TRY(device_view(ptr, &d));
+  ptr = reinterpret_cast<T *>(const_cast<void *>(d));
+  return QZ_OK;
+}
+
+// Batch-1 grouped product with the weights read in place (zero-copy).
+qz_status mapped_common(bool int4, GemvParams &p, const qz_half *x, qz_half *const *ys, int n,
+                        cudaStream_t s) {
+  p.x = reinterpret_cast<const __half *>(x);
+  p.overlap = overlap_enabled();
+  p.ldx = 0;
+  for (int m = 0; m < QZ_MAX_GROUP; ++m) p.ldy[m] = 0;
+  for (int m = 0; m < n; ++m) p.y[m] = reinterpret_cast<__half *>(ys[m]);
+  DeviceInfo di;
+  QZ_TRY(device_info(&di));
+  if (gemv_mapped_smem_bytes(int4, p) > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
+  return launch_gemv_mapped(int4, p, s);
+}
+
 }  // namespace
 }  // namespace qz
 
@@ -434,6 +475,48 @@ qz_status qz_gemm_int4_outlier_grouped(const qz_int4o_weight *ws, int n, int64_t
   fill_int4o(p, ws, n);
   return gemm_common(true, p, B, X, ldx, Ys, ldys, n, workspace, workspace_bytes,
                      (cudaStream_t)s);
+}
+
+qz_status qz_gemv_int8_grouped_mapped(const qz_int8_weight *ws, int n, const qz_half *x,
+                                      qz_half *const *ys, qz_stream s) {
+  if (!ws || !ys || n < 1) return QZ_ERR_INVALID_ARG;
+  if (n > QZ_MAX_GROUP) return QZ_ERR_UNSUPPORTED;
+  qz_int8_weight v[QZ_MAX_GROUP];
+  for (int m = 0; m < n; ++m) {
+    QZ_TRY(check_int8_weight(&ws[m]));
+    if (ws[m].K != ws[0].K) return QZ_ERR_INVALID_ARG;
+    QZ_TRY(check_vec(ys[m], 1, ws[m].N, 0));
+    v[m] = ws[m];
+    QZ_TRY(device_view_t(v[m].q));
+    QZ_TRY(device_view_t(v[m].scale));
+  }
+  QZ_TRY(check_vec(x, 1, ws[0].K, 0));
+  GemvParams p;
+  fill_int8(p, v, n);
+  return mapped_common(false, p, x, ys, n, (cudaStream_t)s);
+}
+
+qz_status qz_gemv_int4_outlier_grouped_mapped(const qz_int4o_weight *ws, int n,
+                                              const qz_half *x, qz_half *const *ys,
+                                              qz_stream s) {
+  if (!ws || !ys || n < 1) return QZ_ERR_INVALID_ARG;
+  if (n > QZ_MAX_GROUP) return QZ_ERR_UNSUPPORTED;
+  qz_int4o_weight v[QZ_MAX_GROUP];
+  for (int m = 0; m < n; ++m) {
+    QZ_TRY(check_int4o_weight(&ws[m]));
+    if (ws[m].K != ws[0].K || ws[m].n_out != ws[0].n_out || ws[m].perm != ws[0].perm)
+      return QZ_ERR_INVALID_ARG;
+    QZ_TRY(check_vec(ys[m], 1, ws[m].N, 0));
+    v[m] = ws[m];
+    QZ_TRY(device_view_t(v[m].perm));
+    QZ_TRY(device_view_t(v[m].w_out));
+    QZ_TRY(device_view_t(v[m].q4));
+    QZ_TRY(device_view_t(v[m].scale));
+  }
+  QZ_TRY(check_vec(x, 1, ws[0].K, 0));
+  GemvParams p;
+  fill_int4o(p, v, n);
+  return mapped_common(true, p, x, ys, n, (cudaStream_t)s);
 }
 
 qz_status qz_gemv_int4_outlier_grouped(const qz_int4o_weight *ws, int n, const qz_half *x,

@@ -63,6 +63,10 @@ int overlap_enabled();
 size_t gemv_smem_bytes(bool int4, int B, const GemvParams &p);
 // Enqueue the CUDA-core GEMV for batch 1 <= B <= 4.
 qz_status launch_gemv(bool int4, int B, const GemvParams &p, cudaStream_t s);
+// Batch-1 CUDA-core GEMV reading the weights in place, where they may lie in
+// mapped pinned host memory (zero-copy); its shared-memory bytes.
+qz_status launch_gemv_mapped(bool int4, const GemvParams &p, cudaStream_t s);
+size_t gemv_mapped_smem_bytes(bool int4, const GemvParams &p);
 
 // Warp-MMA GEMV (mma.sync on dequantized codes) for batch 1..kMvMaxBatch.
 constexpr int kMvMaxBatch = 8;

@@ -358,16 +358,19 @@ class PagedStack:
 # ------------------------------------------------------------ tiering ---
 class TieredStack:
     """Tier A + tier B on one GPU ("NTransformer" summary, 3-Tier Adaptive
-    Caching: VRAM-resident layers, then layers streamed from pinned RAM by
-    host-to-device DMA): the first `resident` layers live in device memory,
-    the others stay in pinned host memory and stream through the pager into
-    two device slots.  Host layers: `distinct` packed blobs reused cyclically,
-    as in PagedStack.  Both tiers run on the pager's compute stream.
+    Caching: VRAM-resident layers, then layers kept in pinned RAM): the first
+    `resident` layers live in device memory, the others stay in pinned host
+    memory and are either streamed through the pager into two device slots
+    (mode "paged": host-to-device DMA) or read in place by the zero-copy GEMV
+    (mode "zero_copy": the ELG page's pinned pool reached by zero-copy DMA).
+    Host layers: `distinct` packed blobs reused cyclically, as in PagedStack.
+    Both tiers run on the pager's compute stream.
     """
 
     def __init__(self, wl: S.Workload, resident: int, n_layers: int | None = None,
-                 distinct: int = 4, device="cuda"):
-        self.wl = wl
+                 distinct: int = 4, device="cuda", mode: str = "paged"):
+        assert mode in ("paged", "zero_copy")
+        self.wl, self.mode = wl, mode
         self.n_layers = wl.layers if n_layers is None else n_layers
         self.resident = max(0, min(resident, self.n_layers))
         self.device = torch.device(device)
@@ -377,6 +380,9 @@ class TieredStack:
         # the resident layers were quantized on the current stream; the step
         # runs on the pager's compute stream, which must not start before them
         self.host.compute_stream.wait_stream(torch.cuda.current_stream(self.device))
+        # zero-copy: the matrices as views into the pinned host blobs
+        self._host_views = ([self.host._mats_in(b) for b in self.host.blobs]
+                            if mode == "zero_copy" else None)
         self.weight_bytes_per_layer = self.host.weight_bytes_per_layer
         self.io_bytes_per_layer = self.host.io_bytes_per_layer
 
@@ -388,12 +394,26 @@ class TieredStack:
         """The stream a step runs on (the pager's compute stream)."""
         return self.host.compute_stream
 
+    def _run_host_layer_in_place(self, j: int, stream):
+        """Layer j of tier B (0-based within the tier), read in place."""
+        hl = j % self.host.distinct
+        mats = self._host_views[hl]
+        xs, ys = self.host.x[hl], self.host.y[hl]
+        for g, names in enumerate(S.GROUPS):
+            api.gemv_mapped([mats[m] for m in names], xs[g][0], [y[0] for y in ys[g]],
+                            stream=stream)
+
     def run_step(self):
         s = self.stream
         for l in range(self.resident):
             for g in range(len(S.GROUPS)):
                 self.dev.run_group(l, g, s)
-        if self.n_layers > self.resident:
+        if self.n_layers <= self.resident:
+            return
+        if self.mode == "zero_copy":
+            for j in range(self.n_layers - self.resident):
+                self._run_host_layer_in_place(j, s)
+        else:
             self.host.run_step()
 
     def close(self):
