@@ -639,6 +639,8 @@ def measure(wl_name: str, batch: int, steps: int, warmup: int, dist_ctx=None,
     out = {
         "workload": wl_name, "batch": batch, "layers": st.n_layers,
         "bytes_per_step": st.bytes_per_step(),
+        "padded_bytes_per_step": st.n_layers * (st.padded_weight_bytes_per_layer() +
+                                                st.io_bytes_per_layer()),
         "weight_bytes_per_layer": st.weight_bytes_per_layer(),
         "ms_per_step": ms, "us_per_layer": ms * 1e3 / st.n_layers,
         "gbs": st.bytes_per_step() / (ms * 1e-3) / 1e9,
@@ -1118,6 +1120,8 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_layer": round(ms_all * 1e3 / r["layers"], 3),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
+        # the same step counted in bytes as stored (rows padded to 16 bytes)
+        "padded_gbs": round(job_gbs(world, r["padded_bytes_per_step"], ms_all), 2),
         "peak_source": f"{peak:.0f} GB/s of {peak_src}",
         "roofline": roofline,
         "cpu_baseline": cpu,

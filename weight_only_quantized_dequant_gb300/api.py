@@ -77,6 +77,10 @@ class Int8Matrix:
         """Algorithmic bytes: N*K codes + one fp32 scale."""
         return self.N * self.K + 4
 
+    def padded_bytes(self) -> int:
+        """Bytes as stored: N*ldq codes (rows padded to 16 bytes) + the scale."""
+        return self.N * self.ldq + 4
+
 
 def quantize_int8(W: torch.Tensor, stream=None) -> Int8Matrix:
     """scale = max|W|/127, q = round(W/scale) (half-to-even), on the GPU."""

@@ -170,6 +170,10 @@ class LayerStack:
         """Algorithmic bytes of one layer's weights (codes, outliers, scales)."""
         return sum(w.nbytes() for w in self.layers[0].mats.values())
 
+    def padded_weight_bytes_per_layer(self) -> int:
+        """Bytes of one layer's weights as stored (rows padded to 16 bytes)."""
+        return sum(w.padded_bytes() for w in self.layers[0].mats.values())
+
     def io_bytes_per_layer(self) -> int:
         """Input and output vectors (+ the permutation tables for INT4)."""
         B, wl = self.batch, self.wl
