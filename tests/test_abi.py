@@ -201,6 +201,30 @@ def test_sequence_validation(lib):
     assert lib.qz_gemv_int4_outlier_sequence(w4, two, 1, xs, ys, P, None) == INVAL
 
 
+def test_mapped_validation(lib):
+    """The zero-copy entry points check sizes, alignment and the shared
+    permutation like the grouped calls, then refuse any weight buffer the
+    runtime cannot name a device address for (here: memory no CUDA context
+    knows), all before anything is launched."""
+    M8, M4 = lib.qz_gemv_int8_grouped_mapped, lib.qz_gemv_int4_outlier_grouped_mapped
+    ws = (_lib.Int8Weight * 5)(*[_w8() for _ in range(5)])
+    ys = (ctypes.c_void_p * 5)(*[P] * 5)
+    assert M8(ws, 5, P, ys, None) == UNSUP
+    assert M8(ws, 0, P, ys, None) == INVAL
+    bad = (_lib.Int8Weight * 2)(_w8(K=32), _w8(K=48, ldq=48))
+    assert M8(bad, 2, P, ys, None) == INVAL
+    mis = (_lib.Int8Weight * 1)(_w8(ldq=40))
+    assert M8(mis, 1, P, ys, None) == ALIGN
+    unknown = (_lib.Int8Weight * 2)(_w8(), _w8())
+    assert M8(unknown, 2, P, ys, None) == INVAL               # no device address for P
+    w4 = (_lib.Int4oWeight * 2)(_w4(), _w4(perm=P + 16))
+    assert M4(w4, 2, P, ys, None) == INVAL                   # perm must be shared
+    w4 = (_lib.Int4oWeight * 1)(_w4(q4=PU))
+    assert M4(w4, 1, P, ys, None) == ALIGN
+    w4 = (_lib.Int4oWeight * 2)(_w4(), _w4())
+    assert M4(w4, 2, P, ys, None) == INVAL                   # no device address for P
+
+
 def _w4(N=8, K=64, n_out=1, perm=P, w_out=P, q4=P, scale=P, ld_out=None, ld_q4=None):
     lo, lq = O.int4o_layout(K, min(n_out, K))
     return _lib.Int4oWeight(N, K, n_out, lo if ld_out is None else ld_out,
