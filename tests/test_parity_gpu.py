@@ -539,6 +539,42 @@ def test_full_70b_gate_up_grouped_int4_sampled():
         assert_close(y[rows], y_ref[0], a_ref[0], f"70b gate+up sampled m={i}")
 
 
+@pytest.mark.parametrize("fmt,Ns,K,n_out", [("int4o", [7300, 7301], 3000, 31),
+                                             ("int4o", [14600], 8200, 83),
+                                             ("int8", [14593], 1000, 0),
+                                             ("int8", [7000, 7601], 4100, 0)])
+def test_batch1_many_rows_against_oracle(fmt, Ns, K, n_out):
+    """Batch-1 grouped launches with many rows per CTA (97): ragged row
+    pairs and ring stages, rows not a multiple of a ring stage, an odd
+    outlier count, two matrices in one launch; every output against the
+    oracle."""
+    Ws = [S.weight(n, K, 9950 + i + K, device=DEV) for i, n in enumerate(Ns)]
+    x = S.activation(1, K, 9960 + K, device=DEV)
+    if fmt == "int8":
+        ws = [qz().quantize_int8(W) for W in Ws]
+        ys = qz().gemv_int8_grouped(ws, x[0])
+    else:
+        prof = S.x_profile(K, n_out, 9970 + K, device=DEV)
+        colsum = torch.zeros((K,), dtype=torch.int64, device=DEV)
+        for W in Ws:
+            qz().saliency_accumulate(W, colsum)
+        perm = qz().select_outliers(colsum, prof, n_out)
+        ws = [qz().quantize_int4_outlier(W, perm, n_out) for W in Ws]
+        ys = qz().gemv_int4_outlier_grouped(ws, x[0])
+    assert qz().device_error() == 0
+    xn = x.cpu().numpy()
+    for i, (W, y) in enumerate(zip(Ws, ys)):
+        Wn = W.cpu().numpy()
+        if fmt == "int8":
+            q_ref, s_ref = O.int8_quantize(Wn)
+            y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, xn)
+        else:
+            pn = perm.cpu().numpy()
+            wo, q4, sc = O.int4o_quantize(Wn, pn, n_out)
+            y_ref, a_ref = O.int4o_product_ref(wo, q4, sc, pn, n_out, K, xn)
+        assert_close(y, y_ref[0], a_ref[0], f"many rows {fmt} K={K} m={i}")
+
+
 # ----------------------------------------------------------------- pager ---
 def test_pager_streams_layers_and_reports_injected_failure():
     import weight_only_quantized_dequant_gb300 as m
