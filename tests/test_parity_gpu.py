@@ -78,7 +78,7 @@ def test_int8_quantize_bit_exact(N, K):
     assert not q[:, K:].any()
 
 
-BATCHES = [1, 2, 3, 4, 5, 8, 16, 33, 64]
+BATCHES = [1, 2, 3, 4, 5, 8, 16, 24, 33, 64]
 
 
 @pytest.mark.parametrize("N,K", INT8_SHAPES)

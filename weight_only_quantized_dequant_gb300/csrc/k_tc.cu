@@ -49,10 +49,12 @@ constexpr int kMaxAStages = 6;  // A stages in tensor memory (64 columns each)
 constexpr uint32_t kTmemCols = 512;    // 2 x (outlier, background) accumulators, A above
 constexpr int kProducers = 256;  // 8 warps, two threads per weight row
 constexpr int kEpiWarp = kProducers / 32;     // warps 8-11 drain the accumulators
-constexpr int kMmaWarp = kEpiWarp + 4;        // warp 12 issues the MMAs
+constexpr int kMmaWarp = kEpiWarp + 4;        // warp 12 issues the MMAs of even units
 constexpr int kCodeWarp = kMmaWarp + 1;       // warp 13 fills the code ring
 constexpr int kLoadWarp = kMmaWarp + 2;       // warp 14 fills the activation ring
-constexpr int kThreadsTc = kProducers + 224;
+constexpr int kMma2Warp = kMmaWarp + 3;       // warp 15 issues the MMAs of odd units
+constexpr int kMaxIssuers = 2;
+constexpr int kThreadsTc = kProducers + 256;
 constexpr int kEpiThreads = 128;
 constexpr int kMaxBStages = 8;                // activation ring depth (smem permitting)
 constexpr size_t kBRingBytes = 80 * 1024;     // shared memory given to that ring
@@ -84,7 +86,9 @@ struct TcParams {
   int Np;               // MMA N: B rounded up to 16
   int nbs;              // stages of the activation ring
   int nsa;              // A stages in tensor memory
-  uint32_t a_base;      // first TMEM column of the A stages (4 Np)
+  int nmma;             // MMA-issuing threads (1 or 2), each with its own accumulators
+  int nbuf;             // accumulator buffers (1 or 2) per issuer
+  uint32_t a_base;      // first TMEM column of the A stages (nbuf * nmma * 2 Np)
   const uint8_t *ws;    // gathered activations, one canonical B tile per K tile (or null)
   float *part;          // partials of cut tiles: [kMaxCtas][2][4 quarters][Np/4][32][4] fp32
   unsigned *cnt;        // arrivals per cut tile and TMEM lane quarter, by its first CTA
@@ -232,6 +236,40 @@ __device__ __forceinline__ int slot_elem(int c) {
   return (c & ~7) + ((s & 1) ? 4 + (s >> 1) : (s >> 1));
 }
 
+// Position in a ring of n slots that advances by one per work unit: the slot
+// and the parity of its current round (slot = q mod n, parity = (q / n) & 1),
+// kept without run-time divisions on the serial path of the issuing threads.
+struct RingPos {
+  int slot = 0;
+  uint32_t parity = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++slot == n) {
+      slot = 0;
+      parity ^= 1u;
+    }
+  }
+};
+
+// (tile, K tile) of a work unit, advanced by one unit at a time.
+struct UnitPos {
+  int t, kt;
+  __device__ __forceinline__ UnitPos(int u, int KT) : t(u / KT), kt(u - (u / KT) * KT) {}
+  __device__ __forceinline__ void next(int KT) {
+    if (++kt == KT) {
+      kt = 0;
+      ++t;
+    }
+  }
+};
+
+// Whether the issuer w (of W in {1, 2}) owns a unit among K tiles [a, b) of
+// tile t: units alternate between issuers by their position in the CTA's range.
+__device__ __forceinline__ bool issuer_has(int W, int w, int t, int a, int b, int KT, int u_begin) {
+  if (b <= a) return false;
+  if (W == 1 || b - a >= 2) return true;
+  return ((t * KT + a - u_begin) & 1) == w;
+}
+
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
   return *reinterpret_cast<uint32_t *>(&r);
@@ -308,7 +346,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 
   if (tid == 0) {
     for (int s = 0; s < kMaxAStages; ++s) {
-      mbar_init(smem_u32(&full[s]), kProducers);
+      mbar_init(smem_u32(&full[s]), kProducers / 32);  // one arrival per converter warp
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int s = 0; s < kMaxBStages; ++s) {
@@ -317,10 +355,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     }
     for (int s = 0; s < kMaxRaw; ++s) {
       mbar_init(smem_u32(&rfull[s]), 1);
-      mbar_init(smem_u32(&rempty[s]), kProducers);
+      mbar_init(smem_u32(&rempty[s]), kProducers / 32);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&dfull[s]), 1);
+      mbar_init(smem_u32(&dfull[s]), (uint32_t)tp.nmma);
       mbar_init(smem_u32(&dempty[s]), kEpiThreads);
     }
     for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&fxbar[s]), 1);
@@ -338,8 +376,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: accumulator buffer d at [2 d Np, 2 d Np + 2 Np) (outlier
-  // then background), A stages from tp.a_base = 4 Np.
+  // TMEM columns: issuer w's accumulators in buffer d at
+  // [2 Np (d W + w), 2 Np (d W + w) + 2 Np) (outlier then background), A
+  // stages from tp.a_base = 2 Np W nbuf.
+  const int W = tp.nmma, NBUF = tp.nbuf;
 
   if (warp < kEpiWarp) {
     // ------------------------------------------------------ producers ----
@@ -357,15 +397,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     int i = 0;       // code tiles taken from the raw ring so far
     int t_cur = -1;  // tile of the previous unit
     TileInfo ti = {0, 0, 0};
+    RingPos ap;                    // A stage of the unit
+    UnitPos up(u_begin, KT);       // (tile, K tile) of the unit
     for (int u = u_begin; u < u_end; ++u) {
       const int q = u - u_begin;  // position in this CTA's ring sequence
-      const int s = q % NA;
+      const int s = ap.slot;
+      const uint32_t aph = ap.parity;
+      const int t = up.t, kt = up.kt;
+      ap.next(NA);
+      up.next(KT);
       if (q >= NA) {
-        const bool ok = mbar_wait(smem_u32(&empty[s]), ((q / NA) - 1) & 1, abort_flag);
+        const bool ok = mbar_wait(smem_u32(&empty[s]), aph ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
         fence_after();  // the MMAs that read this A stage are complete
       }
-      const int t = u / KT, kt = u - t * KT;
       if (t != t_cur) {
         ti = tile_info(tp, t);
         t_cur = t;
@@ -408,7 +453,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
           asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(qv[c].x), "=r"(qv[c].y), "=r"(qv[c].z), "=r"(qv[c].w)
                        : "r"(rsrc + 16 * c));
-        mbar_arrive(smem_u32(&rempty[i % DR]));  // the codes are in registers
+        __syncwarp();  // the warp's codes are in registers
+        if (lane == 0) mbar_arrive(smem_u32(&rempty[i % DR]));
         ++i;
         const uint32_t words[8] = {qv[0].x, qv[0].y, qv[0].z, qv[0].w,
                                    qv[1].x, qv[1].y, qv[1].z, qv[1].w};
@@ -434,7 +480,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
           asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(vv[c].x), "=r"(vv[c].y), "=r"(vv[c].z), "=r"(vv[c].w)
                        : "r"(rsrc + 16 * c));
-        mbar_arrive(smem_u32(&rempty[i % DR]));  // the codes are in registers
+        __syncwarp();  // the warp's codes are in registers
+        if (lane == 0) mbar_arrive(smem_u32(&rempty[i % DR]));
         ++i;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -455,7 +502,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       tmem_st32(tmem + lane_base + tp.a_base + (uint32_t)s * (kKT / 2) + (uint32_t)h * 32, o);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       fence_before();
-      mbar_arrive(smem_u32(&full[s]));
+      __syncwarp();  // every lane's tensor-memory stores are complete
+      if (lane == 0) mbar_arrive(smem_u32(&full[s]));
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------- epilogue ----
@@ -509,26 +557,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         // running sums into slot 0; element (n, lane) of a block sits at
         // float ((n / 4) * 32 + lane) * 4 + n % 4
         float4 *sv = reinterpret_cast<float4 *>(stg) + lane;
-        for (int n0 = 0; n0 < tp.B; n0 += 16) {
-          float4 acc[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            acc[q] = have ? sv[(n0 / 4 + q) * 32] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int n4 = 0; n4 < tp.B; n4 += 4) {  // one float4 of columns at a time, partials in CTA order
+          float4 acc = have ? sv[(n4 / 4) * 32] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           for (int i = 0; i < nb; ++i) {
-            const float4 *src = sv + (size_t)(s0 + i) * (blk / 16) + (n0 / 4) * 32;
-            float4 v[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = src[q * 32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              acc[q].x += v[q].x;
-              acc[q].y += v[q].y;
-              acc[q].z += v[q].z;
-              acc[q].w += v[q].w;
-            }
+            const float4 v = sv[(size_t)(s0 + i) * (blk / 16) + (n4 / 4) * 32];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
           }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) sv[(n0 / 4 + q) * 32] = acc[q];
+          sv[(n4 / 4) * 32] = acc;
         }
         have = true;
         k += nb;
@@ -561,21 +599,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       const TileInfo ti = tile_info(tp, t);
       const int64_t grow = ti.row0 + r;
       const bool live = grow < ti.nrows;
-      const bool has_out = INT4 && k0 < tp.ko;
-      const bool has_bg = k1 > tp.ko;
+      const int kso = k1 < tp.ko ? k1 : tp.ko;  // outlier K tiles of the segment: [k0, kso)
+      const int ksb = k0 > tp.ko ? k0 : tp.ko;  // background K tiles: [ksb, k1)
+      bool has_out[kMaxIssuers], has_bg[kMaxIssuers];
+#pragma unroll
+      for (int w = 0; w < kMaxIssuers; ++w) {
+        has_out[w] = INT4 && w < W && issuer_has(W, w, t, k0, kso, KT, u_begin);
+        has_bg[w] = w < W && issuer_has(W, w, t, ksb, k1, KT, u_begin);
+      }
       const bool cut = !(k0 == 0 && k1 == KT);
       float s_i = 1.0f;
       if (live) s_i = INT4 ? __ldg(p.scale[ti.m] + grow) : __ldg(p.scale[ti.m]);
       __half *yrow = p.y[ti.m] + grow;
       const int64_t ldy = p.ldy[ti.m];
-      const int db = j & 1;
-      const bool ok = mbar_wait(smem_u32(&dfull[db]), (j >> 1) & 1, abort_flag);
+      const int db = NBUF == 2 ? (j & 1) : 0;
+      const bool ok = mbar_wait(smem_u32(&dfull[db]), (NBUF == 2 ? (j >> 1) : j) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         aborted = true;
         break;
       }
       fence_after();
-      const uint32_t dcol = tmem + lane_base + (uint32_t)(db * 2 * Np);
+      const uint32_t dcol = tmem + lane_base + (uint32_t)(db * W * 2 * Np);
       // partial of a cut tile: float4 (n / 4, lane) of its (slot, quarter) block
       float4 *mine = nullptr;
       float *mine_c = reinterpret_cast<float *>(b_st) + r;  // kCluster: [n][kM] in its own rings
@@ -584,15 +628,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                    tp.part + (size_t)((cta * 2 + part_slot(tp, cta, t)) * 4 + qtr) * Np * 32) +
                lane;
       for (int c0 = 0; c0 < Np; c0 += 16) {
-        float vb[16], vo[16], y[16];
-        tmem_ld16(dcol + (uint32_t)Np + c0, vb);
-        if (INT4) tmem_ld16(dcol + c0, vo);
+        float y[16], o[16];  // y: background sum, then the result
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const float bg = has_bg ? vb[jj] : 0.0f;
-          const float o = has_out ? vo[jj] : 0.0f;
-          y[jj] = fmaf(s_i, bg, o);  // this CTA's units of the tile
+        for (int jj = 0; jj < 16; ++jj) y[jj] = o[jj] = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kMaxIssuers; ++w) {  // issuers' partials, in issuer order
+          float v[16];
+          const uint32_t col = dcol + (uint32_t)(w * 2 * Np);
+          if (has_bg[w]) {
+            tmem_ld16(col + (uint32_t)Np + c0, v);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) y[jj] += v[jj];
+          }
+          if (has_out[w]) {
+            tmem_ld16(col + c0, v);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) o[jj] += v[jj];
+          }
         }
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) y[jj] = fmaf(s_i, y[jj], o[jj]);  // this CTA's units of the tile
         if (!cut) {
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
@@ -632,41 +687,64 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       }
     }
     if (def_t >= 0 && !aborted) finish_tile(def_t, def_lo, def_hi);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
+  } else if (warp == kMmaWarp || warp == kMma2Warp) {
+    // ---------------------------------------------------- MMA issuers ---
+    // One thread per issuing warp; issuer w takes the units at positions
+    // q = w (mod W) of the CTA's range into its own accumulators, so that the
+    // serial issue cost of each tcgen05.mma is paid by W threads in parallel.
+    // Every issuer commits once per segment to the accumulator-full barrier
+    // (W arrivals), after the drain of that buffer's previous segment.
+    const int w = warp == kMmaWarp ? 0 : 1;
+    if (lane == 0 && w < W) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
-      // ---------------------------------------------------- MMA issuer ---
       const uint32_t idesc = idesc_f16(kM, Np);
-      int j = -1, k0 = 0;
+      int j = -1;
       uint32_t dcol = 0;
+      int db = 0;
+      bool seen_out = false, seen_bg = false;  // this issuer's first unit of each kind in the segment
+      RingPos ap, bp;
+      UnitPos up(u_begin, KT);
       for (int u = u_begin; u < u_end; ++u) {
         const int q = u - u_begin;
-        const int t = u / KT, kt = u - t * KT;
+        const int kt = up.kt;
+        const int s = ap.slot, sb = bp.slot;
+        const uint32_t aph = ap.parity, bph = bp.parity;
+        up.next(KT);
+        ap.next(NA);
+        bp.next(NB);
         if (q == 0 || kt == 0) {  // a new segment: next accumulator buffer
           ++j;
-          k0 = kt;
-          dcol = (uint32_t)((j & 1) * 2 * Np);
-          if (j >= 2) {
-            if (!mbar_wait(smem_u32(&dempty[j & 1]), ((j >> 1) - 1) & 1, abort_flag)) break;
+          db = NBUF == 2 ? (j & 1) : 0;
+          dcol = (uint32_t)((db * W + w) * 2 * Np);
+          seen_out = seen_bg = false;
+          if (j >= NBUF) {
+            if (!mbar_wait(smem_u32(&dempty[db]), ((NBUF == 2 ? (j >> 1) : j) - 1) & 1, abort_flag))
+              break;
             fence_after();
           }
         }
-        const int s = q % NA, sb = q % NB;
-        if (!mbar_wait(smem_u32(&full[s]), (q / NA) & 1, abort_flag)) break;
-        if (!mbar_wait(smem_u32(&bfull[sb]), (q / NB) & 1, abort_flag)) break;
-        fence_after();
-        const bool outl = kt < tp.ko;
-        const uint32_t a0 = tmem + tp.a_base + (uint32_t)s * (kKT / 2);
-        const uint32_t b0 = smem_u32(b_st + sb * bBytes);
-        const uint32_t d = tmem + dcol + (outl ? 0u : (uint32_t)Np);
-        const bool first = outl ? kt == k0 : kt == (k0 > tp.ko ? k0 : tp.ko);
+        if ((q & (W - 1)) == w) {
+          if (!mbar_wait(smem_u32(&full[s]), aph, abort_flag)) break;
+          if (!mbar_wait(smem_u32(&bfull[sb]), bph, abort_flag)) break;
+          fence_after();
+          const bool outl = kt < tp.ko;
+          const uint32_t a0 = tmem + tp.a_base + (uint32_t)s * (kKT / 2);
+          const uint32_t b0 = smem_u32(b_st + sb * bBytes);
+          const uint32_t d = tmem + dcol + (outl ? 0u : (uint32_t)Np);
+          const bool first = outl ? !seen_out : !seen_bg;
+          if (outl)
+            seen_out = true;
+          else
+            seen_bg = true;
+          const uint64_t bd = sdesc(b0);
 #pragma unroll
-        for (int k16 = 0; k16 < kKT / 16; ++k16)
-          mma_f16_ta(d, a0 + 8 * k16, sdesc(b0 + k16 * 2 * kLBO), idesc,
-                     (first && k16 == 0) ? 0u : 1u);
-        mma_commit(smem_u32(&empty[s]));
-        mma_commit(smem_u32(&bempty[sb]));
-        if (u + 1 == u_end || kt + 1 == KT) mma_commit(smem_u32(&dfull[j & 1]));
+          for (int k16 = 0; k16 < kKT / 16; ++k16)  // (the descriptor's address field is in 16 B)
+            mma_f16_ta(d, a0 + 8 * k16, bd + (uint64_t)(k16 * 2 * kLBO / 16), idesc,
+                       (first && k16 == 0) ? 0u : 1u);
+          mma_commit(smem_u32(&empty[s]));
+          mma_commit(smem_u32(&bempty[sb]));
+        }
+        if (u + 1 == u_end || kt + 1 == KT) mma_commit(smem_u32(&dfull[db]));
       }
     }
   } else if (warp == kCodeWarp) {
@@ -677,8 +755,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     if (lane == 0) {
       constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
       int i = 0;
+      UnitPos up(u_begin, KT);
       for (int u = u_begin; u < u_end; ++u) {
-        const int t = u / KT, kt = u - t * KT;
+        const int t = up.t, kt = up.kt;
+        up.next(KT);
         if (kt < tp.ko) continue;  // outlier units read fp16 rows directly
         const uint32_t bar = smem_u32(&rfull[i % DR]);
         if (i >= DR) {
@@ -710,11 +790,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     // arrives by one bulk copy; without one this warp gathers it.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int q = 0;
+    RingPos bp;
+    UnitPos up(u_begin, KT);
     for (int u = u_begin; u < u_end; ++u, ++q) {
-      const int kt = u % KT;
-      const int sb = q % NB;
+      const int kt = up.kt;
+      const int sb = bp.slot;
+      const uint32_t bph = bp.parity;
+      up.next(KT);
+      bp.next(NB);
       if (q >= NB) {
-        const bool ok = mbar_wait(smem_u32(&bempty[sb]), ((q / NB) - 1) & 1, abort_flag);
+        const bool ok = mbar_wait(smem_u32(&bempty[sb]), bph ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       uint8_t *Bt = b_st + sb * bBytes;
@@ -983,7 +1068,20 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   tp.B = B;
   tp.Np = (B + 15) / 16 * 16;
   tp.nbs = tc_b_stages(tp.Np);
-  tp.a_base = (uint32_t)(4 * tp.Np);
+  // Two MMA issuers with double-buffered accumulators where tensor memory
+  // leaves at least 4 A stages, else single-buffered, else one issuer.
+  tp.nmma = 1;
+  tp.nbuf = 2;
+  for (int cand = 0; cand < 3; ++cand) {
+    const int W = cand < 2 ? 2 : 1, nb = cand == 1 ? 1 : 2;
+    const int64_t a_base = (int64_t)nb * W * 2 * tp.Np;
+    if ((kTmemCols - a_base) / (kKT / 2) >= 4 || cand == 2) {
+      tp.nmma = W;
+      tp.nbuf = nb;
+      break;
+    }
+  }
+  tp.a_base = (uint32_t)(tp.nbuf * tp.nmma * 2 * tp.Np);
   tp.nsa = (int)((kTmemCols - tp.a_base) / (kKT / 2));
   if (tp.nsa > kMaxAStages) tp.nsa = kMaxAStages;
   tp.ko = int4 ? (g.n_out + kKT - 1) / kKT : 0;
