@@ -7,15 +7,21 @@
 //
 //  * A (weights) is the MMA's M side, in tiles of 128 output rows.  Producer
 //    warps turn packed codes into exact fp16 integers in registers (INT4: one
-//    LOP3 on the 0x6400 exponent per nibble pair; INT8: one PRMT per byte
-//    pair) and store them into tensor memory, where the MMA reads A.  No fp16
-//    weight tensor exists in HBM.
+//    LOP3 onto the 0x6400 exponent and one packed subtract or fused
+//    multiply-add per nibble pair, no shifts for half of the pairs; INT8: one
+//    PRMT per byte pair) and store them into tensor memory, where the MMA
+//    reads A.  No fp16 weight tensor exists in HBM.
 //  * B (activations, N = batch rounded up to 16) is gathered through the
 //    permutation once per call into the canonical K-major layout, in the k
 //    order the nibble conversion produces, and streamed into shared memory.
-//  * One thread issues tcgen05.mma (kind::f16, fp32 accumulate) into two
-//    TMEM accumulators: outlier channels and INT4 background, so that the
-//    per-row scale multiplies the background only: y = D_out + s_i * D_bg.
+//  * tcgen05.mma (kind::f16, fp32 accumulate) into two TMEM accumulators:
+//    outlier channels and INT4 background, so that the per-row scale
+//    multiplies the background only: y = D_out + s_i * D_bg.  Issuing one
+//    MMA costs its thread about 60 SM clocks whatever N is (measured: one
+//    thread, 2048 weights per instruction), so two threads in two warps issue
+//    alternate work units into accumulators of their own, and the epilogue
+//    adds the two in issuer order.  Per-unit ring positions are counters,
+//    not divisions: the issuing threads run serial code.
 //  * Schedules of the (tile, K tile) work units of all matrices of the call,
 //    chosen per call by a cost model: persistent stream-K (one contiguous
 //    range per CTA, one CTA per SM, so every SM gets the same number of MMAs
@@ -24,9 +30,10 @@
 //    a cluster of S CTAs per tile that split its K tiles and add their
 //    partials in rank order through distributed shared memory (few tiles),
 //    or persistent whole tiles (no workspace).  All are deterministic.
-//  * The accumulators are double-buffered, so the epilogue warps drain one
-//    tile while the MMAs of the next run.  Every wait is bounded in time and
-//    reports a timeout through a device flag.
+//  * Up to batch 32 the accumulators are double-buffered, so the epilogue
+//    warps drain one tile while the MMAs of the next run (above that tensor
+//    memory holds one buffer per issuer beside four A stages).  Every wait is
+//    bounded in time and reports a timeout through a device flag.
 #include <cuda.h>
 
 #include <cstring>
@@ -270,6 +277,13 @@ __device__ __forceinline__ bool issuer_has(int W, int w, int t, int a, int b, in
   return ((t * KT + a - u_begin) & 1) == w;
 }
 
+// a * b + c on fp16 pairs (one rounding).
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b),
+                      *reinterpret_cast<__half2 *>(&c));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
   return *reinterpret_cast<uint32_t *>(&r);
@@ -344,38 +358,82 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   const int cta = (int)blockIdx.x;
   const int u_begin = range_start(tp, cta), u_end = range_start(tp, cta + 1);
 
-  if (tid == 0) {
-    for (int s = 0; s < kMaxAStages; ++s) {
-      mbar_init(smem_u32(&full[s]), kProducers / 32);  // one arrival per converter warp
-      mbar_init(smem_u32(&empty[s]), 1);
+  // Code loader state, carried from the prologue into its main loop: the
+  // loader sets up its own ring barriers, only arrives at the start-up
+  // barrier (named barrier 1) and issues the first ring of code copies while
+  // the other warps set up the rest and warp 0 allocates tensor memory.
+  constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
+  int cl_i = 0, cl_u = u_begin, cl_t = 0, cl_kt = 0;
+  auto issue_codes = [&](int i, int t, int kt) {
+    const uint32_t bar = smem_u32(&rfull[i % DR]);
+    const TileInfo ti = tile_info(tp, t);
+    const uint64_t cmap = reinterpret_cast<uint64_t>(&tp.codes_map[ti.m]);
+    const int x = INT4 ? (kt - tp.ko) * RB : kt * RB;
+    asm volatile(
+        "{\n\t.reg .b64 t;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
+        "r"((uint32_t)(kM * RB))
+        : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(raw) + (uint32_t)(i % DR) * (kM * RB)),
+        "l"(cmap), "r"(x), "r"((int)ti.row0), "r"(bar)
+        : "memory");
+  };
+  uint32_t tmem = 0;
+  if (warp == kCodeWarp) {
+    if (lane == 0) {
+      for (int s = 0; s < kMaxRaw; ++s) {
+        mbar_init(smem_u32(&rfull[s]), 1);
+        mbar_init(smem_u32(&rempty[s]), kProducers / 32);
+      }
+      *abort_flag = 0;  // (thread 0 writes the same; this warp may poll it first)
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int s = 0; s < kMaxBStages; ++s) {
-      mbar_init(smem_u32(&bfull[s]), 1);
-      mbar_init(smem_u32(&bempty[s]), 1);
+    __syncwarp();
+    asm volatile("bar.arrive 1, %0;" ::"n"(kThreadsTc) : "memory");
+    if (lane == 0) {
+      UnitPos up(u_begin, KT);
+      for (; cl_u < u_end && cl_i < DR; ++cl_u) {
+        const int t = up.t, kt = up.kt;
+        up.next(KT);
+        if (kt < tp.ko) continue;  // outlier units read fp16 rows directly
+        issue_codes(cl_i, t, kt);
+        ++cl_i;
+      }
+      cl_t = up.t;
+      cl_kt = up.kt;
     }
-    for (int s = 0; s < kMaxRaw; ++s) {
-      mbar_init(smem_u32(&rfull[s]), 1);
-      mbar_init(smem_u32(&rempty[s]), kProducers / 32);
+  } else {
+    if (tid == 0) {
+      for (int s = 0; s < kMaxAStages; ++s) {
+        mbar_init(smem_u32(&full[s]), kProducers / 32);  // one arrival per converter warp
+        mbar_init(smem_u32(&empty[s]), 1);
+      }
+      for (int s = 0; s < kMaxBStages; ++s) {
+        mbar_init(smem_u32(&bfull[s]), 1);
+        mbar_init(smem_u32(&bempty[s]), 1);
+      }
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(smem_u32(&dfull[s]), (uint32_t)tp.nmma);
+        mbar_init(smem_u32(&dempty[s]), kEpiThreads);
+      }
+      for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&fxbar[s]), 1);
+      *abort_flag = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&dfull[s]), (uint32_t)tp.nmma);
-      mbar_init(smem_u32(&dempty[s]), kEpiThreads);
+    if (warp == 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&fxbar[s]), 1);
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreadsTc) : "memory");
+    fence_after();
+    tmem = *tmem_slot;
   }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  fence_before();
-  __syncthreads();
-  fence_after();
-  const uint32_t tmem = *tmem_slot;
   // TMEM columns: issuer w's accumulators in buffer d at
   // [2 Np (d W + w), 2 Np (d W + w) + 2 Np) (outlier then background), A
   // stages from tp.a_base = 2 Np W nbuf.
@@ -390,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     // Background (INT4) or all (INT8) K tiles arrive as packed codes in the
     // raw ring (filled by the code loader warp); each thread converts its bytes.
-    constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB, HB = RawRing<INT4>::HB;
+    constexpr int HB = RawRing<INT4>::HB;
     const uint32_t raw_me = smem_u32(raw) + (uint32_t)r * RB + (uint32_t)h * HB;
     // Weights only: no wait for the preceding kernel (under programmatic
     // launch the caller guarantees that nothing in flight writes them).
@@ -462,13 +520,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
         for (int kg = 0; kg < 8; ++kg) {
           const uint32_t w = words[kg];
-          // 1024 + (q+8) - 1032 = q, exact in fp16; elements past kb hold
-          // zero nibbles (q = 0) from the row padding, rows past N zeros;
-          // slot order 0,4,1,5,2,6,3,7 (pairs (e0,e4), (e1,e5), ...)
-          o[4 * kg] = hsub2_u32(((w >> 0) & 0x000F000Fu) ^ bias, bias);
-          o[4 * kg + 1] = hsub2_u32(((w >> 4) & 0x000F000Fu) ^ bias, bias);
-          o[4 * kg + 2] = hsub2_u32(((w >> 8) & 0x000F000Fu) ^ bias, bias);
-          o[4 * kg + 3] = hsub2_u32(((w >> 12) & 0x000F000Fu) ^ bias, bias);
+          // Nibble pairs at bits 0-3 / 16-19: 1024 + (q+8) - 1032 = q.  Pairs
+          // at bits 4-7 / 20-23 are masked in place: 1024 + 16 (q+8), then
+          // x/16 - 72 = q in one fused step (every value a small integer,
+          // exact in fp16).  One shift by 8 serves the upper two pairs.
+          // Elements past kb hold zero nibbles (q = 0) from the row padding,
+          // rows past N zeros; slot order 0,4,1,5,2,6,3,7 (pairs (e0,e4),
+          // (e1,e5), ...).
+          const uint32_t w8 = w >> 8;
+          o[4 * kg] = hsub2_u32((w & 0x000F000Fu) ^ bias, bias);
+          o[4 * kg + 1] = hfma2_u32((w & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u, 0xD480D480u);
+          o[4 * kg + 2] = hsub2_u32((w8 & 0x000F000Fu) ^ bias, bias);
+          o[4 * kg + 3] = hfma2_u32((w8 & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u, 0xD480D480u);
         }
       } else {
         const bool ok = mbar_wait(smem_u32(&rfull[i % DR]), (i / DR) & 1, abort_flag);
@@ -753,31 +816,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     // CTA's units, one 2D tensor copy of kM rows x ROWB bytes each, DR ahead
     // of the converters.  The codes are static: no wait for earlier kernels.
     if (lane == 0) {
-      constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
-      int i = 0;
+      // (the first ring of copies went out in the prologue)
+      int i = cl_i;
       UnitPos up(u_begin, KT);
-      for (int u = u_begin; u < u_end; ++u) {
+      up.t = cl_t;
+      up.kt = cl_kt;
+      for (int u = cl_u; u < u_end; ++u) {
         const int t = up.t, kt = up.kt;
         up.next(KT);
         if (kt < tp.ko) continue;  // outlier units read fp16 rows directly
-        const uint32_t bar = smem_u32(&rfull[i % DR]);
         if (i >= DR) {
           if (!mbar_wait(smem_u32(&rempty[i % DR]), ((i / DR) - 1) & 1, abort_flag)) break;
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-        const TileInfo ti = tile_info(tp, t);
-        const uint64_t cmap = reinterpret_cast<uint64_t>(&tp.codes_map[ti.m]);
-        const int x = INT4 ? (kt - tp.ko) * RB : kt * RB;
-        asm volatile(
-            "{\n\t.reg .b64 t;\n\t"
-            "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(bar),
-            "r"((uint32_t)(kM * RB))
-            : "memory");
-        asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
-            "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(raw) + (uint32_t)(i % DR) * (kM * RB)),
-            "l"(cmap), "r"(x), "r"((int)ti.row0), "r"(bar)
-            : "memory");
+        issue_codes(i, t, kt);
         ++i;
       }
       if (*(volatile int *)abort_flag)  // let the copies in flight land
@@ -890,7 +942,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 
 // The B operand of every K tile, gathered through the permutation (INT4:
 // in the k order of the nibble conversion) into the canonical K-major layout,
-// one contiguous tile of Np x 64 fp16 per K tile.  One CTA per K tile.
+// one contiguous tile of Np x 64 fp16 per K tile.  One CTA per (K tile, 16
+// batch rows).
 template <bool INT4>
 __global__ void __launch_bounds__(256) tc_xprep_kernel(const __grid_constant__ TcParams tp,
                                                        uint8_t *ws) {
@@ -899,7 +952,7 @@ __global__ void __launch_bounds__(256) tc_xprep_kernel(const __grid_constant__ T
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int kt = blockIdx.x;
   // the arrival counters of the cut tiles start every call at zero
-  if (kt == 0 && tp.cnt)
+  if (kt == 0 && blockIdx.y == 0 && tp.cnt)
     for (int i = threadIdx.x; i < 4 * tp.G; i += blockDim.x) tp.cnt[i] = 0u;
   const int bBytes = tp.Np * kKT * 2;
   uint8_t *tile = ws + (size_t)kt * bBytes;
@@ -907,8 +960,9 @@ __global__ void __launch_bounds__(256) tc_xprep_kernel(const __grid_constant__ T
   // Eight elements per thread and step, all eight loads issued before the
   // one 16-byte store: the compiler cannot prove that the workspace does not
   // alias the inputs, so loads and stores mixed in one loop stay in order.
-  const int total = tp.Np * kKT;
-  for (int base = threadIdx.x * 8; base < total; base += 256 * 8) {
+  // this CTA's batch rows: [16 y, 16 y + 16)
+  const int total = (blockIdx.y + 1) * 16 * kKT;
+  for (int base = blockIdx.y * 16 * kKT + threadIdx.x * 8; base < total; base += 256 * 8) {
     __half v[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -1212,7 +1266,7 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   cfg.numAttrs = na;
   if (tp.ws) {  // gather the activations once (and clear the counters), then the GEMM
     cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3((unsigned)tp.KT);
+    pc.gridDim = dim3((unsigned)tp.KT, (unsigned)(tp.Np / 16));
     pc.blockDim = dim3(256);
     pc.stream = s;
     pc.attrs = attr;
