@@ -99,8 +99,6 @@ struct TcParams {
   const uint8_t *ws;    // gathered activations, one canonical B tile per K tile (or null)
   float *part;          // partials of cut tiles: [kMaxCtas][2][4 quarters][Np/4][32][4] fp32
   unsigned *cnt;        // arrivals per cut tile and TMEM lane quarter, by its first CTA
-  int fx_cap;           // partials of one lane quarter the reduction stages at once (>= 2)
-  uint32_t fx_bytes;    // shared-memory staging bytes per lane quarter
   int ko;               // K tiles of the outlier block
   int kbt;              // K tiles of the background block
   int KT;               // K tiles per tile: ko + kbt
@@ -162,6 +160,16 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
       "{\n\t.reg .b64 st;\n\t"
       "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
       : "memory");
+}
+
+// 16 bytes from global memory through L2 only (not L1).
+__device__ __forceinline__ float4 ld_cg_f4(const float4 *p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
 }
 
 // Canonical K-major, no-swizzle shared-memory matrix descriptor.
@@ -341,8 +349,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int bBytes = tp.Np * kKT * 2;
   const int NB = tp.nbs, NA = tp.nsa, KT = tp.KT, Np = tp.Np;
-  // [barriers | activation ring | raw-code ring | ...]; once a CTA's last
-  // MMA is done, everything past the barriers stages the cut-tile reduction
+  // [barriers | activation ring | raw-code ring | ...]; under the cluster
+  // schedule, once a CTA's MMAs are done its rings hold its partial
   uint64_t *bars = reinterpret_cast<uint64_t *>(base);
   uint8_t *b_st = base + kBarBytes;                  // NB * bBytes
   uint8_t *raw = b_st + NB * bBytes;                 // RawRing<INT4>::BYTES
@@ -350,8 +358,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   uint64_t *bfull = bars + 2 * kMaxAStages, *bempty = bfull + kMaxBStages;
   uint64_t *rfull = bempty + kMaxBStages, *rempty = rfull + kMaxRaw;
   uint64_t *dfull = rempty + kMaxRaw, *dempty = dfull + 2;
-  uint64_t *fxbar = dempty + 2;                      // one per lane quarter
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fxbar + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dempty + 2);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -418,7 +425,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         mbar_init(smem_u32(&dfull[s]), (uint32_t)tp.nmma);
         mbar_init(smem_u32(&dempty[s]), kEpiThreads);
       }
-      for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&fxbar[s]), 1);
       *abort_flag = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -575,84 +581,67 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     const int qtr = warp - kEpiWarp;  // == warp % 4: the TMEM lane quarter it may read
     const int r = qtr * 32 + lane;
     const uint32_t lane_base = (uint32_t)(qtr * 32) << 16;
-    const uint32_t blk = (uint32_t)Np * 32u * 4u;  // one CTA's partial of one lane quarter
-    uint8_t *stg = b_st + (size_t)qtr * tp.fx_bytes;
-    const uint32_t fxb = smem_u32(&fxbar[qtr]);
-    int fx_uses = 0;
     // Adds the partials of cut tile t (CTAs c_lo..c_hi, in that order) for
-    // this lane quarter and stores the rows.  Runs once this CTA's last MMA
-    // is done, with the rings free: the partials of up to fx_cap CTAs come
-    // in by bulk copies at once; slot 0 carries the running sum between
-    // batches.  False if a wait gave up.
-    auto finish_tile = [&](int t, int c_lo, int c_hi) -> bool {
+    // this lane quarter and stores the rows.  Each lane reads its own float4s
+    // of every partial straight from L2 (ld.global.cg: other SMs wrote them
+    // and L1 is not coherent with them), two partials per round trip, so the
+    // sum needs no shared memory and runs as soon as the count says so.
+    auto finish_tile = [&](int t, int c_lo, int c_hi) {
       const TileInfo ti = tile_info(tp, t);
       const int64_t grow = ti.row0 + r;
       const bool live = grow < ti.nrows;
       __half *yrow = p.y[ti.m] + grow;
       const int64_t ldy = p.ldy[ti.m];
-      bool have = false;
-      for (int k = c_lo; k <= c_hi;) {
-        const int s0 = have ? 1 : 0;
-        const int nb = tp.fx_cap - s0 < c_hi - k + 1 ? tp.fx_cap - s0 : c_hi - k + 1;
-        if (lane == 0) {
-          asm volatile("fence.proxy.async;" ::: "memory");
-          asm volatile(
-              "{\n\t.reg .b64 t;\n\t"
-              "mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1;\n\t}" ::"r"(fxb),
-              "r"((uint32_t)nb * blk)
-              : "memory");
-          for (int i = 0; i < nb; ++i) {
-            const float *src =
-                tp.part + (size_t)(((k + i) * 2 + part_slot(tp, k + i, t)) * 4 + qtr) * Np * 32;
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
-                "%2, [%3];" ::"r"(smem_u32(stg) + (uint32_t)(s0 + i) * blk),
-                "l"(src), "r"(blk), "r"(fxb)
-                : "memory");
-          }
-        }
-        const bool okf = mbar_wait(fxb, fx_uses & 1, abort_flag);
-        ++fx_uses;
-        if (!__all_sync(0xffffffffu, okf)) {
-          if (lane == 0) mbar_drain(fxb, (fx_uses - 1) & 1);
-          return false;
-        }
-        // running sums into slot 0; element (n, lane) of a block sits at
-        // float ((n / 4) * 32 + lane) * 4 + n % 4
-        float4 *sv = reinterpret_cast<float4 *>(stg) + lane;
-        for (int n4 = 0; n4 < tp.B; n4 += 4) {  // one float4 of columns at a time, partials in CTA order
-          float4 acc = have ? sv[(n4 / 4) * 32] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          for (int i = 0; i < nb; ++i) {
-            const float4 v = sv[(size_t)(s0 + i) * (blk / 16) + (n4 / 4) * 32];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-          }
-          sv[(n4 / 4) * 32] = acc;
-        }
-        have = true;
-        k += nb;
-        __syncwarp();
-      }
-      // the finished rows
-      if (live) {
-        const float4 *sv = reinterpret_cast<const float4 *>(stg) + lane;
-        for (int n0 = 0; n0 < tp.B; n0 += 4) {
-          const float4 a = sv[(n0 / 4) * 32];
-          const float e[4] = {a.x, a.y, a.z, a.w};
+      auto part = [&](int k) {  // CTA k's partial of this lane quarter: float4 (n / 4, lane)
+        return reinterpret_cast<const float4 *>(
+                   tp.part + (size_t)((k * 2 + part_slot(tp, k, t)) * 4 + qtr) * Np * 32) +
+               lane;
+      };
+      for (int n0 = 0; n0 < tp.B; n0 += 16) {  // 16 columns: 4 float4 per partial
+        float4 acc[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (n0 + q < tp.B) yrow[(int64_t)(n0 + q) * ldy] = __float2half_rn(e[q]);
+        for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int k = c_lo; k <= c_hi; k += 2) {
+          const bool two = k + 1 <= c_hi;
+          const float4 *pa = part(k) + (n0 / 4) * 32;
+          const float4 *pb = part(two ? k + 1 : k) + (n0 / 4) * 32;
+          float4 va[4], vb[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) va[q] = ld_cg_f4(pa + q * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) vb[q] = two ? ld_cg_f4(pb + q * 32) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[q].x += va[q].x;
+            acc[q].y += va[q].y;
+            acc[q].z += va[q].z;
+            acc[q].w += va[q].w;
+          }
+          if (two) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[q].x += vb[q].x;
+              acc[q].y += vb[q].y;
+              acc[q].z += vb[q].z;
+              acc[q].w += vb[q].w;
+            }
+          }
+        }
+        if (live) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float e[4] = {acc[q].x, acc[q].y, acc[q].z, acc[q].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int n = n0 + 4 * q + i;
+              if (n < tp.B) yrow[(int64_t)n * ldy] = __float2half_rn(e[i]);
+            }
+          }
         }
       }
-      __syncwarp();
-      return true;
     };
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int j = 0;
-    int def_t = -1, def_lo = 0, def_hi = 0;  // a cut tile to finish after the last MMA
-    bool aborted = false;
     for (int u = u_begin; u < u_end; ++j) {
       const int t = u / KT;
       const int k0 = u - t * KT;
@@ -677,10 +666,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       const int64_t ldy = p.ldy[ti.m];
       const int db = NBUF == 2 ? (j & 1) : 0;
       const bool ok = mbar_wait(smem_u32(&dfull[db]), (NBUF == 2 ? (j >> 1) : j) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        aborted = true;
-        break;
-      }
+      if (!__all_sync(0xffffffffu, ok)) break;
       fence_after();
       const uint32_t dcol = tmem + lane_base + (uint32_t)(db * W * 2 * Np);
       // partial of a cut tile: float4 (n / 4, lane) of its (slot, quarter) block
@@ -740,16 +726,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                      : "memory");
       prev = __shfl_sync(0xffffffffu, prev, 0);
       if (prev != (unsigned)(c_hi - c_lo)) continue;
-      // (lane 0's acquire orders its bulk copies of the others' partials)
-      if (u == u_end) {
-        if (!finish_tile(t, c_lo, c_hi)) aborted = true;
-      } else {  // only a first segment: finish it after the last MMA
-        def_t = t;
-        def_lo = c_lo;
-        def_hi = c_hi;
-      }
+      __syncwarp();  // lane 0's acquire, then every lane's loads of the partials
+      finish_tile(t, c_lo, c_hi);
     }
-    if (def_t >= 0 && !aborted) finish_tile(def_t, def_lo, def_hi);
   } else if (warp == kMmaWarp || warp == kMma2Warp) {
     // ---------------------------------------------------- MMA issuers ---
     // One thread per issuing warp; issuer w takes the units at positions
@@ -1170,20 +1149,12 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   tp.tiles = (int)tiles;
   tp.U = (int)(tiles * tp.KT);
   if (tc_smem_bytes(int4, tp.Np) > (size_t)di.max_smem_optin) return QZ_ERR_UNSUPPORTED;
-  // 200 KB: room to stage six partials of a lane quarter at batch 64, and
-  // below the SM's total, so that a small kernel launched before this one
-  // (the input gather) can still run beside it under programmatic launch
+  // 200 KB: below the SM's total, so that a small kernel launched before
+  // this one (the input gather) can still run beside it under programmatic
+  // launch; the cluster schedule stages its partial ([B][kM] fp32) in the rings
   const size_t smem = (size_t)di.max_smem_optin < (size_t)200 * 1024 ? (size_t)di.max_smem_optin
                                                                       : (size_t)200 * 1024;
   if (smem < tc_smem_bytes(int4, tp.Np)) return QZ_ERR_UNSUPPORTED;
-  {
-    // staging per lane quarter: whole partials of one quarter (Np x 32 fp32)
-    const size_t blk = (size_t)tp.Np * 32 * 4;
-    const size_t per_q = (smem - 1024 - kBarBytes) / 4 / blk * blk;
-    tp.fx_bytes = (uint32_t)per_q;
-    tp.fx_cap = (int)(per_q / blk);
-    if (tp.fx_cap < 2) return QZ_ERR_UNSUPPORTED;
-  }
   auto kern = int4 ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_status(e);
