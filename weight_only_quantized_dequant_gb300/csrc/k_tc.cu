@@ -54,7 +54,8 @@ constexpr int kM = 128;         // weight rows per tile (MMA M)
 constexpr int kKT = 128;        // K elements per work unit (one pipeline stage)
 constexpr int kMaxAStages = 6;  // A stages in tensor memory (64 columns each)
 constexpr uint32_t kTmemCols = 512;    // 2 x (outlier, background) accumulators, A above
-constexpr int kProducers = 256;  // 8 warps, two threads per weight row
+constexpr int kProducers = 256;  // 8 warps: two groups of 4 (alternate units), one thread per row
+constexpr int kGroupWarps = 4;   // converter warps that fill one A stage
 constexpr int kEpiWarp = kProducers / 32;     // warps 8-11 drain the accumulators
 constexpr int kMmaWarp = kEpiWarp + 4;        // warp 12 issues the MMAs of even units
 constexpr int kCodeWarp = kMmaWarp + 1;       // warp 13 fills the code ring
@@ -76,7 +77,6 @@ template <bool INT4>
 struct RawRing {
   static constexpr int DEPTH = INT4 ? 8 : 4;        // K tiles in flight
   static constexpr int ROWB = INT4 ? kKT / 2 : kKT;  // packed bytes per row per K tile
-  static constexpr int HB = ROWB / 2;                // bytes of one producer thread
   static constexpr int BYTES = DEPTH * kM * ROWB;
 };
 constexpr int kMaxRaw = 8;
@@ -369,10 +369,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   // loader sets up its own ring barriers, only arrives at the start-up
   // barrier (named barrier 1) and issues the first ring of code copies while
   // the other warps set up the rest and warp 0 allocates tensor memory.
-  constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB;
-  int cl_i = 0, cl_u = u_begin, cl_t = 0, cl_kt = 0;
-  auto issue_codes = [&](int i, int t, int kt) {
-    const uint32_t bar = smem_u32(&rfull[i % DR]);
+  // The ring is split between the two converter groups: group g owns slots
+  // g, g + 2, ..., so that every slot has one consumer that takes its
+  // copies in order (an mbarrier wait tells phases apart by parity only).
+  constexpr int DR = RawRing<INT4>::DEPTH, RB = RawRing<INT4>::ROWB, DRG = DR / 2;
+  static_assert(DR % 2 == 0, "the code ring splits evenly between the two groups");
+  int cl_n0 = 0, cl_n1 = 0;  // copies issued per group
+  int cl_u = u_begin, cl_t = 0, cl_kt = 0;
+  auto issue_codes = [&](int slot, int t, int kt) {
+    const uint32_t bar = smem_u32(&rfull[slot]);
     const TileInfo ti = tile_info(tp, t);
     const uint64_t cmap = reinterpret_cast<uint64_t>(&tp.codes_map[ti.m]);
     const int x = INT4 ? (kt - tp.ko) * RB : kt * RB;
@@ -383,7 +388,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         : "memory");
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(raw) + (uint32_t)(i % DR) * (kM * RB)),
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(raw) + (uint32_t)slot * (kM * RB)),
         "l"(cmap), "r"(x), "r"((int)ti.row0), "r"(bar)
         : "memory");
   };
@@ -392,21 +397,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     if (lane == 0) {
       for (int s = 0; s < kMaxRaw; ++s) {
         mbar_init(smem_u32(&rfull[s]), 1);
-        mbar_init(smem_u32(&rempty[s]), kProducers / 32);
+        mbar_init(smem_u32(&rempty[s]), kGroupWarps);
       }
       *abort_flag = 0;  // (thread 0 writes the same; this warp may poll it first)
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
     asm volatile("bar.arrive 1, %0;" ::"n"(kThreadsTc) : "memory");
-    if (lane == 0) {
+    if (lane == 0) {  // in unit order, until the next unit's sub-ring is full
       UnitPos up(u_begin, KT);
-      for (; cl_u < u_end && cl_i < DR; ++cl_u) {
+      for (; cl_u < u_end; ++cl_u) {
         const int t = up.t, kt = up.kt;
+        const int g = (cl_u - u_begin) & 1, c = g ? cl_n1 : cl_n0;
+        if (kt >= tp.ko && c == DRG) break;
         up.next(KT);
         if (kt < tp.ko) continue;  // outlier units read fp16 rows directly
-        issue_codes(cl_i, t, kt);
-        ++cl_i;
+        issue_codes(g + 2 * c, t, kt);
+        if (g)
+          ++cl_n1;
+        else
+          ++cl_n0;
       }
       cl_t = up.t;
       cl_kt = up.kt;
@@ -414,7 +424,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
   } else {
     if (tid == 0) {
       for (int s = 0; s < kMaxAStages; ++s) {
-        mbar_init(smem_u32(&full[s]), kProducers / 32);  // one arrival per converter warp
+        mbar_init(smem_u32(&full[s]), kGroupWarps);  // one arrival per converter warp of a group
         mbar_init(smem_u32(&empty[s]), 1);
       }
       for (int s = 0; s < kMaxBStages; ++s) {
@@ -447,19 +457,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
 
   if (warp < kEpiWarp) {
     // ------------------------------------------------------ producers ----
-    // Warp w converts k slots [64 h, 64 h + 64) of the rows of TMEM lane
-    // quarter w % 4 (h = w / 4): thread = one row, its 64 fp16 codes go to
-    // 32 columns of its own TMEM lane with one tcgen05.st.
-    const int h = warp >> 2, r = (warp & 3) * 32 + lane;
+    // Two groups of 4 warps (one per TMEM lane quarter) take alternate units:
+    // group g the units at positions q = g (mod 2), so that every wait and
+    // arrival of a group covers a whole unit's conversion.  Thread = one row
+    // of the tile: its 128 codes of the unit become 64 fp16 pairs in two
+    // halves of 32 TMEM columns of its own lane, one tcgen05.st each.
+    const int g = warp >> 2, r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     // Background (INT4) or all (INT8) K tiles arrive as packed codes in the
-    // raw ring (filled by the code loader warp); each thread converts its bytes.
-    constexpr int HB = RawRing<INT4>::HB;
-    const uint32_t raw_me = smem_u32(raw) + (uint32_t)r * RB + (uint32_t)h * HB;
+    // raw ring (filled by the code loader warp); each thread converts its row.
+    const uint32_t raw_me = smem_u32(raw) + (uint32_t)r * RB;
     // Weights only: no wait for the preceding kernel (under programmatic
     // launch the caller guarantees that nothing in flight writes them).
-    int i = 0;       // code tiles taken from the raw ring so far
-    int t_cur = -1;  // tile of the previous unit
+    int n = 0;       // code tiles this group has taken from its sub-ring
+    int t_cur = -1;  // tile of the previous unit of this group
     TileInfo ti = {0, 0, 0};
     RingPos ap;                    // A stage of the unit
     UnitPos up(u_begin, KT);       // (tile, K tile) of the unit
@@ -470,6 +481,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       const int t = up.t, kt = up.kt;
       ap.next(NA);
       up.next(KT);
+      const bool outl = INT4 && kt < tp.ko;
+      if ((q & 1) != g) continue;
       if (q >= NA) {
         const bool ok = mbar_wait(smem_u32(&empty[s]), aph ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -481,94 +494,111 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       }
       const int64_t grow = ti.row0 + r;
       const bool live = grow < ti.nrows;
-      const bool outl = kt < tp.ko;
-      uint32_t o[32];  // fp16 pairs of k slots 2j, 2j+1 of this thread's 64
-      if (INT4 && outl) {
-        const int t0 = kt * kKT + h * (kKT / 2);
+      const uint32_t acol = tmem + lane_base + tp.a_base + (uint32_t)s * (kKT / 2);
+      uint32_t o[32];  // fp16 pairs of k slots 2j, 2j+1 of one half (64 slots)
+      if (outl) {
         const uint4 *src = reinterpret_cast<const uint4 *>(p.w_out[ti.m] + grow * p.ld_out[ti.m]);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int t0 = kt * kKT + h * (kKT / 2);
 #pragma unroll
-        for (int kg = 0; kg < 8; ++kg) {
-          const int tt = t0 + kg * 8;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (live && tt < p.n_out) {
-            v = __ldg(src + tt / 8);
-            // zero the slots past n_out inside the last group
-            const int valid = p.n_out - tt;
-            if (valid < 8) {
-              uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          for (int kg = 0; kg < 8; ++kg) {
+            const int tt = t0 + kg * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (live && tt < p.n_out) {
+              v = __ldg(src + tt / 8);
+              // zero the slots past n_out inside the last group
+              const int valid = p.n_out - tt;
+              if (valid < 8) {
+                uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (e >= valid) w[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
-              v = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 8; ++e)
+                  if (e >= valid) w[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+                v = make_uint4(w[0], w[1], w[2], w[3]);
+              }
             }
+            o[4 * kg] = v.x;
+            o[4 * kg + 1] = v.y;
+            o[4 * kg + 2] = v.z;
+            o[4 * kg + 3] = v.w;
           }
-          o[4 * kg] = v.x;
-          o[4 * kg + 1] = v.y;
-          o[4 * kg + 2] = v.z;
-          o[4 * kg + 3] = v.w;
-        }
-      } else if (INT4) {
-        const bool ok = mbar_wait(smem_u32(&rfull[i % DR]), (i / DR) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const uint32_t rsrc = raw_me + (uint32_t)(i % DR) * (kM * RB);
-        uint4 qv[2];
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(qv[c].x), "=r"(qv[c].y), "=r"(qv[c].z), "=r"(qv[c].w)
-                       : "r"(rsrc + 16 * c));
-        __syncwarp();  // the warp's codes are in registers
-        if (lane == 0) mbar_arrive(smem_u32(&rempty[i % DR]));
-        ++i;
-        const uint32_t words[8] = {qv[0].x, qv[0].y, qv[0].z, qv[0].w,
-                                   qv[1].x, qv[1].y, qv[1].z, qv[1].w};
-        const uint32_t bias = 0x64086408u;   // 1032 in both halves after the XOR
-#pragma unroll
-        for (int kg = 0; kg < 8; ++kg) {
-          const uint32_t w = words[kg];
-          // Nibble pairs at bits 0-3 / 16-19: 1024 + (q+8) - 1032 = q.  Pairs
-          // at bits 4-7 / 20-23 are masked in place: 1024 + 16 (q+8), then
-          // x/16 - 72 = q in one fused step (every value a small integer,
-          // exact in fp16).  One shift by 8 serves the upper two pairs.
-          // Elements past kb hold zero nibbles (q = 0) from the row padding,
-          // rows past N zeros; slot order 0,4,1,5,2,6,3,7 (pairs (e0,e4),
-          // (e1,e5), ...).
-          const uint32_t w8 = w >> 8;
-          o[4 * kg] = hsub2_u32((w & 0x000F000Fu) ^ bias, bias);
-          o[4 * kg + 1] = hfma2_u32((w & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u, 0xD480D480u);
-          o[4 * kg + 2] = hsub2_u32((w8 & 0x000F000Fu) ^ bias, bias);
-          o[4 * kg + 3] = hfma2_u32((w8 & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u, 0xD480D480u);
+          tmem_st32(acol + (uint32_t)h * 32, o);
         }
       } else {
-        const bool ok = mbar_wait(smem_u32(&rfull[i % DR]), (i / DR) & 1, abort_flag);
+        const int slot = g + 2 * (n % DRG);
+        const bool ok = mbar_wait(smem_u32(&rfull[slot]), (n / DRG) & 1, abort_flag);
+        ++n;
         if (!__all_sync(0xffffffffu, ok)) break;
-        const uint32_t rsrc = raw_me + (uint32_t)(i % DR) * (kM * RB);
-        uint4 vv[4];
+        const uint32_t rsrc = raw_me + (uint32_t)slot * (kM * RB);
+        if (INT4) {
+          uint4 qv[4];  // the row's 64 code bytes
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(vv[c].x), "=r"(vv[c].y), "=r"(vv[c].z), "=r"(vv[c].w)
-                       : "r"(rsrc + 16 * c));
-        __syncwarp();  // the warp's codes are in registers
-        if (lane == 0) mbar_arrive(smem_u32(&rempty[i % DR]));
-        ++i;
+          for (int c = 0; c < 4; ++c)
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(qv[c].x), "=r"(qv[c].y), "=r"(qv[c].z), "=r"(qv[c].w)
+                         : "r"(rsrc + 16 * c));
+          __syncwarp();  // the warp's codes are in registers
+          if (lane == 0) mbar_arrive(smem_u32(&rempty[slot]));
+          const uint32_t bias = 0x64086408u;  // 1032 in both halves after the XOR
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t w[4] = {vv[c].x ^ 0x80808080u, vv[c].y ^ 0x80808080u,
-                                 vv[c].z ^ 0x80808080u, vv[c].w ^ 0x80808080u};
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t words[8] = {qv[2 * h].x,     qv[2 * h].y,     qv[2 * h].z,
+                                       qv[2 * h].w,     qv[2 * h + 1].x, qv[2 * h + 1].y,
+                                       qv[2 * h + 1].z, qv[2 * h + 1].w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // 0x64 above each offset-binary byte: 1024 + (q + 128); minus 1152
-            o[8 * c + 2 * k] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4140), 0x64806480u);
-            o[8 * c + 2 * k + 1] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4342), 0x64806480u);
+            for (int kg = 0; kg < 8; ++kg) {
+              const uint32_t w = words[kg];
+              // Nibble pairs at bits 0-3 / 16-19: 1024 + (q+8) - 1032 = q.
+              // Pairs at bits 4-7 / 20-23 are masked in place: 1024 + 16 (q+8),
+              // then x/16 - 72 = q in one fused step (every value a small
+              // integer, exact in fp16).  One shift by 8 serves the upper two
+              // pairs.  Elements past kb hold zero nibbles (q = 0) from the
+              // row padding, rows past N zeros; slot order 0,4,1,5,2,6,3,7
+              // (pairs (e0,e4), (e1,e5), ...).
+              const uint32_t w8 = w >> 8;
+              o[4 * kg] = hsub2_u32((w & 0x000F000Fu) ^ bias, bias);
+              o[4 * kg + 1] = hfma2_u32((w & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u, 0xD480D480u);
+              o[4 * kg + 2] = hsub2_u32((w8 & 0x000F000Fu) ^ bias, bias);
+              o[4 * kg + 3] = hfma2_u32((w8 & 0x00F000F0u) ^ 0x64806480u, 0x2C002C00u, 0xD480D480u);
+            }
+            if (!live) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = 0;
+            }
+            tmem_st32(acol + (uint32_t)h * 32, o);
+          }
+        } else {
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            uint4 vv[4];  // 64 code bytes of this half
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(vv[c].x), "=r"(vv[c].y), "=r"(vv[c].z), "=r"(vv[c].w)
+                           : "r"(rsrc + 64 * h + 16 * c));
+            if (h == 1) {
+              __syncwarp();  // the warp's codes are in registers
+              if (lane == 0) mbar_arrive(smem_u32(&rempty[slot]));
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t w[4] = {vv[c].x ^ 0x80808080u, vv[c].y ^ 0x80808080u,
+                                     vv[c].z ^ 0x80808080u, vv[c].w ^ 0x80808080u};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                // 0x64 above each offset-binary byte: 1024 + (q + 128); minus 1152
+                o[8 * c + 2 * k] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4140), 0x64806480u);
+                o[8 * c + 2 * k + 1] = hsub2_u32(__byte_perm(w[k], 0x64646464u, 0x4342), 0x64806480u);
+              }
+            }
+            if (!live) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = 0;
+            }
+            tmem_st32(acol + (uint32_t)h * 32, o);
           }
         }
       }
-      if (!live) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = 0;
-      }
-      tmem_st32(tmem + lane_base + tp.a_base + (uint32_t)s * (kKT / 2) + (uint32_t)h * 32, o);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       fence_before();
       __syncwarp();  // every lane's tensor-memory stores are complete
@@ -795,8 +825,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     // CTA's units, one 2D tensor copy of kM rows x ROWB bytes each, DR ahead
     // of the converters.  The codes are static: no wait for earlier kernels.
     if (lane == 0) {
-      // (the first ring of copies went out in the prologue)
-      int i = cl_i;
+      // (the first copies went out in the prologue)
+      int n0 = cl_n0, n1 = cl_n1;
       UnitPos up(u_begin, KT);
       up.t = cl_t;
       up.kt = cl_kt;
@@ -804,15 +834,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         const int t = up.t, kt = up.kt;
         up.next(KT);
         if (kt < tp.ko) continue;  // outlier units read fp16 rows directly
-        if (i >= DR) {
-          if (!mbar_wait(smem_u32(&rempty[i % DR]), ((i / DR) - 1) & 1, abort_flag)) break;
+        const int g = (u - u_begin) & 1, c = g ? n1 : n0;
+        const int slot = g + 2 * (c % DRG);
+        if (c >= DRG) {
+          if (!mbar_wait(smem_u32(&rempty[slot]), ((c / DRG) - 1) & 1, abort_flag)) break;
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-        issue_codes(i, t, kt);
-        ++i;
+        issue_codes(slot, t, kt);
+        if (g)
+          ++n1;
+        else
+          ++n0;
       }
       if (*(volatile int *)abort_flag)  // let the copies in flight land
-        for (int k = i > DR ? i - DR : 0; k < i; ++k) mbar_drain(smem_u32(&rfull[k % DR]), (k / DR) & 1);
+        for (int g = 0; g < 2; ++g) {
+          const int ng = g ? n1 : n0;
+          for (int c = ng > DRG ? ng - DRG : 0; c < ng; ++c)
+            mbar_drain(smem_u32(&rfull[g + 2 * (c % DRG)]), (c / DRG) & 1);
+        }
     }
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------ activation loader ---
@@ -1117,6 +1156,9 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   tp.a_base = (uint32_t)(tp.nbuf * tp.nmma * 2 * tp.Np);
   tp.nsa = (int)((kTmemCols - tp.a_base) / (kKT / 2));
   if (tp.nsa > kMaxAStages) tp.nsa = kMaxAStages;
+  // Even, so that each A stage is filled by one converter group and read by
+  // one issuer, in order (mbarrier waits tell phases apart by parity only).
+  tp.nsa &= ~1;
   tp.ko = int4 ? (g.n_out + kKT - 1) / kKT : 0;
   tp.kbt = int4 ? (g.kb + kKT - 1) / kKT : (g.K + kKT - 1) / kKT;
   tp.KT = tp.ko + tp.kbt;
