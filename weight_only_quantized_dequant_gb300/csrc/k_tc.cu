@@ -1203,11 +1203,13 @@ qz_status launch_tc(bool int4, int B, const GemvParams &g, const int64_t *mat_ro
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
   if (e != cudaSuccess) return cuda_status(e);
 
-  // Schedule.  Estimated times in microseconds (GB300 measurements): a
-  // launch costs kStart (start-up to the first MMA and the drain after the
-  // last), a unit 0.9 (8 MMAs); stream-K adds the L2 reduction of its cut
-  // tiles, a cluster of S > 1 its shared-memory reduction, and clusters come
-  // in waves of what fits on the GPCs at once.
+  // Schedule.  Estimated times in microseconds, fitted to GB300 timings of
+  // an earlier build of this kernel (units now cost about half as much; the
+  // choices were re-checked against forced schedules and still pick the
+  // faster one): a launch costs kStart (start-up to the first MMA and the
+  // drain after the last), a unit 0.9 (8 MMAs); stream-K adds the L2
+  // reduction of its cut tiles, a cluster of S > 1 its shared-memory
+  // reduction, and clusters come in waves of what fits on the GPCs at once.
   const int gmax = di.sms < kMaxCtas ? di.sms : kMaxCtas;
   const double kStart = 3.5, kUnit = 0.9;
   double best = 1e30;
