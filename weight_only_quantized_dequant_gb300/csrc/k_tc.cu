@@ -531,12 +531,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         if (!__all_sync(0xffffffffu, ok)) break;
         const uint32_t rsrc = raw_me + (uint32_t)slot * (kM * RB);
         if (INT4) {
-          uint4 qv[4];  // the row's 64 code bytes
+          uint4 qv[4];  // the row's 64 code bytes (chunk c at c ^ ((r / 2) % 4): 64-byte swizzle)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(qv[c].x), "=r"(qv[c].y), "=r"(qv[c].z), "=r"(qv[c].w)
-                         : "r"(rsrc + 16 * c));
+                         : "r"(rsrc + 16u * ((uint32_t)c ^ (((uint32_t)r >> 1) & 3u))));
           __syncwarp();  // the warp's codes are in registers
           if (lane == 0) mbar_arrive(smem_u32(&rempty[slot]));
           const uint32_t bias = 0x64086408u;  // 1032 in both halves after the XOR
@@ -570,12 +570,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         } else {
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
-            uint4 vv[4];  // 64 code bytes of this half
+            uint4 vv[4];  // 64 code bytes of this half (chunk k at k ^ (r % 8): 128-byte swizzle)
 #pragma unroll
             for (int c = 0; c < 4; ++c)
               asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                            : "=r"(vv[c].x), "=r"(vv[c].y), "=r"(vv[c].z), "=r"(vv[c].w)
-                           : "r"(rsrc + 64 * h + 16 * c));
+                           : "r"(rsrc + 16u * ((uint32_t)(4 * h + c) ^ ((uint32_t)r & 7u))));
             if (h == 1) {
               __syncwarp();  // the warp's codes are in registers
               if (lane == 0) mbar_arrive(smem_u32(&rempty[slot]));
@@ -1064,6 +1064,9 @@ EncodeTiledFn encode_tiled() {
 
 // The packed codes of one matrix as a 2D byte tensor [rows][ld bytes], read
 // in boxes of kM rows x row_bytes bytes (rows past the end read as zeros).
+// The copy swizzles the 16-byte chunks of each row (64- or 128-byte pattern,
+// the row's own size), so that the converter threads, one row each, read a
+// chunk column without shared-memory bank conflicts.
 qz_status codes_map(CUtensorMap *map, const uint8_t *codes, int64_t ld, int64_t rows,
                     int row_bytes) {
   EncodeTiledFn fn = encode_tiled();
@@ -1074,7 +1077,10 @@ qz_status codes_map(CUtensorMap *map, const uint8_t *codes, int64_t ld, int64_t 
   const cuuint32_t estride[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dim,
                         stride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                        : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                          : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? QZ_OK : QZ_ERR_INVALID_ARG;
 }
