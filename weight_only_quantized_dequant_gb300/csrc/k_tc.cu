@@ -472,19 +472,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     int n = 0;       // code tiles this group has taken from its sub-ring
     int t_cur = -1;  // tile of the previous unit of this group
     TileInfo ti = {0, 0, 0};
-    RingPos ap;                    // A stage of the unit
-    UnitPos up(u_begin, KT);       // (tile, K tile) of the unit
-    for (int u = u_begin; u < u_end; ++u) {
-      const int q = u - u_begin;  // position in this CTA's ring sequence
-      const int s = ap.slot;
-      const uint32_t aph = ap.parity;
+    // This group visits only its own units, positions q = g, g + 2, ...
+    // (A stage q mod NA: NA is even, so the group's stages are its own).
+    int s = g % NA;                // A stage of the unit
+    uint32_t aph = 0;              // parity of the stage's current round
+    UnitPos up(u_begin + g, KT);   // (tile, K tile) of the unit
+    const int n_units = u_end - u_begin;
+    for (int q = g; q < n_units; q += 2) {
       const int t = up.t, kt = up.kt;
-      ap.next(NA);
-      up.next(KT);
+      const int s_here = s;
+      const uint32_t aph_here = aph;
+      up.kt += 2;
+      while (up.kt >= KT) {
+        up.kt -= KT;
+        ++up.t;
+      }
+      s += 2;
+      if (s >= NA) {
+        s -= NA;
+        aph ^= 1u;
+      }
       const bool outl = INT4 && kt < tp.ko;
-      if ((q & 1) != g) continue;
       if (q >= NA) {
-        const bool ok = mbar_wait(smem_u32(&empty[s]), aph ^ 1u, abort_flag);
+        const bool ok = mbar_wait(smem_u32(&empty[s_here]), aph_here ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
         fence_after();  // the MMAs that read this A stage are complete
       }
@@ -494,7 +504,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       }
       const int64_t grow = ti.row0 + r;
       const bool live = grow < ti.nrows;
-      const uint32_t acol = tmem + lane_base + tp.a_base + (uint32_t)s * (kKT / 2);
+      const uint32_t acol = tmem + lane_base + tp.a_base + (uint32_t)s_here * (kKT / 2);
       uint32_t o[32];  // fp16 pairs of k slots 2j, 2j+1 of one half (64 slots)
       if (outl) {
         const uint4 *src = reinterpret_cast<const uint4 *>(p.w_out[ti.m] + grow * p.ld_out[ti.m]);
@@ -602,7 +612,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       fence_before();
       __syncwarp();  // every lane's tensor-memory stores are complete
-      if (lane == 0) mbar_arrive(smem_u32(&full[s]));
+      if (lane == 0) mbar_arrive(smem_u32(&full[s_here]));
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------- epilogue ----
@@ -770,53 +780,87 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     if (lane == 0 && w < W) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       const uint32_t idesc = idesc_f16(kM, Np);
-      int j = -1;
+      // This issuer visits only its own units (positions q = w, w + W, ...).
+      // Segment j of the range is tile t0 + j; the issuer enters every
+      // segment in order (waiting for the drain of that buffer's previous
+      // segment) and commits each one's accumulator-full barrier once, right
+      // after its last own unit there, or on leaving a segment it had no unit
+      // in, so that the barrier sees W arrivals per segment.
+      const int n_units = u_end - u_begin;
+      const int t0 = u_begin / KT, j_last = n_units > 0 ? (u_end - 1) / KT - t0 : -1;
+      int jc = -1;       // segment entered
+      bool cm = false;   // its accumulator-full barrier committed
       uint32_t dcol = 0;
       int db = 0;
       bool seen_out = false, seen_bg = false;  // this issuer's first unit of each kind in the segment
-      RingPos ap, bp;
-      UnitPos up(u_begin, KT);
-      for (int u = u_begin; u < u_end; ++u) {
-        const int q = u - u_begin;
-        const int kt = up.kt;
-        const int s = ap.slot, sb = bp.slot;
-        const uint32_t aph = ap.parity, bph = bp.parity;
-        up.next(KT);
-        ap.next(NA);
-        bp.next(NB);
-        if (q == 0 || kt == 0) {  // a new segment: next accumulator buffer
-          ++j;
-          db = NBUF == 2 ? (j & 1) : 0;
+      bool ok = true;
+      auto enter_through = [&](int jq) {  // move to segment jq, closing the ones left
+        while (jc < jq) {
+          if (jc >= 0 && !cm) mma_commit(smem_u32(&dfull[db]));
+          ++jc;
+          cm = false;
+          db = NBUF == 2 ? (jc & 1) : 0;
           dcol = (uint32_t)((db * W + w) * 2 * Np);
           seen_out = seen_bg = false;
-          if (j >= NBUF) {
-            if (!mbar_wait(smem_u32(&dempty[db]), ((NBUF == 2 ? (j >> 1) : j) - 1) & 1, abort_flag))
-              break;
+          if (jc >= NBUF) {
+            if (!mbar_wait(smem_u32(&dempty[db]), ((NBUF == 2 ? (jc >> 1) : jc) - 1) & 1, abort_flag)) {
+              ok = false;
+              return;
+            }
             fence_after();
           }
         }
-        if ((q & (W - 1)) == w) {
-          if (!mbar_wait(smem_u32(&full[s]), aph, abort_flag)) break;
-          if (!mbar_wait(smem_u32(&bfull[sb]), bph, abort_flag)) break;
-          fence_after();
-          const bool outl = kt < tp.ko;
-          const uint32_t a0 = tmem + tp.a_base + (uint32_t)s * (kKT / 2);
-          const uint32_t b0 = smem_u32(b_st + sb * bBytes);
-          const uint32_t d = tmem + dcol + (outl ? 0u : (uint32_t)Np);
-          const bool first = outl ? !seen_out : !seen_bg;
-          if (outl)
-            seen_out = true;
-          else
-            seen_bg = true;
-          const uint64_t bd = sdesc(b0);
+      };
+      UnitPos up(u_begin + w, KT);  // (tile, K tile) of position q
+      int s = w % NA, sb = w % NB;
+      uint32_t aph = 0, bph = 0;
+      for (int q = w; q < n_units && ok; q += W) {
+        const int kt = up.kt;
+        enter_through(up.t - t0);
+        if (!ok) break;
+        if (!mbar_wait(smem_u32(&full[s]), aph, abort_flag)) break;
+        if (!mbar_wait(smem_u32(&bfull[sb]), bph, abort_flag)) break;
+        fence_after();
+        const bool outl = kt < tp.ko;
+        const uint32_t a0 = tmem + tp.a_base + (uint32_t)s * (kKT / 2);
+        const uint32_t b0 = smem_u32(b_st + sb * bBytes);
+        const uint32_t d = tmem + dcol + (outl ? 0u : (uint32_t)Np);
+        const bool first = outl ? !seen_out : !seen_bg;
+        if (outl)
+          seen_out = true;
+        else
+          seen_bg = true;
+        const uint64_t bd = sdesc(b0);
 #pragma unroll
-          for (int k16 = 0; k16 < kKT / 16; ++k16)  // (the descriptor's address field is in 16 B)
-            mma_f16_ta(d, a0 + 8 * k16, bd + (uint64_t)(k16 * 2 * kLBO / 16), idesc,
-                       (first && k16 == 0) ? 0u : 1u);
-          mma_commit(smem_u32(&empty[s]));
-          mma_commit(smem_u32(&bempty[sb]));
+        for (int k16 = 0; k16 < kKT / 16; ++k16)  // (the descriptor's address field is in 16 B)
+          mma_f16_ta(d, a0 + 8 * k16, bd + (uint64_t)(k16 * 2 * kLBO / 16), idesc,
+                     (first && k16 == 0) ? 0u : 1u);
+        mma_commit(smem_u32(&empty[s]));
+        mma_commit(smem_u32(&bempty[sb]));
+        if (q + W >= n_units || kt + W >= KT) {  // its last unit of this segment
+          mma_commit(smem_u32(&dfull[db]));
+          cm = true;
         }
-        if (u + 1 == u_end || kt + 1 == KT) mma_commit(smem_u32(&dfull[db]));
+        // next own position: W units on
+        up.kt += W;
+        while (up.kt >= KT) {
+          up.kt -= KT;
+          ++up.t;
+        }
+        s += W;
+        if (s >= NA) {
+          s -= NA;
+          aph ^= 1u;
+        }
+        sb += W;
+        if (sb >= NB) {
+          sb -= NB;
+          bph ^= 1u;
+        }
+      }
+      if (ok) {  // the segments after its last unit, and the last one's barrier
+        enter_through(j_last);
+        if (ok && jc >= 0 && !cm) mma_commit(smem_u32(&dfull[db]));
       }
     }
   } else if (warp == kCodeWarp) {
