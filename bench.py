@@ -440,7 +440,8 @@ def copy_probe_gbs(device) -> float:
 # The other configurations, reported as sub-results of the headline line.
 SUB_CONFIGS = [("gemma2_9b_int8", 1), ("gemma2_9b_int8", 16), ("llama32_3b_int4o", 1),
                ("llama_7b_int4o", 1), ("llama_7b_int4o", 4), ("llama_7b_int4o", 16),
-               ("llama_7b_int4o", 64), ("llama_70b_int4o", 1)]
+               ("llama_7b_int4o", 64), ("llama_7b_int8", 1), ("llama_70b_int8", 1),
+               ("llama_70b_int4o", 1)]
 
 
 def measure_tiny(steps: int, warmup: int, device, peak: float) -> dict:

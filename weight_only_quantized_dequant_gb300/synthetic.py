@@ -73,6 +73,9 @@ WORKLOADS = {
     "llama_7b_int4o": Workload("llama_7b_int4o", "int4o", 4096, 4096, 4096, 11008, 32, 7000,
                                batches=(1, 4, 16, 64)),
     "llama_70b_int4o": Workload("llama_70b_int4o", "int4o", 8192, 8192, 1024, 28672, 80, 70000),
+    # the same decoder shapes in the per-tensor INT8 format
+    "llama_7b_int8": Workload("llama_7b_int8", "int8", 4096, 4096, 4096, 11008, 32, 7500),
+    "llama_70b_int8": Workload("llama_70b_int8", "int8", 8192, 8192, 1024, 28672, 80, 70500),
 }
 
 
