@@ -539,6 +539,30 @@ def test_full_70b_gate_up_grouped_int4_sampled():
         assert_close(y[rows], y_ref[0], a_ref[0], f"70b gate+up sampled m={i}")
 
 
+def test_full_70b_gate_up_grouped_int8_sampled():
+    """The largest batch-1 launch of the 70B-shaped INT8 stack: gate and up
+    (2 x 28672 x 8192) in one grouped call.  The per-tensor scale and the
+    codes of sampled rows against the oracle quantizer run on each whole
+    matrix; outputs on 64 sampled rows of each matrix plus the rows at both
+    ends."""
+    N, K = 28672, 8192
+    Ws = [S.weight(N, K, 91 + i, device=DEV) for i in range(2)]
+    ws = [qz().quantize_int8(W) for W in Ws]
+    x = S.activation(1, K, 94, device=DEV)
+    ys = qz().gemv_int8_grouped(ws, x[0])
+    assert qz().device_error() == 0
+    rng = np.random.default_rng(2)
+    for i, (W, w, y) in enumerate(zip(Ws, ws, ys)):
+        q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+        assert w.scale.item() == float(s_ref)
+        rows = np.unique(np.concatenate([rng.choice(N, 64, replace=False),
+                                         [0, 1, 15, 16, N - 17, N - 16, N - 1]]))
+        q_rows = w.q[torch.from_numpy(rows).to(DEV)].cpu().numpy()[:, :K]
+        assert np.array_equal(q_rows, q_ref[rows])
+        y_ref, a_ref = O.int8_product_ref(q_ref[rows], s_ref, x.cpu().numpy())
+        assert_close(y[rows], y_ref[0], a_ref[0], f"70b int8 gate+up sampled m={i}")
+
+
 @pytest.mark.parametrize("fmt,Ns,K,n_out", [("int4o", [7300, 7301], 3000, 31),
                                              ("int4o", [14600], 8200, 83),
                                              ("int8", [14593], 1000, 0),
