@@ -187,14 +187,35 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D (TMEM) += A (TMEM: lane = row, 2 fp16 of K per column) * B (shared).
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                           uint32_t idesc, uint32_t accumulate) {
+// The eight MMAs of one unit (K slots 0..127): D (TMEM) += A[:, 16k:16k+16] *
+// B[16k:16k+16, :], A in TMEM at a0 + 8k (lane = row, 2 fp16 of K per column),
+// B in shared memory with its descriptor's low word advanced by 16 per step
+// (the address field, in 16-byte units, cannot carry: shared memory is below
+// 256 KB); only the first may start the accumulator (acc0 == 0).  One asm
+// block keeps the issuing thread's instructions per MMA to three.
+__device__ __forceinline__ void mma8_f16_ta(uint32_t d, uint32_t a0, uint32_t blo, uint32_t bhi,
+                                            uint32_t idesc, uint32_t acc0) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 lo, a;\n\t"
+      "setp.ne.b32 p0, %5, 0;\n\t"
+      "setp.eq.b32 p1, %5, %5;\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p0;\n\t"
+      "add.u32 a, %1, 8;\n\tadd.u32 lo, %2, 16;\n\tmov.b64 b, {lo, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, p1;\n\t"
+      "add.u32 a, %1, 16;\n\tadd.u32 lo, %2, 32;\n\tmov.b64 b, {lo, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, p1;\n\t"
+      "add.u32 a, %1, 24;\n\tadd.u32 lo, %2, 48;\n\tmov.b64 b, {lo, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, p1;\n\t"
+      "add.u32 a, %1, 32;\n\tadd.u32 lo, %2, 64;\n\tmov.b64 b, {lo, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, p1;\n\t"
+      "add.u32 a, %1, 40;\n\tadd.u32 lo, %2, 80;\n\tmov.b64 b, {lo, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, p1;\n\t"
+      "add.u32 a, %1, 48;\n\tadd.u32 lo, %2, 96;\n\tmov.b64 b, {lo, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, p1;\n\t"
+      "add.u32 a, %1, 56;\n\tadd.u32 lo, %2, 112;\n\tmov.b64 b, {lo, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, p1;\n\t}" ::"r"(d),
+      "r"(a0), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0));
 }
 
 // 32 consecutive 32-bit TMEM columns of this thread's lane.
@@ -830,11 +851,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
           seen_out = true;
         else
           seen_bg = true;
+        static_assert(kKT / 16 == 8 && 2 * kLBO / 16 == 16, "mma8_f16_ta covers one unit");
         const uint64_t bd = sdesc(b0);
-#pragma unroll
-        for (int k16 = 0; k16 < kKT / 16; ++k16)  // (the descriptor's address field is in 16 B)
-          mma_f16_ta(d, a0 + 8 * k16, bd + (uint64_t)(k16 * 2 * kLBO / 16), idesc,
-                     (first && k16 == 0) ? 0u : 1u);
+        mma8_f16_ta(d, a0, (uint32_t)bd, (uint32_t)(bd >> 32), idesc, first ? 0u : 1u);
         mma_commit(smem_u32(&empty[s]));
         mma_commit(smem_u32(&bempty[sb]));
         if (q + W >= n_units || kt + W >= KT) {  // its last unit of this segment
