@@ -96,6 +96,33 @@ def test_int8_gemm(N, K, B):
     assert_close(Y, y_ref, a_ref, f"int8 N={N} K={K} B={B}")
 
 
+def two_byte_aligned_rows(X: torch.Tensor) -> torch.Tensor:
+    """Copy of X whose first row starts 2 bytes past a 16-byte boundary and
+    whose rows are K + 1 fp16 apart (so no row is 16-byte aligned at K % 8 ==
+    0): the inputs' fp16 alignment is all the interface promises."""
+    B, K = X.shape
+    buf = torch.zeros((B * (K + 1) + 8,), dtype=X.dtype, device=X.device)
+    out = buf[1:1 + B * (K + 1)].view(B, K + 1)[:, :K]
+    out.copy_(X)
+    assert out.data_ptr() % 16 == 2
+    return out
+
+
+@pytest.mark.parametrize("N,K", [(37, 100), (257, 1000), (1024, 4096), (96, 14336)])
+@pytest.mark.parametrize("B", [1, 3])
+def test_int8_inputs_only_two_byte_aligned(N, K, B):
+    """The GEMV reads inputs 16 bytes at a time where they are 16-byte aligned
+    and element by element otherwise; both give the oracle's result."""
+    W = S.weight(N, K, 2100 + N + K, device=DEV)
+    X = two_byte_aligned_rows(S.activation(B, K, 3100 + B, device=DEV))
+    w = qz().quantize_int8(W)
+    Y = qz().gemv_int8(w, X[0]).unsqueeze(0) if B == 1 else qz().gemm_int8(w, X)
+    assert qz().device_error() == 0
+    q_ref, s_ref = O.int8_quantize(W.cpu().numpy())
+    y_ref, a_ref = O.int8_product_ref(q_ref, s_ref, X.cpu().numpy())
+    assert_close(Y, y_ref, a_ref, f"int8 2-byte-aligned x N={N} K={K} B={B}")
+
+
 def test_int8_zero_matrix():
     W = torch.zeros((5, 40), dtype=torch.float16, device=DEV)
     w = qz().quantize_int8(W)
@@ -203,6 +230,20 @@ def test_int4_gemm(N, K, n_out, B):
     wo, q4, s = O.int4o_quantize(W.cpu().numpy(), perm.cpu().numpy(), n_out)
     y_ref, a_ref = O.int4o_product_ref(wo, q4, s, perm.cpu().numpy(), n_out, K, X.cpu().numpy())
     assert_close(Y, y_ref, a_ref, f"int4 N={N} K={K} n_out={n_out} B={B}")
+
+
+@pytest.mark.parametrize("N,K,n_out", [(64, 520, 6), (129, 4096, 41), (64, 11008, 111)])
+@pytest.mark.parametrize("B", [1, 3, 16])
+def test_int4_inputs_only_two_byte_aligned(N, K, n_out, B):
+    """INT4 products with inputs at fp16 alignment only (see the INT8 case)."""
+    W, prof, perm = _int4_inputs(N, K, n_out, 5100 + K + n_out)
+    w = qz().quantize_int4_outlier(W, perm, n_out)
+    X = two_byte_aligned_rows(S.activation(B, K, 6100 + B, device=DEV))
+    Y = qz().gemv_int4_outlier(w, X[0]).unsqueeze(0) if B == 1 else qz().gemm_int4_outlier(w, X)
+    assert qz().device_error() == 0
+    wo, q4, s = O.int4o_quantize(W.cpu().numpy(), perm.cpu().numpy(), n_out)
+    y_ref, a_ref = O.int4o_product_ref(wo, q4, s, perm.cpu().numpy(), n_out, K, X.cpu().numpy())
+    assert_close(Y, y_ref, a_ref, f"int4 2-byte-aligned x N={N} K={K} n_out={n_out} B={B}")
 
 
 def test_int4_grouped_matches_separate():
