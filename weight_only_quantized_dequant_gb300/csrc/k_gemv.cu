@@ -409,8 +409,8 @@ __global__ void __launch_bounds__(W * 32, Ring<B>::MINB)
   // The first stages are issued before the wait: weights are static, so
   // under programmatic overlap they stream in during the previous kernel.
   // With the permutation read before the wait, its first loads go out
-  // before these copies (measured: 70B-shaped step +0.9%, 3B +1.5%; queued
-  // behind the copies the loads came back 1-2 us later).
+  // before these copies (measured against the copies first: 70B-shaped step
+  // +0.9%, 3B +1.5%).
   auto issue_first = [&]() {
     if constexpr (!ZC) {
       if (items > 0) prow_setup(0);
