@@ -5,8 +5,9 @@ layer), replayed from a CUDA graph.  The stack (several GB) is far larger
 than the 129 MB L2, so no flush is needed between steps.  The headline is
 the 70B-shaped outlier-aware INT4 stack (80 layers, 35.3 GB, the largest
 configuration on one GPU); the line also carries one sub-result per other
-configuration (Gemma-2-9B INT8, Llama-3.2-3B INT4, 7B INT4 at batch 1/4/16/64,
-the 256 x 256 INT8 check) under "workloads".
+configuration (Gemma-2-9B INT8 at batch 1/16, Llama-3.2-3B INT4, 7B INT4 at
+batch 1/4/16/64, 7B and 70B INT8, the 256 x 256 INT8 check, the Gemma INT8
+stack paged from pinned host memory) under "workloads".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--no-sub] [--head] [--paged] [--tiered]
